@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused ZeRO flat-parameter step on GB300.
+
+One "step" is one pass of the whole hot path over one batch of gradients:
+reduce_grads (registration of the N replica gradients) -> zero_step (the fused
+rank-order fp32 reduce, Adam, bf16 cast) -> gather_weights (ZeRO-3 per-unit
+copies; nothing to do for stages 0-2) -> post_step.
+
+Default workload: Llama-style model, hidden 1024, intermediate 2048, 16/4
+heads, 8 layers, vocab 1024 (73,417,728 params) flattened into one
+FlatParameter, N = 8 simulated ranks, ZeRO-2, bf16 gradients ~N(0, 1e-3),
+fp32 Adam.  Every step moves (2N + 26) B/param = 3.08 GB, well above the
+129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host instead (a bounded sample of the same workload).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused ZeRO step params/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# Workloads.
+# ---------------------------------------------------------------------------
+def workload(name: str):
+    import synth_inputs as si
+    if name == "llama1024_zero2_n8":
+        return dict(pl=si.llama_1024(), n=8, stage=2, grad_dtype="bf16", grad_std=1e-3, per_unit=False,
+                    outliers=0.0)
+    if name == "llama2048_zero3_n8":
+        return dict(pl=si.llama_2048_units(), n=8, stage=3, grad_dtype="bf16", grad_std=1e-3, per_unit=True,
+                    outliers=0.0)
+    if name == "stage_buffer_zero1_fp32_n2":
+        return dict(pl=si.llama_2048_stage_buffer(), n=2, stage=1, grad_dtype="fp32", grad_std=1e-3,
+                    per_unit=False, outliers=0.0)
+    if name == "toy_mlp_n4":
+        return dict(pl=si.toy_mlp(), n=4, stage=2, grad_dtype="bf16", grad_std=1e-2, per_unit=True, outliers=0.0)
+    if name.startswith("flat:"):
+        _, numel, n = name.split(":")
+        return dict(pl=si.single_buffer(int(float(numel))), n=int(n), stage=2, grad_dtype="bf16", grad_std=1e-2,
+                    per_unit=False, outliers=0.001)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def bytes_per_param(n: int, grad_dtype: str) -> int:
+    """Algorithmic bytes per (padded) element of one fused step: N replica
+    gradient reads + master/m/v read (12) + master/m/v write (12) + bf16 write (2)."""
+    return (2 if grad_dtype == "bf16" else 4) * n + 26
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for rel in ("zero_sharded_mixed_flatparameter_gb300/csrc/zero_kernels.cu",
+                "zero_sharded_mixed_flatparameter_gb300/csrc/zero_internal.h"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch of the step kernel from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "step_kernel_dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_source_sha()
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        fields = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if fields.get("workload") == workload_name and fields.get("kernel_sha") == sha:
+            return float(fields["dram_bytes_per_launch"])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region.
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        loaded = [s for s, p in zip(sm, power) if p is not None] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (replicas only: ranks run independent copies).
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(values, op: str, world: int, device):
+    """max / sum of a list of floats over ranks (identity at world 1)."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return t.tolist()
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample of the workload.
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """The oracle's literal per-rank ZeRO step on a contiguous window of the
+    workload: one unit of ``sample_params`` elements with the workload's N,
+    stage, gradient dtype and value distributions (inputs drawn once)."""
+
+    def __init__(self, wl, sample_params: int, seed: int = 7):
+        import oracle
+        import synth_inputs as si
+        self.oracle = oracle
+        self.n, self.stage, gd = wl["n"], max(wl["stage"], 1), wl["grad_dtype"]
+        self.sample_params = sample_params
+        self.lay = oracle.layout([sample_params], [0], self.n, self.stage)
+        init = si.normal_fp32(sample_params, 0.02, seed).numpy()
+        self.state = oracle.make_master([sample_params], self.lay, [init])
+        self.grads = [si.as_numpy_bits(t) for t in
+                      si.replica_grads(self.n, self.lay.total_padded, wl["grad_std"], seed + 1, gd,
+                                       outlier_fraction=wl["outliers"])]
+        self.hyper = oracle.Hyper(n_ranks=self.n, grad_dtype=gd)
+        self.t = 0
+
+    def step(self):
+        self.t += 1
+        master, m, v, p16 = self.state
+        self.oracle.zero_step(self.hyper, self.stage, self.t, self.lay, self.grads, master, m, v, p16)
+
+
+def cpu_baseline(wl, sample_params: int = 4_000_000, min_seconds: float = 10.0):
+    sample = OracleSample(wl, sample_params)
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        sample.step()
+        steps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    value = sample_params * steps / dt
+    return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "host_cores_total": os.cpu_count(),
+            "sample": (f"{steps} literal per-rank oracle steps on a contiguous {sample_params:,}-param window "
+                       f"of the workload (N={wl['n']}, {wl['grad_dtype']} grads), {dt:.1f} s single-threaded")}
+
+
+# ---------------------------------------------------------------------------
+# Our arm.
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import synth_inputs as si
+    from zero_sharded_mixed_flatparameter_gb300 import build_lib
+    from zero_sharded_mixed_flatparameter_gb300.runner import FlatStep
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    if rank == 0:
+        build_lib.build()
+    barrier(world)
+    wl = workload(args.workload)
+    pl, n = wl["pl"], wl["n"]
+
+    init_flat = si.normal_fp32(pl.total, 0.02, 1 + rank, device=device)
+    offs = [0]
+    for k in pl.numel:
+        offs.append(offs[-1] + k)
+    init = [init_flat[offs[p]:offs[p + 1]] for p in range(len(pl.numel))]
+    fs = FlatStep(pl.numel, pl.unit, stage=wl["stage"], n_ranks=n, grad_dtype=wl["grad_dtype"], init_params=init,
+                  device=device)
+    del init, init_flat
+    padded = fs.padded
+    grads = si.replica_grads(n, padded, wl["grad_std"], 100 + rank, wl["grad_dtype"], device=device,
+                             outlier_fraction=wl["outliers"])
+    units = [fs.layout(i) for i in range(fs.n_units)]
+    gather_bufs = []
+    if wl["stage"] == 3:
+        gather_bufs = [torch.empty(max(u[1], 1), dtype=torch.bfloat16, device=device) for u in units]
+    stream = torch.cuda.current_stream(device)
+
+    def one_step(ev_pair=None):
+        launches = 0
+        if wl["per_unit"]:
+            for i, (numel, pad, shard, base) in enumerate(units):
+                fs.reduce_grads(i, [g[base:base + pad] for g in grads])
+        else:
+            fs.reduce_grads(-1, grads)
+        if ev_pair is not None:
+            ev_pair[0].record(stream)
+        fs.step()
+        if ev_pair is not None:
+            ev_pair[1].record(stream)
+        launches += fs.last_launches()
+        for i, buf in enumerate(gather_bufs):
+            fs.gather_weights(i, buf)
+            launches += fs.last_launches()
+        fs.post_step()
+        return launches
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize(device)
+
+    # ---- device-resident timed region ----
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(device)
+        start.record(stream)
+        for k in range(args.steps):
+            launches += one_step(pairs[k])
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+    total_ms = start.elapsed_time(end)
+    step_kernel_ms = [a.elapsed_time(b) for a, b in pairs]
+    clock = clocks.summary()
+
+    total_ms_max, kern_ms_max = aggregate([total_ms, statistics.mean(step_kernel_ms)], "max", world, device)
+    params_all = aggregate([float(pl.total * args.steps)], "sum", world, device)[0]
+    value = params_all / (total_ms_max / 1e3)
+
+    bpp = bytes_per_param(n, wl["grad_dtype"])
+    bytes_per_launch = bpp * padded
+    achieved_gbs = bytes_per_launch / (kern_ms_max / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = recorded_traffic(args.workload)
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        host_grads = [g.to("cpu").pin_memory() for g in grads]
+        host_out = torch.empty(padded, dtype=torch.bfloat16).pin_memory()
+        for _ in range(min(args.warmup, 2)):
+            for hg, g in zip(host_grads, grads):
+                g.copy_(hg, non_blocking=True)
+            one_step()
+            host_out.copy_(fs.param16, non_blocking=True)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for _ in range(args.steps):
+            for hg, g in zip(host_grads, grads):
+                g.copy_(hg, non_blocking=True)
+            one_step()
+            host_out.copy_(fs.param16, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        e2e_ms = aggregate([e0.elapsed_time(e1)], "max", world, device)[0]
+        esz = 2 if wl["grad_dtype"] == "bf16" else 4
+        e2e = {"value": params_all / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": n * padded * esz, "d2h_bytes_per_step": padded * 2,
+               "ms_per_step": e2e_ms / args.steps}
+        del host_grads, host_out
+
+    fs.close()
+    del grads
+    torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; bf16/fp32 grads, fp32 state)",
+            "config": {"workload": args.workload, "model": pl.name, "params": pl.total, "padded_params": padded,
+                       "units": fs.n_units, "n_ranks_simulated": n, "zero_stage": wl["stage"],
+                       "grad_dtype": wl["grad_dtype"], "optimizer": "Adam fp32 (lr 1e-3, betas 0.9/0.999, eps 1e-8)",
+                       "parallelism": f"{world} GPU replica(s); N={n} DP ranks simulated per GPU",
+                       "l2": f"inputs larger than L2: {bytes_per_launch / 1e9:.2f} GB moved per step (L2 129 MB)"},
+            "hbm_gbs": achieved_gbs, "hbm_frac_of_peak": achieved_gbs / peak,
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": achieved_gbs / peak, "peak_source": f"hbm_gbs {peak_kind}",
+                         "traffic": traffic, "algorithmic_bytes_per_launch": bytes_per_launch,
+                         "bytes_per_param": bpp, "kernel": "step_vec_kernel",
+                         "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms)},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clock,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the CPU oracle on the host cores.
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wl = workload(args.workload)
+    sample_params = 2_000_000
+    sample = OracleSample(wl, sample_params)
+    for _ in range(args.warmup):
+        sample.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sample.step()
+    dt = time.perf_counter() - t0
+    value = sample_params * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "model": wl["pl"].name, "params": wl["pl"].total,
+                   "n_ranks_simulated": wl["n"], "zero_stage": wl["stage"], "grad_dtype": wl["grad_dtype"]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step: one literal per-rank oracle step on a contiguous {sample_params:,}-param "
+                                   f"window of the workload (N={wl['n']}, {wl['grad_dtype']} grads), single-threaded"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama1024_zero2_n8")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

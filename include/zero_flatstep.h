@@ -1,0 +1,243 @@
+/*
+ * zero_flatstep.h — C ABI of the GB300 (sm_103a) ZeRO-1/2/3 optimizer step
+ * over a flattened, padded 1-D FlatParameter, with N data-parallel replicas
+ * simulated on one GPU.
+ *
+ * The calls follow the ShardingStrategy protocol of Femtotron dev log #6
+ * ("ZeRO-1 and ZeRO-2: abstraction design", section "ShardingStrategy as a
+ * first-class abstraction"): make_master / reduce_grads / gather_weights /
+ * post_step are the four points where ZeRO enters a training step, with the
+ * optimizer step between reduce_grads and gather_weights.  Plain data
+ * parallelism (stage 0, "NoShard") runs through the same calls.
+ *
+ * Conventions for every call:
+ *  - Plain pointers and sizes only.  "dev" pointers are CUDA device memory
+ *    owned by the caller; the library never allocates, frees or retains
+ *    device memory, and holds only host-side metadata in a zero_ctx.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Device work is enqueued on it asynchronously; the caller keeps
+ *    every buffer alive until that work has completed on the stream.
+ *  - Every call returns a zero_status; nothing crosses the ABI as an
+ *    exception.  A call that fails leaves the context unchanged.  The text of
+ *    the last error is available from zero_last_error().
+ *  - A context is not thread-safe: calls on one context must not overlap.
+ */
+#ifndef ZERO_FLATSTEP_H
+#define ZERO_FLATSTEP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum zero_status {
+  ZERO_OK = 0,
+  ZERO_EINVAL = 1,   /* invalid argument (null/misaligned pointer, bad size, bad config) */
+  ZERO_ENOMEM = 2,   /* host allocation of metadata failed */
+  ZERO_ECUDA = 3,    /* a CUDA runtime call or kernel launch failed */
+  ZERO_ESTATE = 4,   /* call not allowed in the context's current state */
+  ZERO_ENOTSUP = 5   /* valid request this build does not support */
+} zero_status;
+
+typedef enum zero_grad_dtype {
+  ZERO_GRAD_BF16 = 0,  /* replica gradients are bf16 (2 bytes/element) */
+  ZERO_GRAD_FP32 = 1   /* replica gradients are fp32 (fp32 gradient accumulation) */
+} zero_grad_dtype;
+
+/*
+ * Optimizer and sharding configuration.
+ *  stage       0 = plain data parallelism (no sharding, no padding), 1 = ZeRO-1
+ *              (optimizer state sharded), 2 = ZeRO-2 (+ gradients), 3 = ZeRO-3
+ *              (+ parameters) — CMU 15-779 Lecture 13 notes §3.1-3.3.
+ *  n_ranks     N simulated data-parallel replicas, 1..16.
+ *  grad_dtype  zero_grad_dtype of the replica gradient buffers.
+ *  adamw       1 = decoupled weight decay (AdamW), 0 = Adam (weight_decay must be 0).
+ *  lr, beta1, beta2, eps, weight_decay: fp32 Adam hyper-parameters
+ *              (notes §2.1); beta1, beta2 in [0, 1), eps >= 0, lr finite.
+ */
+typedef struct zero_config {
+  int32_t stage;
+  int32_t n_ranks;
+  int32_t grad_dtype;
+  int32_t adamw;
+  float lr;
+  float beta1;
+  float beta2;
+  float eps;
+  float weight_decay;
+} zero_config;
+
+/*
+ * Caller-allocated device buffers, each of `padded_numel` elements (see
+ * zero_plan / zero_padded_numel) and 16-byte aligned:
+ *  master      fp32 master weights (the optimizer's copy, notes §2.2)
+ *  exp_avg     fp32 Adam first moment m
+ *  exp_avg_sq  fp32 Adam second moment v
+ *  param16     bf16 parameters.  Stages 0-2: the full compute copy every
+ *              replica holds after the all-gather.  Stage 3: the rank-major
+ *              shard storage (rank d's shard of unit i at base_i + d*shard_i),
+ *              which has the same byte layout.
+ */
+typedef struct zero_buffers {
+  float* master;
+  float* exp_avg;
+  float* exp_avg_sq;
+  void* param16;
+} zero_buffers;
+
+typedef struct zero_ctx zero_ctx;
+
+/*
+ * zero_plan — FlatParameter layout only (host, no device work).
+ * Lecture notes §0.4 and §5.2: each unit's parameters are flattened and
+ * concatenated in caller order, right-padded with zeros to a multiple of the
+ * shard count F (N for stages 1-3, 1 for stage 0) and split into F equal
+ * shards; rank d owns shard d.  Femtotron dev log #6 ("master is sharded 1-D,
+ * not by shape").
+ *  param_numel[n_params]  element count of each parameter (>= 0)
+ *  param_unit[n_params]   unit (FlatParameter) id of each parameter; ids are
+ *                         nondecreasing and start at 0 (n_units = last id + 1;
+ *                         a skipped id is an empty unit)
+ *  out                    receives a context usable for layout / ledger queries;
+ *                         step calls on it return ZERO_ESTATE.
+ * Errors: ZERO_EINVAL for a bad config, negative sizes, decreasing unit ids or
+ * null pointers with n_params > 0; ZERO_ENOMEM.
+ */
+zero_status zero_plan(const zero_config* cfg, const int64_t* param_numel, const int32_t* param_unit,
+                      int32_t n_params, zero_ctx** out);
+
+/*
+ * zero_make_master — the protocol's make_master: plan the layout (as
+ * zero_plan), then build the fp32 master from the caller's fp32 parameters:
+ * copy parameter p (init_params[p], param_numel[p] fp32 device elements,
+ * 4-byte aligned) to its flat offset, zero every pad, zero m and v, write
+ * param16 = bf16(master) (round to nearest even) and set the step count t = 0.
+ * Enqueued on `stream`; init_params may be released once it completes.
+ * Errors: as zero_plan, plus ZERO_EINVAL for a null `bufs`, a null or
+ * non-16-byte-aligned buffer, a null init pointer for a non-empty parameter,
+ * or a pointer that is not device memory; ZERO_ECUDA on launch failure.
+ */
+zero_status zero_make_master(const zero_config* cfg, const int64_t* param_numel,
+                             const int32_t* param_unit, int32_t n_params,
+                             const float* const* init_params, const zero_buffers* bufs,
+                             void* stream, zero_ctx** out);
+
+/* Number of units; total padded and unpadded element counts. */
+zero_status zero_num_units(const zero_ctx* ctx, int32_t* n_units);
+zero_status zero_padded_numel(const zero_ctx* ctx, int64_t* padded, int64_t* numel);
+
+/*
+ * zero_layout — unit i's element count, padded count (multiple of F), shard
+ * length (padded / F) and flat base offset (sum of earlier padded counts).
+ * ZERO_EINVAL if unit is out of range.
+ */
+zero_status zero_layout(const zero_ctx* ctx, int32_t unit, int64_t* numel, int64_t* padded,
+                        int64_t* shard, int64_t* base);
+
+/* Flat offset of parameter p inside the padded buffer. */
+zero_status zero_param_offset(const zero_ctx* ctx, int32_t param, int64_t* offset);
+
+/*
+ * zero_state_bytes — per-rank model-state bytes of this layout under `stage`
+ * (lecture notes §2.3 and §9 item 2: bf16 params 2, bf16 grads 2, optimizer
+ * state K = 12 bytes per element; stage 1 shards K, stage 2 also the grads,
+ * stage 3 also the params): 16P, 4P + 12S, 2P + 14S, 16S with P the padded
+ * total and S the per-rank shard total.  per_rank_bytes has n_ranks entries.
+ */
+zero_status zero_state_bytes(const zero_ctx* ctx, int32_t stage, int64_t* per_rank_bytes);
+
+/*
+ * zero_stage3_peak_bytes — ZeRO-3 model-state peak of one rank during
+ * backward (lecture notes §3.5 and §11 Exercise 5): resident shards, plus the
+ * grad shards of units already reduce-scattered, plus the full bf16 params and
+ * grads of the unit being processed (units processed last to first).
+ * peak_unit receives the unit where the peak occurs (-1 if none).
+ */
+zero_status zero_stage3_peak_bytes(const zero_ctx* ctx, int64_t* peak_bytes, int32_t* peak_unit);
+
+/*
+ * zero_reduce_grads — the protocol's reduce_grads (Femtotron dev log #7, the
+ * ZeRO-2 post-accumulate-grad hook: flatten, zero-pad, reduce-scatter AVG).
+ * Registers the N replicas' gradients of one unit (unit >= 0: N pointers to
+ * padded_i elements each) or of the whole buffer (unit == -1: N pointers to
+ * padded_numel elements each).  Pad entries must be zero, as the hook's zero
+ * padding makes them.  The reduction itself — the rank-order fp32 sum scaled
+ * by 1/N, the local stand-in for reduce-scatter — is fused into zero_step, so
+ * this call does no device work; the buffers must stay valid and unchanged
+ * until the zero_step that consumes them has completed on its stream.
+ * Registering a unit again replaces its pointers.
+ * Errors: ZERO_EINVAL (unit out of range, null pointer, pointer not aligned to
+ * the element size); ZERO_ESTATE if no buffers are bound or a step is pending
+ * its post_step.
+ */
+zero_status zero_reduce_grads(zero_ctx* ctx, int32_t unit, const void* const* replica_grads,
+                              void* stream);
+
+/*
+ * zero_step — one optimizer step, t <- t + 1, in one fused pass over the
+ * padded flat buffer (lecture notes §2.1-§3.3; Femtotron dev logs #4/#5 step
+ * order).  For every element j of every rank's shard:
+ *   g  = ((G_0[j] + G_1[j]) + ... + G_{N-1}[j]) * (1/N)      fp32, rank order
+ *   w  = w * (1 - lr*wd)                                      AdamW only
+ *   m  = beta1*m + (1-beta1)*g;  v = beta2*v + (1-beta2)*g*g
+ *   w  = w - lr * ((m / (1-beta1^t)) / (sqrt(v / (1-beta2^t)) + eps))
+ *   param16[j] = bf16_rne(w)     (the all-gather's stand-in for stages 0-2)
+ * Every operation is a separately rounded IEEE fp32 operation (no FMA
+ * contraction, IEEE division and square root).  Requires every unit's
+ * gradients registered since the last post_step.
+ * Errors: ZERO_ESTATE (no buffers, missing gradients, step already taken
+ * without post_step); ZERO_ECUDA (launch failure; t is left unchanged).
+ */
+zero_status zero_step(zero_ctx* ctx, void* stream);
+
+/*
+ * zero_gather_weights — the protocol's gather_weights.  Stage 3 (ZeRO-3
+ * unshard, lecture notes §3.3 and §5.1): copy unit `unit`'s N bf16 shards, in
+ * rank order, into `unit_buf` (padded_i bf16 elements, device, 2-byte
+ * aligned); unit == -1 copies the whole padded buffer.  Stages 0-2: the fused
+ * step has already written every replica's full bf16 copy, so this returns
+ * ZERO_OK without device work (unit_buf may be NULL).
+ * Errors: ZERO_EINVAL (unit out of range, null/misaligned unit_buf at stage 3);
+ * ZERO_ESTATE (no buffers bound); ZERO_ECUDA.
+ */
+zero_status zero_gather_weights(zero_ctx* ctx, int32_t unit, void* unit_buf, void* stream);
+
+/*
+ * zero_post_step — the protocol's post_step: forget the registered gradients
+ * so the next step needs fresh ones.  ZERO_ESTATE unless a step was taken
+ * since the last post_step.  No device work.
+ */
+zero_status zero_post_step(zero_ctx* ctx, void* stream);
+
+/* Number of steps taken (t). */
+zero_status zero_step_count(const zero_ctx* ctx, int64_t* t);
+
+/*
+ * Number of kernels the last zero_step / zero_gather_weights call on this
+ * context enqueued (0 when it had nothing to do).  Host bookkeeping only.
+ */
+zero_status zero_last_launches(const zero_ctx* ctx, int32_t* launches);
+
+/* Set the learning rate used by later steps (a scheduler's lr update). */
+zero_status zero_set_lr(zero_ctx* ctx, float lr);
+
+/* Release the context's host metadata.  Device buffers stay the caller's. */
+zero_status zero_destroy(zero_ctx* ctx);
+
+/*
+ * Text of the last error on `ctx`; with ctx == NULL, the last error of a
+ * failed zero_plan / zero_make_master on the calling thread.  The string is
+ * owned by the library and valid until the next call on the same context
+ * (or thread).
+ */
+const char* zero_last_error(const zero_ctx* ctx);
+
+/* Constant name of a status code. */
+const char* zero_status_string(zero_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_FLATSTEP_H */

@@ -1,0 +1,70 @@
+// Internal interface between the host runtime (zero_runtime.cpp) and the
+// sm_103a kernels (zero_kernels.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace zfs {
+
+constexpr int kMaxRanks = 16;     // N simulated data-parallel replicas
+constexpr int kMaxSegs = 48;      // gradient segments per step launch
+constexpr int kVec = 8;           // elements per thread-iteration (16 B of bf16)
+constexpr int kStepThreads = 256; // threads per CTA of the step kernels
+
+// A run of consecutive flat elements whose N replica gradients are
+// contiguous buffers: element base + k reads g[r][k].
+struct Seg {
+  long long base;        // flat element offset
+  long long len;         // elements
+  long long vec_start;   // index of this segment's first vector in the
+                         // concatenated vector space of the launch
+  const void* g[kMaxRanks];
+};
+
+// Everything one step launch needs, passed by value as a __grid_constant__
+// kernel parameter (no device-side tables, nothing to allocate).
+struct StepArgs {
+  float* master;
+  float* m;
+  float* v;
+  uint16_t* p16;         // bf16 bit patterns
+  float inv_n;           // 1 / N
+  float lr;
+  float beta1;
+  float beta2;
+  float omb1;            // 1 - beta1
+  float omb2;            // 1 - beta2
+  float eps;
+  float bc1;             // 1 - beta1^t
+  float bc2;             // 1 - beta2^t
+  float decay;           // 1 - lr * wd  (exactly 1 for plain Adam)
+  int n_ranks;
+  int grad_fp32;         // 0 = bf16 grads, 1 = fp32 grads
+  int nseg;
+  long long total_vec;   // vectors over all segments (vector kernel)
+  long long total_elems; // elements over all segments (scalar kernel)
+  Seg seg[kMaxSegs];
+};
+
+// Launchers.  Each returns the cudaError_t of its launch.
+// Vector kernel: every segment has base % kVec == 0 and 16-byte aligned
+// gradient pointers; the last kVec-1 elements of a segment may be ragged.
+cudaError_t launch_step_vec(const StepArgs& a, cudaStream_t stream);
+// Scalar kernel: any alignment (used for segments the vector kernel cannot take).
+cudaError_t launch_step_scalar(const StepArgs& a, cudaStream_t stream);
+
+// make_master pieces.
+cudaError_t launch_zero_fill(float* master, float* m, float* v, uint16_t* p16, long long n,
+                             cudaStream_t stream);
+cudaError_t launch_copy_param(const float* src, float* master, uint16_t* p16, long long offset,
+                              long long n, cudaStream_t stream);
+
+// ZeRO-3 unit gather: copy n bf16 elements; *launches counts the kernels enqueued.
+cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaStream_t stream, int* launches);
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
+
+}  // namespace zfs

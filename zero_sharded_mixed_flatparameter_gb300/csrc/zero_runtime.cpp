@@ -1,0 +1,563 @@
+// Host runtime of the ZeRO flat-parameter library: the C ABI declared in
+// include/zero_flatstep.h.  It owns only host metadata — the FlatParameter
+// layout, the registered gradient pointers, the step count and error text —
+// and enqueues the sm_103a kernels of zero_kernels.cu on the caller's stream.
+//
+// Protocol: Femtotron dev log #6 (ShardingStrategy: make_master /
+// reduce_grads / gather_weights / post_step).  Layout: CMU 15-779 Lecture 13
+// notes §0.4 and §5.2 (flatten, concatenate, right-pad to a multiple of F,
+// split evenly).  Ledger: same notes §2.3, §3.5, §9 item 2, §11 Exercise 5.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "zero_flatstep.h"
+#include "zero_internal.h"
+
+namespace {
+
+thread_local std::string g_thread_error;
+
+enum class Phase { kPlanned, kReady, kStepped };
+
+}  // namespace
+
+struct zero_ctx {
+  zero_config cfg{};
+  int32_t n_units = 0;
+  int32_t n_params = 0;
+  int64_t shards = 1;  // F
+  std::vector<int64_t> unit_numel, unit_padded, unit_shard, unit_base, param_offset;
+  int64_t padded_total = 0;
+  int64_t numel_total = 0;
+
+  Phase phase = Phase::kPlanned;
+  zero_buffers bufs{};
+  int device = -1;
+  int64_t t = 0;
+  int32_t last_launches = 0;
+
+  // Registered replica gradient pointers, n_units x kMaxRanks.
+  std::vector<const void*> grads;
+  std::vector<uint8_t> registered;
+
+  std::string error;
+};
+
+namespace {
+
+zero_status fail(zero_ctx* ctx, zero_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (ctx) {
+    ctx->error = buf;
+  } else {
+    g_thread_error = buf;
+  }
+  return st;
+}
+
+zero_status fail_cuda(zero_ctx* ctx, const char* what, cudaError_t e) {
+  return fail(ctx, ZERO_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t grad_bytes(const zero_config& c) { return c.grad_dtype == ZERO_GRAD_FP32 ? 4 : 2; }
+
+zero_status check_config(const zero_config* cfg, zero_ctx* errctx) {
+  if (!cfg) return fail(errctx, ZERO_EINVAL, "config is NULL");
+  if (cfg->stage < 0 || cfg->stage > 3) return fail(errctx, ZERO_EINVAL, "stage %d not in 0..3", cfg->stage);
+  if (cfg->n_ranks < 1 || cfg->n_ranks > zfs::kMaxRanks)
+    return fail(errctx, ZERO_EINVAL, "n_ranks %d not in 1..%d", cfg->n_ranks, zfs::kMaxRanks);
+  if (cfg->grad_dtype != ZERO_GRAD_BF16 && cfg->grad_dtype != ZERO_GRAD_FP32)
+    return fail(errctx, ZERO_EINVAL, "grad_dtype %d is neither bf16 (0) nor fp32 (1)", cfg->grad_dtype);
+  if (cfg->adamw != 0 && cfg->adamw != 1) return fail(errctx, ZERO_EINVAL, "adamw must be 0 or 1");
+  if (!std::isfinite(cfg->lr)) return fail(errctx, ZERO_EINVAL, "lr is not finite");
+  if (!(cfg->beta1 >= 0.0f && cfg->beta1 < 1.0f)) return fail(errctx, ZERO_EINVAL, "beta1 not in [0, 1)");
+  if (!(cfg->beta2 >= 0.0f && cfg->beta2 < 1.0f)) return fail(errctx, ZERO_EINVAL, "beta2 not in [0, 1)");
+  if (!(cfg->eps >= 0.0f) || !std::isfinite(cfg->eps)) return fail(errctx, ZERO_EINVAL, "eps must be finite and >= 0");
+  if (!std::isfinite(cfg->weight_decay) || cfg->weight_decay < 0.0f)
+    return fail(errctx, ZERO_EINVAL, "weight_decay must be finite and >= 0");
+  if (!cfg->adamw && cfg->weight_decay != 0.0f)
+    return fail(errctx, ZERO_EINVAL, "weight_decay needs adamw = 1 (only decoupled decay is provided)");
+  return ZERO_OK;
+}
+
+// FlatParameter layout: per unit, numel = sum of its params; padded = the
+// smallest multiple of F not below numel; shard = padded / F; base = running
+// sum of padded sizes.  Params sit back to back in caller order.
+zero_status plan_layout(zero_ctx* ctx, const int64_t* param_numel, const int32_t* param_unit, int32_t n_params) {
+  if (n_params < 0) return fail(nullptr, ZERO_EINVAL, "n_params is negative");
+  if (n_params > 0 && (!param_numel || !param_unit))
+    return fail(nullptr, ZERO_EINVAL, "param_numel / param_unit is NULL");
+  int32_t last = 0;
+  for (int32_t p = 0; p < n_params; ++p) {
+    if (param_numel[p] < 0) return fail(nullptr, ZERO_EINVAL, "param %d has negative numel", p);
+    if (param_unit[p] < last) return fail(nullptr, ZERO_EINVAL, "param_unit decreases at param %d", p);
+    last = param_unit[p];
+  }
+  if (n_params > 0 && param_unit[0] < 0) return fail(nullptr, ZERO_EINVAL, "param_unit is negative");
+  const int32_t n_units = n_params > 0 ? param_unit[n_params - 1] + 1 : 0;
+  const int64_t F = ctx->cfg.stage == 0 ? 1 : ctx->cfg.n_ranks;
+  ctx->shards = F;
+  ctx->n_units = n_units;
+  ctx->n_params = n_params;
+  ctx->unit_numel.assign(n_units, 0);
+  ctx->unit_padded.assign(n_units, 0);
+  ctx->unit_shard.assign(n_units, 0);
+  ctx->unit_base.assign(n_units, 0);
+  ctx->param_offset.assign(n_params, 0);
+  for (int32_t p = 0; p < n_params; ++p) {
+    const int64_t before = ctx->unit_numel[param_unit[p]];
+    if (before > INT64_MAX / 4 - param_numel[p]) return fail(nullptr, ZERO_EINVAL, "parameter sizes overflow");
+    ctx->unit_numel[param_unit[p]] = before + param_numel[p];
+  }
+  int64_t base = 0, numel = 0;
+  for (int32_t i = 0; i < n_units; ++i) {
+    const int64_t rem = ctx->unit_numel[i] % F;
+    ctx->unit_padded[i] = ctx->unit_numel[i] + (rem ? F - rem : 0);
+    ctx->unit_shard[i] = ctx->unit_padded[i] / F;
+    ctx->unit_base[i] = base;
+    if (base > INT64_MAX / 16 - ctx->unit_padded[i]) return fail(nullptr, ZERO_EINVAL, "parameter sizes overflow");
+    base += ctx->unit_padded[i];
+    numel += ctx->unit_numel[i];
+  }
+  ctx->padded_total = base;
+  ctx->numel_total = numel;
+  int32_t cur = -1;
+  int64_t cursor = 0;
+  for (int32_t p = 0; p < n_params; ++p) {
+    if (param_unit[p] != cur) {
+      cur = param_unit[p];
+      cursor = ctx->unit_base[cur];
+    }
+    ctx->param_offset[p] = cursor;
+    cursor += param_numel[p];
+  }
+  ctx->grads.assign(static_cast<size_t>(n_units) * zfs::kMaxRanks, nullptr);
+  ctx->registered.assign(n_units, 0);
+  return ZERO_OK;
+}
+
+bool is_device_pointer(const void* p, int* device) {
+  cudaPointerAttributes attr{};
+  const cudaError_t e = cudaPointerGetAttributes(&attr, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error state of this query
+    return false;
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return false;
+  if (device) *device = attr.device;
+  return true;
+}
+
+zero_status check_current_device(zero_ctx* ctx) {
+  int dev = -1;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(ctx, "cudaGetDevice", e);
+  if (dev != ctx->device)
+    return fail(ctx, ZERO_ESTATE, "current device %d is not the context's device %d", dev, ctx->device);
+  return ZERO_OK;
+}
+
+zero_status require_bound(zero_ctx* ctx) {
+  if (ctx->phase == Phase::kPlanned) return fail(ctx, ZERO_ESTATE, "no buffers bound (context from zero_plan)");
+  return check_current_device(ctx);
+}
+
+// Scalars of step t, each from its definition (evaluated in double where the
+// definition has a power or a product of hyper-parameters, rounded once).
+void fill_scalars(const zero_ctx* ctx, int64_t t, zfs::StepArgs* a) {
+  const zero_config& c = ctx->cfg;
+  a->inv_n = 1.0f / static_cast<float>(c.n_ranks);
+  a->lr = c.lr;
+  a->beta1 = c.beta1;
+  a->beta2 = c.beta2;
+  a->omb1 = 1.0f - c.beta1;
+  a->omb2 = 1.0f - c.beta2;
+  a->eps = c.eps;
+  a->bc1 = static_cast<float>(1.0 - std::pow(static_cast<double>(c.beta1), static_cast<double>(t)));
+  a->bc2 = static_cast<float>(1.0 - std::pow(static_cast<double>(c.beta2), static_cast<double>(t)));
+  a->decay = c.adamw ? static_cast<float>(1.0 - static_cast<double>(c.lr) * static_cast<double>(c.weight_decay))
+                     : 1.0f;
+  a->n_ranks = c.n_ranks;
+  a->grad_fp32 = c.grad_dtype == ZERO_GRAD_FP32 ? 1 : 0;
+}
+
+struct PlannedSeg {
+  int64_t base, len;
+  const void* g[zfs::kMaxRanks];
+};
+
+// One segment per non-empty unit, merged with the previous one when every
+// replica's buffer continues exactly where the previous unit's ended (a
+// whole-buffer registration becomes a single segment).
+std::vector<PlannedSeg> build_segments(const zero_ctx* ctx) {
+  const int N = ctx->cfg.n_ranks;
+  const size_t esz = grad_bytes(ctx->cfg);
+  std::vector<PlannedSeg> out;
+  for (int32_t i = 0; i < ctx->n_units; ++i) {
+    if (ctx->unit_padded[i] == 0) continue;
+    const void* const* g = &ctx->grads[static_cast<size_t>(i) * zfs::kMaxRanks];
+    if (!out.empty()) {
+      PlannedSeg& prev = out.back();
+      bool contiguous = prev.base + prev.len == ctx->unit_base[i];
+      for (int r = 0; r < N && contiguous; ++r) {
+        contiguous = static_cast<const char*>(prev.g[r]) + prev.len * esz == static_cast<const char*>(g[r]);
+      }
+      if (contiguous) {
+        prev.len += ctx->unit_padded[i];
+        continue;
+      }
+    }
+    PlannedSeg s{};
+    s.base = ctx->unit_base[i];
+    s.len = ctx->unit_padded[i];
+    for (int r = 0; r < N; ++r) s.g[r] = g[r];
+    out.push_back(s);
+  }
+  return out;
+}
+
+bool vector_ok(const PlannedSeg& s, int N) {
+  if (s.base % zfs::kVec != 0) return false;
+  for (int r = 0; r < N; ++r)
+    if (!aligned(s.g[r], 16)) return false;
+  return true;
+}
+
+// Launch one kernel per batch of up to kMaxSegs segments of one kind.
+zero_status launch_batches(zero_ctx* ctx, const std::vector<PlannedSeg>& segs, bool vec, int64_t t,
+                           cudaStream_t stream, int32_t* launches) {
+  const int N = ctx->cfg.n_ranks;
+  size_t i = 0;
+  while (i < segs.size()) {
+    zfs::StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.master = ctx->bufs.master;
+    a.m = ctx->bufs.exp_avg;
+    a.v = ctx->bufs.exp_avg_sq;
+    a.p16 = static_cast<uint16_t*>(ctx->bufs.param16);
+    fill_scalars(ctx, t, &a);
+    long long vecs = 0, elems = 0;
+    int n = 0;
+    for (; i < segs.size() && n < zfs::kMaxSegs; ++i, ++n) {
+      zfs::Seg& s = a.seg[n];
+      s.base = segs[i].base;
+      s.len = segs[i].len;
+      s.vec_start = vecs;
+      for (int r = 0; r < N; ++r) s.g[r] = segs[i].g[r];
+      vecs += s.len / zfs::kVec;
+      elems += s.len;
+    }
+    a.nseg = n;
+    a.total_vec = vecs;
+    a.total_elems = elems;
+    const cudaError_t e = vec ? zfs::launch_step_vec(a, stream) : zfs::launch_step_scalar(a, stream);
+    if (e != cudaSuccess) return fail_cuda(ctx, "step kernel launch", e);
+    ++*launches;
+  }
+  return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+zero_status zero_plan(const zero_config* cfg, const int64_t* param_numel, const int32_t* param_unit,
+                      int32_t n_params, zero_ctx** out) {
+  if (!out) return fail(nullptr, ZERO_EINVAL, "out is NULL");
+  *out = nullptr;
+  zero_status st = check_config(cfg, nullptr);
+  if (st != ZERO_OK) return st;
+  zero_ctx* ctx = new (std::nothrow) zero_ctx;
+  if (!ctx) return fail(nullptr, ZERO_ENOMEM, "cannot allocate context");
+  ctx->cfg = *cfg;
+  try {
+    st = plan_layout(ctx, param_numel, param_unit, n_params);
+  } catch (const std::bad_alloc&) {
+    st = fail(nullptr, ZERO_ENOMEM, "cannot allocate layout tables");
+  }
+  if (st != ZERO_OK) {
+    delete ctx;
+    return st;
+  }
+  *out = ctx;
+  return ZERO_OK;
+}
+
+zero_status zero_make_master(const zero_config* cfg, const int64_t* param_numel, const int32_t* param_unit,
+                             int32_t n_params, const float* const* init_params, const zero_buffers* bufs,
+                             void* stream, zero_ctx** out) {
+  if (!out) return fail(nullptr, ZERO_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!bufs) return fail(nullptr, ZERO_EINVAL, "bufs is NULL");
+  zero_ctx* ctx = nullptr;
+  zero_status st = zero_plan(cfg, param_numel, param_unit, n_params, &ctx);
+  if (st != ZERO_OK) return st;
+  auto bail = [&](zero_status s) {
+    g_thread_error = ctx->error;
+    delete ctx;
+    return s;
+  };
+  const void* need[4] = {bufs->master, bufs->exp_avg, bufs->exp_avg_sq, bufs->param16};
+  const char* names[4] = {"master", "exp_avg", "exp_avg_sq", "param16"};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return bail(fail(ctx, ZERO_ECUDA, "no CUDA device"));
+  for (int k = 0; k < 4; ++k) {
+    if (!need[k]) return bail(fail(ctx, ZERO_EINVAL, "buffer %s is NULL", names[k]));
+    if (!aligned(need[k], 16)) return bail(fail(ctx, ZERO_EINVAL, "buffer %s is not 16-byte aligned", names[k]));
+    int pdev = -1;
+    if (!is_device_pointer(need[k], &pdev))
+      return bail(fail(ctx, ZERO_EINVAL, "buffer %s is not CUDA device memory", names[k]));
+    if (pdev != dev) return bail(fail(ctx, ZERO_EINVAL, "buffer %s is on device %d, current is %d", names[k], pdev, dev));
+  }
+  for (int32_t p = 0; p < n_params; ++p) {
+    if (param_numel[p] == 0) continue;
+    if (!init_params || !init_params[p]) return bail(fail(ctx, ZERO_EINVAL, "init param %d is NULL", p));
+    if (!aligned(init_params[p], 4)) return bail(fail(ctx, ZERO_EINVAL, "init param %d is not 4-byte aligned", p));
+    if (!is_device_pointer(init_params[p], nullptr))
+      return bail(fail(ctx, ZERO_EINVAL, "init param %d is not CUDA device memory", p));
+  }
+  ctx->bufs = *bufs;
+  ctx->device = dev;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint16_t* p16 = static_cast<uint16_t*>(bufs->param16);
+  cudaError_t e = zfs::launch_zero_fill(bufs->master, bufs->exp_avg, bufs->exp_avg_sq, p16, ctx->padded_total, s);
+  if (e != cudaSuccess) return bail(fail_cuda(ctx, "make_master zero fill", e));
+  for (int32_t p = 0; p < n_params; ++p) {
+    e = zfs::launch_copy_param(init_params ? init_params[p] : nullptr, bufs->master, p16, ctx->param_offset[p],
+                               param_numel[p], s);
+    if (e != cudaSuccess) return bail(fail_cuda(ctx, "make_master copy", e));
+  }
+  ctx->phase = Phase::kReady;
+  ctx->t = 0;
+  *out = ctx;
+  return ZERO_OK;
+}
+
+zero_status zero_num_units(const zero_ctx* ctx, int32_t* n_units) {
+  if (!ctx || !n_units) return fail(nullptr, ZERO_EINVAL, "NULL argument");
+  *n_units = ctx->n_units;
+  return ZERO_OK;
+}
+
+zero_status zero_padded_numel(const zero_ctx* ctx, int64_t* padded, int64_t* numel) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  if (padded) *padded = ctx->padded_total;
+  if (numel) *numel = ctx->numel_total;
+  return ZERO_OK;
+}
+
+zero_status zero_layout(const zero_ctx* ctx, int32_t unit, int64_t* numel, int64_t* padded, int64_t* shard,
+                        int64_t* base) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  zero_ctx* c = const_cast<zero_ctx*>(ctx);
+  if (unit < 0 || unit >= ctx->n_units) return fail(c, ZERO_EINVAL, "unit %d out of range [0, %d)", unit, ctx->n_units);
+  if (numel) *numel = ctx->unit_numel[unit];
+  if (padded) *padded = ctx->unit_padded[unit];
+  if (shard) *shard = ctx->unit_shard[unit];
+  if (base) *base = ctx->unit_base[unit];
+  return ZERO_OK;
+}
+
+zero_status zero_param_offset(const zero_ctx* ctx, int32_t param, int64_t* offset) {
+  if (!ctx || !offset) return fail(nullptr, ZERO_EINVAL, "NULL argument");
+  zero_ctx* c = const_cast<zero_ctx*>(ctx);
+  if (param < 0 || param >= ctx->n_params) return fail(c, ZERO_EINVAL, "param %d out of range", param);
+  *offset = ctx->param_offset[param];
+  return ZERO_OK;
+}
+
+zero_status zero_state_bytes(const zero_ctx* ctx, int32_t stage, int64_t* per_rank_bytes) {
+  if (!ctx || !per_rank_bytes) return fail(nullptr, ZERO_EINVAL, "NULL argument");
+  zero_ctx* c = const_cast<zero_ctx*>(ctx);
+  if (stage < 0 || stage > 3) return fail(c, ZERO_EINVAL, "stage %d not in 0..3", stage);
+  const int64_t N = ctx->cfg.n_ranks;
+  int64_t P = 0, S = 0;
+  for (int32_t i = 0; i < ctx->n_units; ++i) {
+    P += ctx->unit_padded[i];
+    S += ctx->unit_padded[i] / N;
+  }
+  int64_t bytes;
+  switch (stage) {
+    case 0: bytes = 16 * P; break;
+    case 1: bytes = 4 * P + 12 * S; break;
+    case 2: bytes = 2 * P + 14 * S; break;
+    default: bytes = 16 * S; break;
+  }
+  for (int64_t r = 0; r < N; ++r) per_rank_bytes[r] = bytes;
+  return ZERO_OK;
+}
+
+zero_status zero_stage3_peak_bytes(const zero_ctx* ctx, int64_t* peak_bytes, int32_t* peak_unit) {
+  if (!ctx || !peak_bytes) return fail(nullptr, ZERO_EINVAL, "NULL argument");
+  const int64_t N = ctx->cfg.n_ranks;
+  int64_t S = 0;
+  for (int32_t i = 0; i < ctx->n_units; ++i) S += ctx->unit_padded[i] / N;
+  const int64_t resident = 14 * S;  // bf16 param shard 2 + fp32 master/m/v 12
+  int64_t best = resident, reduced = 0;
+  int32_t where = -1;
+  for (int32_t k = ctx->n_units - 1; k >= 0; --k) {
+    const int64_t at = resident + reduced + 4 * ctx->unit_padded[k];
+    if (at > best) {
+      best = at;
+      where = k;
+    }
+    reduced += 2 * (ctx->unit_padded[k] / N);
+  }
+  *peak_bytes = best;
+  if (peak_unit) *peak_unit = where;
+  return ZERO_OK;
+}
+
+zero_status zero_reduce_grads(zero_ctx* ctx, int32_t unit, const void* const* replica_grads, void* stream) {
+  (void)stream;  // the reduction is fused into zero_step; nothing is enqueued here
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  zero_status st = require_bound(ctx);
+  if (st != ZERO_OK) return st;
+  if (ctx->phase == Phase::kStepped) return fail(ctx, ZERO_ESTATE, "reduce_grads after step: call post_step first");
+  if (unit < -1 || unit >= ctx->n_units) return fail(ctx, ZERO_EINVAL, "unit %d out of range", unit);
+  if (!replica_grads) return fail(ctx, ZERO_EINVAL, "replica_grads is NULL");
+  const int N = ctx->cfg.n_ranks;
+  const size_t esz = grad_bytes(ctx->cfg);
+  const int64_t len = unit < 0 ? ctx->padded_total : ctx->unit_padded[unit];
+  for (int r = 0; r < N; ++r) {
+    if (len > 0 && !replica_grads[r]) return fail(ctx, ZERO_EINVAL, "replica %d gradient is NULL", r);
+    if (!aligned(replica_grads[r], esz))
+      return fail(ctx, ZERO_EINVAL, "replica %d gradient is not %zu-byte aligned", r, esz);
+  }
+  if (unit >= 0) {
+    for (int r = 0; r < N; ++r) ctx->grads[static_cast<size_t>(unit) * zfs::kMaxRanks + r] = replica_grads[r];
+    ctx->registered[unit] = 1;
+  } else {
+    for (int32_t i = 0; i < ctx->n_units; ++i) {
+      for (int r = 0; r < N; ++r) {
+        const char* b = static_cast<const char*>(replica_grads[r]);
+        ctx->grads[static_cast<size_t>(i) * zfs::kMaxRanks + r] = b ? b + ctx->unit_base[i] * esz : nullptr;
+      }
+      ctx->registered[i] = 1;
+    }
+  }
+  return ZERO_OK;
+}
+
+zero_status zero_step(zero_ctx* ctx, void* stream) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  zero_status st = require_bound(ctx);
+  if (st != ZERO_OK) return st;
+  if (ctx->phase == Phase::kStepped) return fail(ctx, ZERO_ESTATE, "step already taken: call post_step first");
+  for (int32_t i = 0; i < ctx->n_units; ++i) {
+    if (!ctx->registered[i]) return fail(ctx, ZERO_ESTATE, "unit %d has no registered gradients", i);
+  }
+  const int64_t t = ctx->t + 1;
+  std::vector<PlannedSeg> vec_segs, scalar_segs;
+  try {
+    for (const PlannedSeg& s : build_segments(ctx)) {
+      (vector_ok(s, ctx->cfg.n_ranks) ? vec_segs : scalar_segs).push_back(s);
+    }
+  } catch (const std::bad_alloc&) {
+    return fail(ctx, ZERO_ENOMEM, "cannot allocate segment list");
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t launches = 0;
+  st = launch_batches(ctx, vec_segs, true, t, s, &launches);
+  if (st != ZERO_OK) return st;
+  st = launch_batches(ctx, scalar_segs, false, t, s, &launches);
+  if (st != ZERO_OK) return st;
+  ctx->last_launches = launches;
+  ctx->t = t;
+  ctx->phase = Phase::kStepped;
+  return ZERO_OK;
+}
+
+zero_status zero_gather_weights(zero_ctx* ctx, int32_t unit, void* unit_buf, void* stream) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  zero_status st = require_bound(ctx);
+  if (st != ZERO_OK) return st;
+  if (unit < -1 || unit >= ctx->n_units) return fail(ctx, ZERO_EINVAL, "unit %d out of range", unit);
+  if (ctx->cfg.stage != 3) {  // the fused step already wrote every replica's full copy
+    ctx->last_launches = 0;
+    return ZERO_OK;
+  }
+  const int64_t base = unit < 0 ? 0 : ctx->unit_base[unit];
+  const int64_t len = unit < 0 ? ctx->padded_total : ctx->unit_padded[unit];
+  if (len == 0) {
+    ctx->last_launches = 0;
+    return ZERO_OK;
+  }
+  if (!unit_buf) return fail(ctx, ZERO_EINVAL, "unit_buf is NULL");
+  if (!aligned(unit_buf, 2)) return fail(ctx, ZERO_EINVAL, "unit_buf is not 2-byte aligned");
+  const uint16_t* src = static_cast<const uint16_t*>(ctx->bufs.param16) + base;
+  int32_t launches = 0;
+  const cudaError_t e = zfs::launch_gather(src, static_cast<uint16_t*>(unit_buf), len,
+                                           static_cast<cudaStream_t>(stream), &launches);
+  if (e != cudaSuccess) return fail_cuda(ctx, "gather kernel launch", e);
+  ctx->last_launches = launches;
+  return ZERO_OK;
+}
+
+zero_status zero_post_step(zero_ctx* ctx, void* stream) {
+  (void)stream;
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  if (ctx->phase != Phase::kStepped) return fail(ctx, ZERO_ESTATE, "post_step without a step since the last post_step");
+  std::fill(ctx->registered.begin(), ctx->registered.end(), 0);
+  std::fill(ctx->grads.begin(), ctx->grads.end(), nullptr);
+  ctx->phase = Phase::kReady;
+  return ZERO_OK;
+}
+
+zero_status zero_step_count(const zero_ctx* ctx, int64_t* t) {
+  if (!ctx || !t) return fail(nullptr, ZERO_EINVAL, "NULL argument");
+  *t = ctx->t;
+  return ZERO_OK;
+}
+
+zero_status zero_last_launches(const zero_ctx* ctx, int32_t* launches) {
+  if (!ctx || !launches) return fail(nullptr, ZERO_EINVAL, "NULL argument");
+  *launches = ctx->last_launches;
+  return ZERO_OK;
+}
+
+zero_status zero_set_lr(zero_ctx* ctx, float lr) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  if (!std::isfinite(lr)) return fail(ctx, ZERO_EINVAL, "lr is not finite");
+  ctx->cfg.lr = lr;
+  return ZERO_OK;
+}
+
+zero_status zero_destroy(zero_ctx* ctx) {
+  delete ctx;
+  return ZERO_OK;
+}
+
+const char* zero_last_error(const zero_ctx* ctx) {
+  return ctx ? ctx->error.c_str() : g_thread_error.c_str();
+}
+
+const char* zero_status_string(zero_status status) {
+  switch (status) {
+    case ZERO_OK: return "ZERO_OK";
+    case ZERO_EINVAL: return "ZERO_EINVAL";
+    case ZERO_ENOMEM: return "ZERO_ENOMEM";
+    case ZERO_ECUDA: return "ZERO_ECUDA";
+    case ZERO_ESTATE: return "ZERO_ESTATE";
+    case ZERO_ENOTSUP: return "ZERO_ENOTSUP";
+  }
+  return "ZERO_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,148 @@
+"""Caller-side plumbing around the C ABI: torch allocates the flat buffers and
+owns the stream; every step of the path runs in the library's kernels.
+
+``FlatStep`` plans the FlatParameter layout, allocates master / m / v (fp32)
+and the bf16 parameter buffer of ``padded_numel`` elements on the device,
+builds the master with ``zero_make_master`` and then drives the protocol:
+``reduce_grads`` -> ``step`` -> ``gather_weights`` -> ``post_step``.
+"""
+
+from __future__ import annotations
+
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import binding as B
+
+
+class FlatStep:
+    def __init__(self, param_numel: Sequence[int], param_unit: Sequence[int], *, stage: int, n_ranks: int,
+                 grad_dtype: str = "bf16", lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999,
+                 eps: float = 1e-8, weight_decay: float = 0.0, adamw: bool = False,
+                 init_params: Sequence[torch.Tensor] = (), device: str | torch.device = "cuda",
+                 guard: int = 0, guard_value: float = float("nan")):
+        self.param_numel = [int(x) for x in param_numel]
+        self.param_unit = [int(x) for x in param_unit]
+        self.stage, self.n_ranks, self.grad_dtype = stage, n_ranks, grad_dtype
+        self.cfg = B.make_config(stage, n_ranks, grad_dtype, lr, beta1, beta2, eps, weight_decay, adamw)
+        self.device = torch.device(device)
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        plan = B.zero_plan(self.cfg, self.param_numel, self.param_unit)
+        try:
+            self.padded, self.numel = B.zero_padded_numel(plan)
+            self.n_units = B.zero_num_units(plan)
+        finally:
+            B.zero_destroy(plan)
+        # Optional guard regions around every buffer (canary checks in tests);
+        # a multiple of 8 elements keeps the interior 16-byte aligned.
+        assert guard % 8 == 0
+        self.guard = guard
+        n = self.padded + 2 * guard
+
+        def alloc(dtype):
+            t = torch.empty(max(n, 1), dtype=dtype, device=self.device)
+            t.fill_(guard_value)
+            return t
+
+        self._master, self._m, self._v = alloc(torch.float32), alloc(torch.float32), alloc(torch.float32)
+        self._p16 = alloc(torch.bfloat16)
+        if len(init_params) != len(self.param_numel):
+            raise ValueError("need one fp32 init tensor per parameter")
+        self._init = [p.contiguous() for p in init_params]
+        for p, k in zip(self._init, self.param_numel):
+            if p.dtype != torch.float32 or p.numel() != k:
+                raise ValueError("init params must be fp32 tensors of the declared sizes")
+        self.ctx = B.zero_make_master(self.cfg, self.param_numel, self.param_unit,
+                                      [p.data_ptr() for p in self._init],
+                                      self._ptr(self._master), self._ptr(self._m), self._ptr(self._v),
+                                      self._ptr(self._p16), self.stream_handle())
+        # make_master reads the init params on the stream; once it has run they
+        # may be released.
+        torch.cuda.current_stream(self.device).synchronize()
+        self._init = []
+        self._registered: List[List[torch.Tensor]] = []
+
+    # -- buffers ---------------------------------------------------------------
+    def _ptr(self, t: torch.Tensor) -> int:
+        return t.data_ptr() + self.guard * t.element_size()
+
+    def _view(self, t):
+        return t[self.guard:self.guard + self.padded]
+
+    @property
+    def master(self):
+        return self._view(self._master)
+
+    @property
+    def exp_avg(self):
+        return self._view(self._m)
+
+    @property
+    def exp_avg_sq(self):
+        return self._view(self._v)
+
+    @property
+    def param16(self):
+        return self._view(self._p16)
+
+    def guards(self):
+        """The guard regions of every buffer (must keep their fill value)."""
+        g = self.guard
+        out = []
+        for t in (self._master, self._m, self._v, self._p16):
+            out.append(t[:g])
+            out.append(t[g + self.padded:])
+        return out
+
+    def layout(self, unit: int):
+        return B.zero_layout(self.ctx, unit)
+
+    def param_offset(self, p: int) -> int:
+        return B.zero_param_offset(self.ctx, p)
+
+    @staticmethod
+    def stream_handle(stream: Optional[torch.cuda.Stream] = None) -> int:
+        s = stream if stream is not None else torch.cuda.current_stream()
+        return int(s.cuda_stream)
+
+    def grad_dtype_torch(self):
+        return torch.bfloat16 if self.grad_dtype == "bf16" else torch.float32
+
+    # -- protocol ----------------------------------------------------------------
+    def reduce_grads(self, unit: int, replica_grads: Sequence[torch.Tensor], stream=None) -> None:
+        want = self.grad_dtype_torch()
+        for g in replica_grads:
+            if g.dtype != want or not g.is_contiguous() or g.device != self.device:
+                raise ValueError("replica grads must be contiguous device tensors of the configured dtype")
+        B.zero_reduce_grads(self.ctx, unit, [g.data_ptr() for g in replica_grads], self.stream_handle(stream))
+        self._registered.append(list(replica_grads))  # keep alive until post_step
+
+    def step(self, stream=None) -> None:
+        B.zero_step(self.ctx, self.stream_handle(stream))
+
+    def gather_weights(self, unit: int, out: Optional[torch.Tensor], stream=None) -> None:
+        B.zero_gather_weights(self.ctx, unit, out.data_ptr() if out is not None else 0, self.stream_handle(stream))
+
+    def post_step(self, stream=None) -> None:
+        B.zero_post_step(self.ctx, self.stream_handle(stream))
+        self._registered.clear()
+
+    def step_count(self) -> int:
+        return B.zero_step_count(self.ctx)
+
+    def last_launches(self) -> int:
+        """Kernels enqueued by the last step / gather call."""
+        return B.zero_last_launches(self.ctx)
+
+    def close(self) -> None:
+        if getattr(self, "ctx", None):
+            B.zero_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass
