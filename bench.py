@@ -105,7 +105,9 @@ def recorded_traffic(workload_name: str):
 # Clock sampling during the timed region.
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 50 ms) of SM clock, power and throttle
+    reasons; summary() keeps the samples taken inside the timed window."""
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -113,21 +115,26 @@ class ClockSampler:
         self.device_index = device_index
         self.proc = None
         self.file = None
+        self.window = None
 
     def __enter__(self):
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            time.sleep(0.5)
         except Exception:
             self.proc = None
         return self
 
+    def mark(self, t_start: float, t_end: float):
+        self.window = (t_start, t_end)
+
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -137,32 +144,44 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or self.file is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        import datetime
         self.file.flush()
         rows = []
         with open(self.file.name) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) >= 9:
-                    rows.append(parts)
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        continue
+                    rows.append([ts] + parts[1:])
         os.unlink(self.file.name)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
 
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
-        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        inside = rows
+        if self.window and rows:
+            lo, hi = self.window
+            inside = [r for r in rows if lo - 0.05 <= r[0] <= hi + 0.05]
+        if not inside:
+            # the timed region was shorter than the sampling interval: take the
+            # sample nearest to its middle
+            if not rows:
+                return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            mid = sum(self.window) / 2 if self.window else rows[-1][0]
+            inside = [min(rows, key=lambda r: abs(r[0] - mid))]
+        sm = [num(r[1]) for r in inside if num(r[1]) is not None]
+        mx = [num(r[2]) for r in inside if num(r[2]) is not None]
+        power = [num(r[3]) for r in inside if num(r[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
-        loaded = [s for s, p in zip(sm, power) if p is not None] or sm
-        return {"sm_mhz": statistics.median(loaded) if loaded else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(power) if power else None,
-                "samples": len(rows), "reasons": reasons}
+        reasons = sorted({names[k] for r in inside for k in range(4) if str(r[5 + k]).lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_median": statistics.median(power) if power else None,
+                "samples_in_timed_region": len(inside), "reasons": reasons}
 
 
 # ---------------------------------------------------------------------------
@@ -295,8 +314,14 @@ def run_ours(args):
         fs.post_step()
         return launches
 
-    for _ in range(args.warmup):
+    # Warm-up: W steps, extended until at least 0.3 s of device work has run so
+    # that clocks have ramped before the timed region (the count is reported).
+    warm_done, t_warm = 0, time.perf_counter()
+    while warm_done < args.warmup or time.perf_counter() - t_warm < 0.3:
         one_step()
+        warm_done += 1
+        if warm_done % 16 == 0:
+            torch.cuda.synchronize(device)
     torch.cuda.synchronize(device)
 
     # ---- device-resident timed region ----
@@ -306,12 +331,15 @@ def run_ours(args):
     with ClockSampler(device.index if device.index is not None else 0) as clocks:
         barrier(world)
         torch.cuda.synchronize(device)
+        t_region0 = time.time()
         start.record(stream)
         for k in range(args.steps):
             launches += one_step(pairs[k])
         end.record(stream)
         torch.cuda.synchronize(device)
+        t_region1 = time.time()
         barrier(world)
+        clocks.mark(t_region0, t_region1)
     total_ms = start.elapsed_time(end)
     step_kernel_ms = [a.elapsed_time(b) for a, b in pairs]
     clock = clocks.summary()
@@ -367,7 +395,7 @@ def run_ours(args):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
+            "warmup": warm_done, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; bf16/fp32 grads, fp32 state)",
             "config": {"workload": args.workload, "model": pl.name, "params": pl.total, "padded_params": padded,
                        "units": fs.n_units, "n_ranks_simulated": n, "zero_stage": wl["stage"],
@@ -401,7 +429,14 @@ def run_reference(args):
     import oracle
     oracle.build()
     wl = workload(args.workload)
-    sample_params = 2_000_000
+    # Each step is a bounded sample: sized so that the K timed steps take about
+    # a minute on one core (at most 2M params per step).
+    probe = OracleSample(wl, 262_144)
+    t0 = time.perf_counter()
+    probe.step()
+    rate = 262_144 / max(time.perf_counter() - t0, 1e-6)
+    sample_params = int(min(2_000_000, max(65_536, rate * 60.0 / max(args.steps, 1))))
+    sample_params -= sample_params % 64
     sample = OracleSample(wl, sample_params)
     for _ in range(args.warmup):
         sample.step()
@@ -427,8 +462,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama1024_zero2_n8")
     ap.add_argument("--no-cpu-baseline", action="store_true")

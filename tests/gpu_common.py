@@ -47,7 +47,10 @@ def assert_rel_close(got: np.ndarray, want: np.ndarray, what: str, rtol: float =
     assert np.array_equal(nan_w, nan_g), f"{what}: NaN positions differ"
     ok = ~nan_w
     g64, w64 = got[ok].astype(np.float64), want[ok].astype(np.float64)
-    err = np.abs(g64 - w64)
+    with np.errstate(invalid="ignore"):
+        err = np.abs(g64 - w64)
+    # equal infinities have zero error
+    err = np.where(g64 == w64, 0.0, err)
     bad = err > rtol * np.abs(w64)
     if bad.any():
         i = int(np.flatnonzero(bad)[0])
@@ -76,6 +79,13 @@ def assert_bit_exact(got: np.ndarray, want: np.ndarray, what: str):
     assert ga.dtype.itemsize == wa.dtype.itemsize and ga.size == wa.size, f"{what}: shape/dtype mismatch"
     ui = np.uint32 if ga.dtype.itemsize == 4 else np.uint16
     differ = ga.view(ui) != wa.view(ui)
+    # NaN payloads are not fixed by IEEE arithmetic: a NaN matches any NaN
+    if ga.dtype.itemsize == 4:
+        both_nan = np.isnan(ga.view(np.float32)) & np.isnan(wa.view(np.float32))
+    else:
+        gi, wi = ga.view(np.uint16), wa.view(np.uint16)
+        both_nan = (((gi & 0x7F80) == 0x7F80) & ((gi & 0x7F) != 0) & ((wi & 0x7F80) == 0x7F80) & ((wi & 0x7F) != 0))
+    differ &= ~both_nan
     if differ.any():
         i = int(np.flatnonzero(differ)[0])
         raise AssertionError(f"{what}: {int(differ.sum())} elements differ bitwise; first at {i}: "

@@ -12,6 +12,7 @@ constexpr int kMaxRanks = 16;     // N simulated data-parallel replicas
 constexpr int kMaxSegs = 48;      // gradient segments per step launch
 constexpr int kVec = 8;           // elements per thread-iteration (16 B of bf16)
 constexpr int kStepThreads = 256; // threads per CTA of the step kernels
+constexpr int kStepCtasPerSm = 2; // resident CTAs per SM of the vector step kernel
 
 // A run of consecutive flat elements whose N replica gradients are
 // contiguous buffers: element base + k reads g[r][k].

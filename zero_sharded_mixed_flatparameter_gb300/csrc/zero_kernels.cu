@@ -153,8 +153,11 @@ __device__ __forceinline__ void step_vec8(const StepArgs& a, const Seg& s, long 
   st_stream(a.p16 + j, out);
 }
 
+// Minimum of one resident CTA in the bounds lets each thread keep all of its
+// 16-byte loads in flight before the first use (about 94 registers at N = 8);
+// the grid then caps residency at kStepCtasPerSm CTAs per SM (see launch_step_vec).
 template <int N, bool kFp32>
-__global__ void __launch_bounds__(kStepThreads) step_vec_kernel(const __grid_constant__ StepArgs a) {
+__global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_constant__ StepArgs a) {
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (int s = 0; s < a.nseg; ++s) {
@@ -322,8 +325,13 @@ cudaError_t launch_step_vec(const StepArgs& a, cudaStream_t stream) {
   if (!k) return cudaErrorInvalidValue;
   const int dev = current_device();
   const int sms = cached_sms(dev);
-  const int bps = resident_blocks(&g_info[dev].vec_blocks_per_sm[a.grad_fp32 ? 1 : 0][a.n_ranks],
-                                  reinterpret_cast<const void*>(k));
+  int bps = resident_blocks(&g_info[dev].vec_blocks_per_sm[a.grad_fp32 ? 1 : 0][a.n_ranks],
+                            reinterpret_cast<const void*>(k));
+  // 512 resident threads per SM: measured on GB300 to give the best DRAM
+  // efficiency across N = 1..16 (more threads widen the address window the
+  // grid streams through at once and lower row-buffer locality; fewer leave
+  // too few bytes in flight).
+  if (bps > kStepCtasPerSm) bps = kStepCtasPerSm;
   long long work = a.total_vec;
   if (work < static_cast<long long>(a.nseg) * kVec) work = static_cast<long long>(a.nseg) * kVec;
   const long long grid = grid_for(work, sms, bps);
