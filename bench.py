@@ -295,13 +295,20 @@ def run_ours(args):
         gather_bufs = [torch.empty(max(u[1], 1), dtype=torch.bfloat16, device=device) for u in units]
     stream = torch.cuda.current_stream(device)
 
-    def one_step(ev_pair=None):
+    def one_step(ev_pair=None, clip_pair=None):
         launches = 0
         if wl["per_unit"]:
             for i, (numel, pad, shard, base) in enumerate(units):
                 fs.reduce_grads(i, [g[base:base + pad] for g in grads])
         else:
             fs.reduce_grads(-1, grads)
+        if args.clip > 0:
+            if clip_pair is not None:
+                clip_pair[0].record(stream)
+            fs.clip_grad_norm(args.clip)
+            if clip_pair is not None:
+                clip_pair[1].record(stream)
+            launches += fs.last_launches()
         if ev_pair is not None:
             ev_pair[0].record(stream)
         fs.step()
@@ -326,6 +333,8 @@ def run_ours(args):
 
     # ---- device-resident timed region ----
     pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clip_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)] if args.clip > 0 else [None] * args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
     with ClockSampler(device.index if device.index is not None else 0) as clocks:
@@ -334,7 +343,7 @@ def run_ours(args):
         t_region0 = time.time()
         start.record(stream)
         for k in range(args.steps):
-            launches += one_step(pairs[k])
+            launches += one_step(pairs[k], clip_pairs[k])
         end.record(stream)
         torch.cuda.synchronize(device)
         t_region1 = time.time()
@@ -342,6 +351,7 @@ def run_ours(args):
         clocks.mark(t_region0, t_region1)
     total_ms = start.elapsed_time(end)
     step_kernel_ms = [a.elapsed_time(b) for a, b in pairs]
+    clip_ms = [a.elapsed_time(b) for a, b in clip_pairs] if args.clip > 0 else None
     clock = clocks.summary()
 
     total_ms_max, kern_ms_max = aggregate([total_ms, statistics.mean(step_kernel_ms)], "max", world, device)
@@ -408,6 +418,12 @@ def run_ours(args):
                          "traffic": traffic, "algorithmic_bytes_per_launch": bytes_per_launch,
                          "bytes_per_param": bpp, "kernel": "step_vec_kernel",
                          "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms)},
+            "clip": None if clip_ms is None else {
+                "max_norm": args.clip, "norm_pass_ms_mean": statistics.mean(clip_ms),
+                "norm_pass_bytes": (2 if wl["grad_dtype"] == "bf16" else 4) * n * padded,
+                "norm_pass_gbs": (2 if wl["grad_dtype"] == "bf16" else 4) * n * padded
+                / (statistics.mean(clip_ms) / 1e3) / 1e9,
+                "note": "the clipped step is the norm pass (grad_sq + finalize kernels) plus the step kernel"},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -468,6 +484,8 @@ def main():
     ap.add_argument("--workload", default="llama1024_zero2_n8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clip", type=float, default=0.0,
+                    help="global-norm clipping to this max norm before every step (0: off)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

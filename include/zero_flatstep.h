@@ -184,12 +184,51 @@ zero_status zero_reduce_grads(zero_ctx* ctx, int32_t unit, const void* const* re
  *   w  = w - lr * ((m / (1-beta1^t)) / (sqrt(v / (1-beta2^t)) + eps))
  *   param16[j] = bf16_rne(w)     (the all-gather's stand-in for stages 0-2)
  * Every operation is a separately rounded IEEE fp32 operation (no FMA
- * contraction, IEEE division and square root).  Requires every unit's
+ * contraction, IEEE division and square root).  After zero_clip_grad_norm,
+ * g is multiplied by the clip coefficient before Adam.  Requires every unit's
  * gradients registered since the last post_step.
  * Errors: ZERO_ESTATE (no buffers, missing gradients, step already taken
  * without post_step); ZERO_ECUDA (launch failure; t is left unchanged).
  */
 zero_status zero_step(zero_ctx* ctx, void* stream);
+
+/*
+ * zero_clip_workspace_bytes — size of the device workspace zero_clip_grad_norm
+ * needs for this layout: 32 bytes of header plus 8 bytes per norm chunk
+ * (every unit is cut into chunks of 16,384 elements).
+ */
+zero_status zero_clip_workspace_bytes(const zero_ctx* ctx, int64_t* bytes);
+
+/*
+ * zero_clip_grad_norm — global-norm gradient clipping, the ClipGradNorm
+ * transform Femtotron dev logs #4/#5 apply to the fp32 gradient before AdamW
+ * (the source guide's --clip-grad 1.0 / gradient_clipping 1.0).  On `stream`
+ * it computes the L2 norm of the reduced gradient g = (sum of the N
+ * registered replicas) / N over every element of every unit, and the
+ * coefficient c = min(1, max_norm / (norm + 1e-6)) rounded to fp32; the next
+ * zero_step multiplies every reduced gradient by c before Adam.  The squared
+ * norm is summed over fixed chunks of 16,384 elements of each unit (pads
+ * included, they add zero) in a fixed order, so the result is reproducible
+ * and identical for every stage and for padded or unpadded layouts.
+ *  max_norm    > 0 and finite
+ *  workspace   caller-allocated device scratch of at least
+ *              zero_clip_workspace_bytes() bytes, 16-byte aligned, owned by the
+ *              caller; it holds the norm and coefficient until the next clip
+ *              and must stay allocated until that zero_step has completed.
+ * Call after every unit's gradients are registered and before zero_step.
+ * Errors: ZERO_EINVAL (bad max_norm, null/misaligned/small/host workspace);
+ * ZERO_ESTATE (no buffers, gradients missing, step pending post_step);
+ * ZERO_ECUDA.
+ */
+zero_status zero_clip_grad_norm(zero_ctx* ctx, float max_norm, void* workspace, int64_t workspace_bytes,
+                                void* stream);
+
+/*
+ * zero_grad_norm — the norm computed by the last zero_clip_grad_norm on this
+ * context, copied to the host.  Synchronizes `stream` (the stream the clip
+ * ran on).  ZERO_ESTATE if no clip has run.
+ */
+zero_status zero_grad_norm(zero_ctx* ctx, double* norm, void* stream);
 
 /*
  * zero_gather_weights — the protocol's gather_weights.  Stage 3 (ZeRO-3
@@ -205,7 +244,7 @@ zero_status zero_gather_weights(zero_ctx* ctx, int32_t unit, void* unit_buf, voi
 
 /*
  * zero_post_step — the protocol's post_step: forget the registered gradients
- * so the next step needs fresh ones.  ZERO_ESTATE unless a step was taken
+ * (and the pending clip coefficient) so the next step needs fresh ones.  ZERO_ESTATE unless a step was taken
  * since the last post_step.  No device work.
  */
 zero_status zero_post_step(zero_ctx* ctx, void* stream);

@@ -18,8 +18,10 @@ from .oracle import (  # noqa: F401
     bf16_round,
     bf16_widen,
     build,
+    clip_coef,
     dp_step,
     gather_unit,
+    grad_norm,
     layout,
     library_path,
     make_master,

@@ -68,11 +68,16 @@ def _load():
         lib.oracle_reduce.restype = f32
         lib.oracle_step_scalars.argtypes = [vp, vp, i64, vp]
         lib.oracle_step_scalars.restype = None
-        lib.oracle_zero_step.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp, vp, vp, vp, vp, i32, i32]
+        lib.oracle_zero_step.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32,
+                                         P(ctypes.c_double)]
         lib.oracle_zero_step.restype = ctypes.c_int
-        lib.oracle_dp_step.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp]
+        lib.oracle_dp_step.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp, f32, P(ctypes.c_double)]
         lib.oracle_dp_step.restype = None
-        lib.oracle_step_window.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp]
+        lib.oracle_step_window.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp, f32]
+        lib.oracle_grad_norm.argtypes = [vp, vp, i64, vp]
+        lib.oracle_grad_norm.restype = ctypes.c_double
+        lib.oracle_clip_coef.argtypes = [ctypes.c_double, f32]
+        lib.oracle_clip_coef.restype = f32
         lib.oracle_step_window.restype = None
         lib.oracle_gather_unit.argtypes = [i64, i64, i32, vp, vp]
         lib.oracle_gather_unit.restype = None
@@ -209,37 +214,57 @@ def step_scalars(hyper: Hyper, t: int) -> dict:
 
 
 def zero_step(hyper: Hyper, stage: int, t: int, lay: OracleLayout, grads, master, m, v,
-              param16_copies, plant_skip_allgather: bool = False) -> None:
-    """Literal per-rank ZeRO step in place.  ``param16_copies`` is (n_copies, P) uint16."""
+              param16_copies, plant_skip_allgather: bool = False, max_norm: float = 0.0):
+    """Literal per-rank ZeRO step in place.  ``param16_copies`` is (n_copies, P) uint16.
+
+    ``max_norm`` > 0 clips the reduced gradient to that global L2 norm; the
+    norm is returned (None without clipping)."""
     lib = _load()
     f, i = hyper.pack()
     arrs, ptrs = _grad_ptrs(grads, hyper)
     p16 = param16_copies
     n_copies = p16.shape[0] if p16.ndim == 2 else 1
+    norm = ctypes.c_double(float("nan"))
     rc = lib.oracle_zero_step(_ptr(f), _ptr(i), stage, t, lay.unit_padded.size,
                               _ptr(lay.unit_padded), _ptr(lay.unit_base), ptrs,
                               _ptr(master), _ptr(m), _ptr(v), _ptr(p16), n_copies,
-                              1 if plant_skip_allgather else 0)
+                              1 if plant_skip_allgather else 0, max_norm, ctypes.byref(norm))
     if rc != 0:
         raise ValueError("oracle_zero_step rejected its arguments")
+    return norm.value if max_norm > 0 else None
 
 
-def dp_step(hyper: Hyper, t: int, grads, master, m, v, param16) -> None:
-    """Unsharded data-parallel step in place over the whole buffer."""
+def dp_step(hyper: Hyper, t: int, grads, master, m, v, param16, max_norm: float = 0.0):
+    """Unsharded data-parallel step in place over the whole buffer (returns the norm when clipping)."""
     lib = _load()
     f, i = hyper.pack()
     arrs, ptrs = _grad_ptrs(grads, hyper)
+    norm = ctypes.c_double(float("nan"))
     lib.oracle_dp_step(_ptr(f), _ptr(i), t, master.size, ptrs, _ptr(master), _ptr(m), _ptr(v),
-                       _ptr(param16))
+                       _ptr(param16), max_norm, ctypes.byref(norm))
+    return norm.value if max_norm > 0 else None
 
 
-def step_window(hyper: Hyper, t: int, grads, master, m, v, param16) -> None:
-    """Step t on a window of consecutive elements, in place."""
+def step_window(hyper: Hyper, t: int, grads, master, m, v, param16, clip_coef: float = 1.0) -> None:
+    """Step t on a window of consecutive elements, in place (optionally clipped by ``clip_coef``)."""
     lib = _load()
     f, i = hyper.pack()
     arrs, ptrs = _grad_ptrs(grads, hyper)
     lib.oracle_step_window(_ptr(f), _ptr(i), t, master.size, ptrs, _ptr(master), _ptr(m), _ptr(v),
-                           _ptr(param16))
+                           _ptr(param16), clip_coef)
+
+
+def grad_norm(hyper: Hyper, grads) -> float:
+    """Global L2 norm of the reduced gradient (fp64 squares and sum, element order)."""
+    lib = _load()
+    f, i = hyper.pack()
+    arrs, ptrs = _grad_ptrs(grads, hyper)
+    return float(lib.oracle_grad_norm(_ptr(f), _ptr(i), arrs[0].size, ptrs))
+
+
+def clip_coef(norm: float, max_norm: float) -> float:
+    """min(1, max_norm / (norm + 1e-6)) rounded to fp32."""
+    return float(_load().oracle_clip_coef(norm, max_norm))
 
 
 def gather_unit(param16, unit_base: int, unit_padded: int, n_ranks: int) -> np.ndarray:

@@ -41,6 +41,15 @@
 //    -ffp-contract=off); sqrt and division are IEEE correctly rounded.
 //  * bf16 cast: round to nearest, ties to even, from the IEEE bit patterns;
 //    NaN stays a (quiet) NaN of the same sign; overflow rounds to infinity.
+//  * Gradient clipping (Femtotron #4/#5: ClipGradNorm on the fp32 gradient,
+//    before AdamW; the source guide's --clip-grad / gradient_clipping): the
+//    global L2 norm of the reduced gradient, sqrt(sum_j g_j^2).  Each square
+//    is exact in fp64; the sum uses Neumaier's compensated summation (an
+//    improved Kahan-Babuska sum), so the oracle's own rounding error stays
+//    near one fp64 ulp instead of the n * 2^-53 bound of a plain running sum.
+//    Coefficient min(1, max_norm / (norm + 1e-6)) evaluated in fp64 and
+//    rounded once to fp32; the reduced gradient is multiplied by it (one fp32
+//    multiply) before Adam.
 //
 // Parity pins: every function here is pinned by a "not gpu" test against
 // values printed on the pages, closed forms, invariants or brute force.
@@ -163,6 +172,41 @@ void adam_element(const Hyper& h, const StepScalars& s, float g, float* w, float
   *w = weight;
   *m = m_new;
   *v = v_new;
+}
+
+// Compensated running sum (Neumaier): sum holds the rounded total and comp
+// the rounding errors lost by each addition, recovered exactly.
+struct CompensatedSum {
+  double sum = 0.0;
+  double comp = 0.0;
+  void add(double x) {
+    const double t = sum + x;
+    if (std::fabs(sum) >= std::fabs(x)) {
+      comp = comp + ((sum - t) + x);
+    } else {
+      comp = comp + ((x - t) + sum);
+    }
+    sum = t;
+  }
+  double value() const { return sum + comp; }
+};
+
+// Global L2 norm of the reduced gradient over flat elements [0, n); every
+// square is exact in fp64.
+double grad_norm(const Hyper& h, const StepScalars& s, const void* const* grads, int64_t n) {
+  CompensatedSum sum_sq;
+  for (int64_t j = 0; j < n; ++j) {
+    const double g = static_cast<double>(reduce_element(h, s, grads, j));
+    sum_sq.add(g * g);
+  }
+  return std::sqrt(sum_sq.value());
+}
+
+// Clip coefficient: scale the gradient down to max_norm when its norm is
+// larger; 1 otherwise.
+float clip_coefficient(double norm, float max_norm) {
+  const double coef = static_cast<double>(max_norm) / (norm + 1e-6);
+  return coef < 1.0 ? static_cast<float>(coef) : 1.0f;
 }
 
 Hyper hyper_from(const float* f, const int32_t* i) {
@@ -331,6 +375,15 @@ float oracle_reduce(const float* hyper_f, const int32_t* hyper_i, const void* co
   return reduce_element(h, s, grads, j);
 }
 
+// Global L2 norm of the reduced gradient of n flat elements (exposed for pinning).
+double oracle_grad_norm(const float* hyper_f, const int32_t* hyper_i, int64_t n, const void* const* grads) {
+  const Hyper h = hyper_from(hyper_f, hyper_i);
+  const StepScalars s = step_scalars(h, 1);
+  return grad_norm(h, s, grads, n);
+}
+
+float oracle_clip_coef(double norm, float max_norm) { return clip_coefficient(norm, max_norm); }
+
 // The fp32 scalars of step t (exposed for pinning):
 // out = {1-beta1, 1-beta2, bc1, bc2, decay, 1/N}.
 void oracle_step_scalars(const float* hyper_f, const int32_t* hyper_i, int64_t t, float* out) {
@@ -366,7 +419,8 @@ void oracle_step_scalars(const float* hyper_f, const int32_t* hyper_i, int64_t t
 int oracle_zero_step(const float* hyper_f, const int32_t* hyper_i, int32_t stage, int64_t t,
                      int32_t n_units, const int64_t* unit_padded, const int64_t* unit_base,
                      const void* const* grads, float* master, float* m, float* v,
-                     uint16_t* param16_copies, int32_t n_copies, int32_t plant_skip_allgather) {
+                     uint16_t* param16_copies, int32_t n_copies, int32_t plant_skip_allgather,
+                     float max_norm, double* norm_out) {
   const Hyper h = hyper_from(hyper_f, hyper_i);
   if (stage < 1 || stage > 3 || t < 1) return -1;
   if (n_copies != 1 && n_copies != h.n_ranks) return -1;
@@ -389,6 +443,21 @@ int oracle_zero_step(const float* hyper_f, const int32_t* hyper_i, int32_t stage
       }
     }
   }
+  // Optional global-norm clipping of the reduced gradient: the norm over all
+  // shards of all units, in flat element order; every shard is then scaled
+  // by the same coefficient.
+  const bool clip = max_norm > 0.0f;
+  float coef = 1.0f;
+  if (clip) {
+    CompensatedSum sum_sq;
+    for (int64_t j = 0; j < total; ++j) {
+      const double g = static_cast<double>(grad_shards[j]);
+      sum_sq.add(g * g);
+    }
+    const double norm = std::sqrt(sum_sq.value());
+    coef = clip_coefficient(norm, max_norm);
+    if (norm_out) *norm_out = norm;
+  }
   // 2. + 3. each rank updates its own shard and casts it into its own copy.
   for (int32_t i = 0; i < n_units; ++i) {
     const int64_t shard = unit_padded[i] / N;
@@ -396,7 +465,8 @@ int oracle_zero_step(const float* hyper_f, const int32_t* hyper_i, int32_t stage
       uint16_t* own_copy = param16_copies + (n_copies == 1 ? 0 : static_cast<int64_t>(d) * total);
       for (int64_t e = 0; e < shard; ++e) {
         const int64_t j = unit_base[i] + d * shard + e;
-        adam_element(h, s, grad_shards[j], &master[j], &m[j], &v[j]);
+        const float g = clip ? grad_shards[j] * coef : grad_shards[j];
+        adam_element(h, s, g, &master[j], &m[j], &v[j]);
         own_copy[j] = narrow_bf16(master[j]);
       }
     }
@@ -426,11 +496,20 @@ int oracle_zero_step(const float* hyper_f, const int32_t* hyper_i, int32_t stage
 // averages the full gradient (all-reduce, same fixed rank order) and updates
 // the whole fp32 master itself; one element range [0, n).
 void oracle_dp_step(const float* hyper_f, const int32_t* hyper_i, int64_t t, int64_t n,
-                    const void* const* grads, float* master, float* m, float* v, uint16_t* param16) {
+                    const void* const* grads, float* master, float* m, float* v, uint16_t* param16,
+                    float max_norm, double* norm_out) {
   const Hyper h = hyper_from(hyper_f, hyper_i);
   const StepScalars s = step_scalars(h, t);
+  const bool clip = max_norm > 0.0f;
+  float coef = 1.0f;
+  if (clip) {
+    const double norm = grad_norm(h, s, grads, n);
+    coef = clip_coefficient(norm, max_norm);
+    if (norm_out) *norm_out = norm;
+  }
   for (int64_t j = 0; j < n; ++j) {
-    const float g = reduce_element(h, s, grads, j);
+    const float reduced = reduce_element(h, s, grads, j);
+    const float g = clip ? reduced * coef : reduced;
     adam_element(h, s, g, &master[j], &m[j], &v[j]);
     param16[j] = narrow_bf16(master[j]);
   }
@@ -440,12 +519,17 @@ void oracle_dp_step(const float* hyper_f, const int32_t* hyper_i, int64_t t, int
 // the window's replica gradients; master/m/v/param16 point at the window.
 // Adam is elementwise (lecture notes §3.1), so a window taken anywhere in a
 // large buffer is updated exactly as in the full step.
+// clip_coef != 1 scales the reduced gradient (the coefficient of a global
+// norm computed over the whole buffer, e.g. by oracle_grad_norm).
 void oracle_step_window(const float* hyper_f, const int32_t* hyper_i, int64_t t, int64_t n,
-                        const void* const* grads, float* master, float* m, float* v, uint16_t* param16) {
+                        const void* const* grads, float* master, float* m, float* v, uint16_t* param16,
+                        float clip_coef) {
   const Hyper h = hyper_from(hyper_f, hyper_i);
   const StepScalars s = step_scalars(h, t);
+  const bool clip = clip_coef != 1.0f;
   for (int64_t j = 0; j < n; ++j) {
-    const float g = reduce_element(h, s, grads, j);
+    const float reduced = reduce_element(h, s, grads, j);
+    const float g = clip ? reduced * clip_coef : reduced;
     adam_element(h, s, g, &master[j], &m[j], &v[j]);
     param16[j] = narrow_bf16(master[j]);
   }

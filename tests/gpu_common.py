@@ -117,12 +117,13 @@ class Problem:
     lay: oracle.OracleLayout
     init: List[np.ndarray]
     grads: List[List[np.ndarray]]     # [step][replica] flat padded buffers (host)
+    max_norm: float = 0.0             # > 0: global-norm clipping before every step
 
 
 def make_problem(pl: si.ParamList, n: int, stage: int, grad_dtype: str = "bf16", steps: int = 10,
                  seed: int = 0, lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
                  weight_decay: float = 0.0, adamw: bool = False, grad_std: float = 1e-2,
-                 outlier_fraction: float = 0.0) -> Problem:
+                 outlier_fraction: float = 0.0, max_norm: float = 0.0) -> Problem:
     hyper = oracle.Hyper(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay, adamw=adamw,
                          n_ranks=n, grad_dtype=grad_dtype)
     lay = oracle.layout(pl.numel, pl.unit, n, stage) if pl.numel else None
@@ -141,23 +142,26 @@ def make_problem(pl: si.ParamList, n: int, stage: int, grad_dtype: str = "bf16",
                 flat[off:off + k] = to_np(g)
             reps.append(flat)
         grads.append(reps)
-    return Problem(pl, n, stage, grad_dtype, hyper, lay, init, grads)
+    return Problem(pl, n, stage, grad_dtype, hyper, lay, init, grads, max_norm)
 
 
-def oracle_run(pb: Problem, steps: Optional[int] = None, every_step=None):
+def oracle_run(pb: Problem, steps: Optional[int] = None, every_step=None, norms: Optional[list] = None):
     """Runs the oracle over the problem; returns (master, m, v, p16).
 
     Stage 0 uses the unsharded data-parallel routine; stages 1-3 the literal
-    per-rank ZeRO step.  ``every_step(t, state)`` is called after each step.
+    per-rank ZeRO step.  ``every_step(t, state)`` is called after each step;
+    with clipping the per-step norms are appended to ``norms``.
     """
     master, m, v, p16 = oracle.make_master(pb.pl.numel, pb.lay, pb.init)
     steps = len(pb.grads) if steps is None else steps
     for t in range(1, steps + 1):
         g = pb.grads[t - 1]
         if pb.stage == 0:
-            oracle.dp_step(pb.hyper, t, g, master, m, v, p16)
+            nrm = oracle.dp_step(pb.hyper, t, g, master, m, v, p16, max_norm=pb.max_norm)
         else:
-            oracle.zero_step(pb.hyper, pb.stage, t, pb.lay, g, master, m, v, p16)
+            nrm = oracle.zero_step(pb.hyper, pb.stage, t, pb.lay, g, master, m, v, p16, max_norm=pb.max_norm)
+        if norms is not None:
+            norms.append(nrm)
         if every_step:
             every_step(t, (master.copy(), m.copy(), v.copy(), p16.copy()))
     return master, m, v, p16
@@ -203,13 +207,17 @@ def check_guards(fs: FlatStep, what: str):
 
 
 def run_gpu(pb: Problem, mode: str = "units", every_step=None, guard: int = 64,
-            gather_check: bool = True) -> FlatStep:
+            gather_check: bool = True, norms: Optional[list] = None) -> FlatStep:
     fs = gpu_flatstep(pb, guard=guard)
     try:
         for t in range(1, len(pb.grads) + 1):
             flats = upload_grads(pb, t)
             keep = []
             register(fs, pb, flats, mode, keep)
+            if pb.max_norm > 0:
+                fs.clip_grad_norm(pb.max_norm)
+                if norms is not None:
+                    norms.append(fs.grad_norm())
             fs.step()
             if pb.stage == 3 and gather_check:
                 for i in range(fs.n_units):

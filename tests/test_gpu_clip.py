@@ -1,0 +1,195 @@
+"""Global-norm gradient clipping on the GPU against the oracle.
+
+The oracle sums the squares of the reduced gradient in fp64 in element order
+(the plain definition); the GPU sums fixed chunks in a fixed order with
+~48-bit per-thread accumulation.  Norms must agree to 1e-12 relative; the
+fp32 clip coefficients (and hence all state) then agree bit for bit except
+when the two norms straddle an fp32 rounding boundary, which these seeded
+cases do not.  GPU runs of every stage must be bit-identical (the chunking
+is unit-relative and the pads add zeros)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth_inputs as si
+from gpu_common import (compare_state, ensure_built, gpu_flatstep, make_problem, oracle_run, register, run_gpu,
+                        to_np, upload_grads)
+from zero_sharded_mixed_flatparameter_gb300 import binding as B
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _clip_parity(pb, mode="units"):
+    ref_states, ref_norms, gpu_norms = {}, [], []
+    oracle_run(pb, every_step=lambda t, s: ref_states.__setitem__(t, s), norms=ref_norms)
+
+    def check(t, fs):
+        compare_state(fs, ref_states[t], f"clipped step {t}")
+    fs = run_gpu(pb, mode=mode, every_step=check, norms=gpu_norms)
+    fs.close()
+    for a, b in zip(gpu_norms, ref_norms):
+        assert abs(a - b) <= 1e-12 * abs(b), (a, b)
+    return ref_norms
+
+
+@pytest.mark.parametrize("stage", [0, 1, 2, 3])
+def test_toy_mlp_clipped(stage):
+    # grads ~N(0, 1e-2) over 34,192 params: norm ~1.85, clipped to 0.5
+    pb = make_problem(si.toy_mlp(), 4, stage, steps=10, seed=41, max_norm=0.5)
+    norms = _clip_parity(pb)
+    assert all(x > 0.5 for x in norms)
+
+
+def test_inactive_clip_equals_no_clip():
+    pb = make_problem(si.toy_mlp(), 4, 2, steps=3, seed=42, max_norm=1e6)
+    fs_clip = run_gpu(pb)
+    pb.max_norm = 0.0
+    fs_plain = run_gpu(pb)
+    for a, b in ((fs_clip.master, fs_plain.master), (fs_clip.exp_avg, fs_plain.exp_avg),
+                 (fs_clip.exp_avg_sq, fs_plain.exp_avg_sq), (fs_clip.param16, fs_plain.param16)):
+        assert torch.equal(a.view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32),
+                           b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32))
+    fs_clip.close()
+    fs_plain.close()
+
+
+@pytest.mark.parametrize("n,gd", [(5, "fp32"), (16, "bf16"), (3, "bf16")])
+def test_odd_layouts_clipped(n, gd):
+    # units straddling chunk boundaries, an exact multiple of the chunk, empty units
+    pl = si.from_units([16384 * 2, 16384 + 1, 0, 7, 16384 * 3 - 5, 33])
+    pb = make_problem(pl, n, 3, grad_dtype=gd, steps=3, seed=43 + n, max_norm=0.1)
+    _clip_parity(pb, mode="separate")
+    _clip_parity(pb, mode="units")
+
+
+def test_clipped_stages_bit_identical():
+    pl = si.from_units([16384 * 2, 1552, 16384 + 3, 9])
+    out = {}
+    for stage in (0, 1, 2, 3):
+        pb = make_problem(pl, 3, stage, steps=4, seed=44, max_norm=0.3)
+        norms = []
+        fs = run_gpu(pb, norms=norms)
+        vals = []
+        for buf in (fs.master, fs.exp_avg, fs.exp_avg_sq, fs.param16):
+            a = to_np(buf)
+            vals.append(np.concatenate([a[fs.param_offset(p):fs.param_offset(p) + k] for p, k in enumerate(pl.numel)]))
+        out[stage] = (norms, vals)
+        fs.close()
+    for stage in (1, 2, 3):
+        assert out[stage][0] == out[0][0]
+        for a, b in zip(out[0][1], out[stage][1]):
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def test_norm_independent_of_alignment():
+    # the same gradients through 16-byte-aligned buffers (vector loads) and
+    # buffers offset by one element (element-wise loads) give the same norm
+    pl = si.from_units([40_000])
+    pb = make_problem(pl, 4, 2, steps=1, seed=45, max_norm=0.1)
+    norms = []
+    for offset in (0, 1):
+        fs = gpu_flatstep(pb)
+        flats = upload_grads(pb, 1)
+        shifted = []
+        for f in flats:
+            buf = torch.zeros(f.numel() + 8, dtype=f.dtype, device=f.device)
+            buf[offset:offset + f.numel()] = f
+            shifted.append(buf[offset:offset + f.numel()])
+        fs.reduce_grads(0, shifted)
+        fs.clip_grad_norm(0.1)
+        norms.append(fs.grad_norm())
+        fs.step()
+        fs.post_step()
+        fs.close()
+    assert norms[0] == norms[1]
+
+
+def test_many_units_clipped():
+    sizes = [(8 * (i % 5) + 8) * 4 for i in range(130)]
+    pb = make_problem(si.from_units(sizes), 4, 3, steps=2, seed=46, max_norm=0.05)
+    _clip_parity(pb, mode="separate")
+
+
+def test_clip_errors():
+    pb = make_problem(si.toy_mlp(), 4, 2, steps=1, seed=47)
+    fs = gpu_flatstep(pb)
+    try:
+        need = B.zero_clip_workspace_bytes(fs.ctx)
+        assert need == 32 + 8 * sum(-(-k // 16384) for k in [4224, 16512, 8256, 4160, 1040])
+        ws = torch.empty(need + 16, dtype=torch.uint8, device="cuda")
+        host = torch.empty(need, dtype=torch.uint8)
+
+        def st(fn):
+            with pytest.raises(B.ZeroError) as e:
+                fn()
+            return e.value.status
+        assert st(lambda: B.zero_grad_norm(fs.ctx, 0)) == B.ZERO_ESTATE
+        assert st(lambda: B.zero_clip_grad_norm(fs.ctx, 1.0, ws.data_ptr(), need, 0)) == B.ZERO_ESTATE  # no grads
+        register(fs, pb, upload_grads(pb, 1), "units", [])
+        assert st(lambda: B.zero_clip_grad_norm(fs.ctx, 0.0, ws.data_ptr(), need, 0)) == B.ZERO_EINVAL
+        assert st(lambda: B.zero_clip_grad_norm(fs.ctx, float("nan"), ws.data_ptr(), need, 0)) == B.ZERO_EINVAL
+        assert st(lambda: B.zero_clip_grad_norm(fs.ctx, 1.0, 0, need, 0)) == B.ZERO_EINVAL
+        assert st(lambda: B.zero_clip_grad_norm(fs.ctx, 1.0, ws.data_ptr() + 8, need, 0)) == B.ZERO_EINVAL
+        assert st(lambda: B.zero_clip_grad_norm(fs.ctx, 1.0, ws.data_ptr(), need - 8, 0)) == B.ZERO_EINVAL
+        assert st(lambda: B.zero_clip_grad_norm(fs.ctx, 1.0, host.data_ptr(), need, 0)) == B.ZERO_EINVAL
+        stream = fs.stream_handle()
+        B.zero_clip_grad_norm(fs.ctx, 1.0, ws.data_ptr(), need, stream)
+        assert B.zero_last_launches(fs.ctx) == 2
+        nrm = B.zero_grad_norm(fs.ctx, stream)
+        ref = oracle.grad_norm(pb.hyper, pb.grads[0])
+        assert abs(nrm - ref) <= 1e-12 * ref
+        fs.step()
+        assert st(lambda: B.zero_clip_grad_norm(fs.ctx, 1.0, ws.data_ptr(), need, stream)) == B.ZERO_ESTATE
+        fs.post_step()
+        assert B.zero_grad_norm(fs.ctx, stream) == nrm  # still readable after the step
+    finally:
+        fs.close()
+
+
+def test_full_size_llama_1024_clipped():
+    # 73,417,728 params, N = 8, ZeRO-2, two clipped steps; the oracle computes
+    # the full norm from the gradients copied back, then checks windows
+    pl = si.llama_1024()
+    n, steps, max_norm = 8, 2, 1.0
+    lay = oracle.layout(pl.numel, pl.unit, n, 2)
+    init_flat = si.normal_fp32(pl.total, 0.02, 51, device="cuda")
+    from zero_sharded_mixed_flatparameter_gb300.runner import FlatStep
+    fs = FlatStep(pl.numel, pl.unit, stage=2, n_ranks=n, init_params=[init_flat[int(o):int(o) + k]
+                  for o, k in zip(np.concatenate([[0], np.cumsum(pl.numel)[:-1]]), pl.numel)])
+    rng = np.random.default_rng(52)
+    starts = sorted({0, lay.total_padded - 256, *rng.integers(0, lay.total_padded - 256, 40).tolist()})
+    win = {a: [to_np(init_flat[a:a + 256]), np.zeros(256, np.float32), np.zeros(256, np.float32),
+               np.zeros(256, np.uint16)] for a in starts}
+    del init_flat
+    h = oracle.Hyper(n_ranks=n)
+    try:
+        for t in range(1, steps + 1):
+            grads = si.replica_grads(n, lay.total_padded, 1e-3, 53 + t, "bf16", device="cuda")
+            host = [to_np(g) for g in grads]
+            ref_norm = oracle.grad_norm(h, host)
+            coef = oracle.clip_coef(ref_norm, max_norm)
+            assert coef < 1.0
+            fs.reduce_grads(-1, grads)
+            fs.clip_grad_norm(max_norm)
+            gpu_norm = fs.grad_norm()
+            assert abs(gpu_norm - ref_norm) <= 1e-12 * ref_norm
+            fs.step()
+            fs.post_step()
+            for a in starts:
+                oracle.step_window(h, t, [x[a:a + 256] for x in host], *win[a], clip_coef=coef)
+            del grads, host
+        torch.cuda.synchronize()
+        for a in starts:
+            got = (to_np(fs.master[a:a + 256]), to_np(fs.exp_avg[a:a + 256]), to_np(fs.exp_avg_sq[a:a + 256]),
+                   to_np(fs.param16[a:a + 256]))
+            compare_state(got, win[a], f"window@{a}")
+    finally:
+        fs.close()
+        torch.cuda.empty_cache()

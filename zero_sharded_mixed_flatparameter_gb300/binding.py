@@ -26,7 +26,8 @@ EXPORTED = (
     "zero_plan", "zero_make_master", "zero_num_units", "zero_padded_numel", "zero_layout",
     "zero_param_offset", "zero_state_bytes", "zero_stage3_peak_bytes", "zero_reduce_grads",
     "zero_step", "zero_gather_weights", "zero_post_step", "zero_step_count", "zero_last_launches", "zero_set_lr",
-    "zero_destroy", "zero_last_error", "zero_status_string",
+    "zero_destroy", "zero_last_error", "zero_status_string", "zero_clip_workspace_bytes", "zero_clip_grad_norm",
+    "zero_grad_norm",
 )
 
 
@@ -81,6 +82,9 @@ def load(path: str = LIB_PATH):
             "zero_last_launches": [vp, P(i32)],
             "zero_set_lr": [vp, f32],
             "zero_destroy": [vp],
+            "zero_clip_workspace_bytes": [vp, P(i64)],
+            "zero_clip_grad_norm": [vp, f32, vp, i64, vp],
+            "zero_grad_norm": [vp, P(ctypes.c_double), vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -208,6 +212,22 @@ def zero_last_launches(ctx: int) -> int:
 
 def zero_set_lr(ctx: int, lr: float) -> None:
     _check(load().zero_set_lr(ctx, lr), ctx)
+
+
+def zero_clip_workspace_bytes(ctx: int) -> int:
+    n = ctypes.c_int64()
+    _check(load().zero_clip_workspace_bytes(ctx, ctypes.byref(n)), ctx)
+    return n.value
+
+
+def zero_clip_grad_norm(ctx: int, max_norm: float, workspace: int, workspace_bytes: int, stream: int = 0) -> None:
+    _check(load().zero_clip_grad_norm(ctx, max_norm, workspace or None, workspace_bytes, stream or None), ctx)
+
+
+def zero_grad_norm(ctx: int, stream: int = 0) -> float:
+    out = ctypes.c_double()
+    _check(load().zero_grad_norm(ctx, ctypes.byref(out), stream or None), ctx)
+    return out.value
 
 
 def zero_destroy(ctx: int) -> None:

@@ -46,8 +46,44 @@ struct StepArgs {
   int nseg;
   long long total_vec;   // vectors over all segments (vector kernel)
   long long total_elems; // elements over all segments (scalar kernel)
+  const float* clip;     // device clip coefficient, or nullptr (no clipping)
   Seg seg[kMaxSegs];
 };
+
+// Global-norm clipping.  The squared norm of the reduced gradient is summed
+// over fixed unit-relative chunks of kClipChunk elements (the last chunk of a
+// unit also takes the unit's zero pads), each chunk in a fixed order, then
+// the chunk sums in chunk order: the result does not depend on the stage
+// (padding) or on how the grid is scheduled.
+constexpr long long kClipChunk = 16384;
+constexpr int kFinalizeThreads = 1024;
+
+// Workspace layout: [0] double norm, [8] float coefficient, [32..] double chunk partials.
+constexpr long long kClipHeaderBytes = 32;
+
+struct NormSeg {
+  long long len;          // padded unit length (elements)
+  long long n_chunks;     // chunks of this unit
+  long long chunk_start;  // first chunk's index within this launch
+  long long out_start;    // first chunk's index in the workspace partials
+  int vec_ok;             // 16-byte aligned gradients: vector loads allowed
+  const void* g[kMaxRanks];
+};
+
+struct NormArgs {
+  int n_ranks;
+  int grad_fp32;
+  float inv_n;
+  int nseg;
+  double* partials;
+  NormSeg seg[kMaxSegs];
+};
+
+// Norm pass: one CTA per chunk; writes one partial per chunk.
+cudaError_t launch_grad_sq(const NormArgs& a, long long chunks, cudaStream_t stream);
+// Sums n partials in a fixed order and writes the norm and the clip
+// coefficient min(1, max_norm / (norm + 1e-6)) into the workspace header.
+cudaError_t launch_clip_finalize(void* workspace, long long n_partials, float max_norm, cudaStream_t stream);
 
 // Launchers.  Each returns the cudaError_t of its launch.
 // Vector kernel: every segment has base % kVec == 0 and 16-byte aligned

@@ -72,9 +72,9 @@ __device__ __forceinline__ float reduce_scalar(const StepArgs& a, const Seg& s, 
   return __fmul_rn(acc, a.inv_n);
 }
 
-__device__ __forceinline__ void step_scalar_element(const StepArgs& a, const Seg& s, long long k) {
+__device__ __forceinline__ void step_scalar_element(const StepArgs& a, const Seg& s, long long k, float clip) {
   const long long j = s.base + k;
-  const float g = reduce_scalar(a, s, k);
+  const float g = __fmul_rn(reduce_scalar(a, s, k), clip);
   float w = a.master[j], m = a.m[j], v = a.v[j];
   adam(a, g, w, m, v);
   a.master[j] = w;
@@ -95,7 +95,7 @@ __device__ __forceinline__ long long first_index(long long tid, long long start,
 // Vector kernel: 8 elements per thread-iteration.
 // ---------------------------------------------------------------------------
 template <int N, bool kFp32>
-__device__ __forceinline__ void step_vec8(const StepArgs& a, const Seg& s, long long vi) {
+__device__ __forceinline__ void step_vec8(const StepArgs& a, const Seg& s, long long vi, float clip) {
   const long long j = s.base + vi * kVec;
   float g[kVec];
   if constexpr (!kFp32) {
@@ -138,7 +138,7 @@ __device__ __forceinline__ void step_vec8(const StepArgs& a, const Seg& s, long 
   float m[kVec] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
   float v[kVec] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-  for (int e = 0; e < kVec; ++e) adam(a, __fmul_rn(g[e], a.inv_n), w[e], m[e], v[e]);
+  for (int e = 0; e < kVec; ++e) adam(a, __fmul_rn(__fmul_rn(g[e], a.inv_n), clip), w[e], m[e], v[e]);
   st_stream_f4(a.master + j, make_float4(w[0], w[1], w[2], w[3]));
   st_stream_f4(a.master + j + 4, make_float4(w[4], w[5], w[6], w[7]));
   st_stream_f4(a.m + j, make_float4(m[0], m[1], m[2], m[3]));
@@ -160,11 +160,13 @@ template <int N, bool kFp32>
 __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_constant__ StepArgs a) {
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  // Clip coefficient of the global norm (x 1 is exact when not clipping).
+  const float clip = a.clip ? *a.clip : 1.0f;
   for (int s = 0; s < a.nseg; ++s) {
     const Seg& seg = a.seg[s];
     const long long nvec = seg.len / kVec;
     for (long long vi = first_index(tid, seg.vec_start, stride); vi < nvec; vi += stride) {
-      step_vec8<N, kFp32>(a, seg, vi);
+      step_vec8<N, kFp32>(a, seg, vi, clip);
     }
   }
   // Ragged ends (fewer than 8 elements per segment), element by element.
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
     const long long done = (seg.len / kVec) * kVec;
     const long long k = done + tid - static_cast<long long>(s) * kVec;
     if (tid >= static_cast<long long>(s) * kVec && k < seg.len && k < done + kVec) {
-      step_scalar_element(a, seg, k);
+      step_scalar_element(a, seg, k, clip);
     }
   }
 }
@@ -184,13 +186,162 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
 __global__ void __launch_bounds__(kStepThreads) step_scalar_kernel(const __grid_constant__ StepArgs a) {
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const float clip = a.clip ? *a.clip : 1.0f;
   long long start = 0;
   for (int s = 0; s < a.nseg; ++s) {
     const Seg& seg = a.seg[s];
     for (long long k = first_index(tid, start, stride); k < seg.len; k += stride) {
-      step_scalar_element(a, seg, k);
+      step_scalar_element(a, seg, k, clip);
     }
     start += seg.len;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Global gradient norm.
+// ---------------------------------------------------------------------------
+// Squares are accumulated per thread as an unevaluated fp32 pair (hi, lo):
+// the product's rounding error comes exactly from one fma, the sum's from
+// the two-sum identity, giving ~48-bit accuracy at fp32 throughput (fp64 is
+// scarce on this part).  Values outside [2^-40, 2^40] (and inf/NaN) take an
+// fp64 path, where their squares are exact.
+struct SqAcc {
+  float hi = 0.0f, lo = 0.0f;
+  double wide = 0.0;
+
+  __device__ __forceinline__ void add(float g) {
+    const float ag = fabsf(g);
+    if (ag == 0.0f || (ag >= 0x1p-40f && ag <= 0x1p40f)) {
+      const float p = __fmul_rn(g, g);
+      const float e = __fmaf_rn(g, g, -p);  // exact: g*g = p + e
+      const float t = __fadd_rn(hi, p);
+      const float bp = __fsub_rn(t, hi);
+      const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(t, bp)), __fsub_rn(p, bp));  // hi + p = t + err
+      hi = t;
+      lo = __fadd_rn(lo, __fadd_rn(err, e));
+    } else {
+      const double d = static_cast<double>(g);
+      wide = __dadd_rn(wide, __dmul_rn(d, d));
+    }
+  }
+  __device__ __forceinline__ double total() const {
+    return __dadd_rn(__dadd_rn(static_cast<double>(hi), static_cast<double>(lo)), wide);
+  }
+};
+
+// Fixed-order sum of one double per thread across the CTA (warp tree, then
+// warps in order).  Result valid in thread 0.
+template <int kThreads>
+__device__ __forceinline__ double block_sum(double d, double* smem) {
+  for (int off = 16; off > 0; off >>= 1) d = __dadd_rn(d, __shfl_down_sync(0xffffffffu, d, off));
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) smem[warp] = d;
+  __syncthreads();
+  double total = 0.0;
+  if (threadIdx.x == 0) {
+    total = smem[0];
+    for (int w = 1; w < kThreads / 32; ++w) total = __dadd_rn(total, smem[w]);
+  }
+  return total;
+}
+
+template <int N, bool kFp32>
+__device__ __forceinline__ void reduced8(const NormArgs& a, const NormSeg& s, long long e0, float* g) {
+  if constexpr (!kFp32) {
+    uint4 raw[N];
+#pragma unroll
+    for (int r = 0; r < N; ++r) raw[r] = ld_stream(static_cast<const unsigned short*>(s.g[r]) + e0);
+    g[0] = bf16_lo(raw[0].x); g[1] = bf16_hi(raw[0].x); g[2] = bf16_lo(raw[0].y); g[3] = bf16_hi(raw[0].y);
+    g[4] = bf16_lo(raw[0].z); g[5] = bf16_hi(raw[0].z); g[6] = bf16_lo(raw[0].w); g[7] = bf16_hi(raw[0].w);
+#pragma unroll
+    for (int r = 1; r < N; ++r) {
+      g[0] = __fadd_rn(g[0], bf16_lo(raw[r].x)); g[1] = __fadd_rn(g[1], bf16_hi(raw[r].x));
+      g[2] = __fadd_rn(g[2], bf16_lo(raw[r].y)); g[3] = __fadd_rn(g[3], bf16_hi(raw[r].y));
+      g[4] = __fadd_rn(g[4], bf16_lo(raw[r].z)); g[5] = __fadd_rn(g[5], bf16_hi(raw[r].z));
+      g[6] = __fadd_rn(g[6], bf16_lo(raw[r].w)); g[7] = __fadd_rn(g[7], bf16_hi(raw[r].w));
+    }
+  } else {
+    float4 raw[N][2];
+#pragma unroll
+    for (int r = 0; r < N; ++r) {
+      const float* base = static_cast<const float*>(s.g[r]) + e0;
+      raw[r][0] = ld_stream_f4(base);
+      raw[r][1] = ld_stream_f4(base + 4);
+    }
+    g[0] = raw[0][0].x; g[1] = raw[0][0].y; g[2] = raw[0][0].z; g[3] = raw[0][0].w;
+    g[4] = raw[0][1].x; g[5] = raw[0][1].y; g[6] = raw[0][1].z; g[7] = raw[0][1].w;
+#pragma unroll
+    for (int r = 1; r < N; ++r) {
+      g[0] = __fadd_rn(g[0], raw[r][0].x); g[1] = __fadd_rn(g[1], raw[r][0].y);
+      g[2] = __fadd_rn(g[2], raw[r][0].z); g[3] = __fadd_rn(g[3], raw[r][0].w);
+      g[4] = __fadd_rn(g[4], raw[r][1].x); g[5] = __fadd_rn(g[5], raw[r][1].y);
+      g[6] = __fadd_rn(g[6], raw[r][1].z); g[7] = __fadd_rn(g[7], raw[r][1].w);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) g[e] = __fmul_rn(g[e], a.inv_n);
+}
+
+// Same reduction as the step (rank order, then x 1/N) for one element of any alignment.
+__device__ __forceinline__ float reduced1(const NormArgs& a, const NormSeg& s, long long k) {
+  float acc;
+  if (a.grad_fp32) {
+    acc = __ldcs(static_cast<const float*>(s.g[0]) + k);
+    for (int r = 1; r < a.n_ranks; ++r) acc = __fadd_rn(acc, __ldcs(static_cast<const float*>(s.g[r]) + k));
+  } else {
+    acc = __uint_as_float(static_cast<uint32_t>(__ldcs(static_cast<const unsigned short*>(s.g[0]) + k)) << 16);
+    for (int r = 1; r < a.n_ranks; ++r) {
+      const uint32_t h = __ldcs(static_cast<const unsigned short*>(s.g[r]) + k);
+      acc = __fadd_rn(acc, __uint_as_float(h << 16));
+    }
+  }
+  return __fmul_rn(acc, a.inv_n);
+}
+
+// One CTA per chunk.  Thread t takes the chunk's 8-element groups t, t+256,
+// ... in order and accumulates their elements in order; the vector and the
+// element-wise paths visit elements in the same order, so the chunk's sum does
+// not depend on the gradients' alignment.
+template <int N, bool kFp32>
+__global__ void __launch_bounds__(kStepThreads) grad_sq_kernel(const __grid_constant__ NormArgs a) {
+  __shared__ double smem[kStepThreads / 32];
+  const long long b = blockIdx.x;
+  int si = 0;
+  while (si + 1 < a.nseg && b >= a.seg[si + 1].chunk_start) ++si;
+  const NormSeg& s = a.seg[si];
+  const long long k = b - s.chunk_start;
+  const long long c0 = k * kClipChunk;
+  const long long c1 = (k == s.n_chunks - 1) ? s.len : c0 + kClipChunk;
+  const long long len = c1 - c0;
+  SqAcc acc;
+  for (long long grp = threadIdx.x; grp * kVec < len; grp += kStepThreads) {
+    const long long e0 = c0 + grp * kVec;
+    if (s.vec_ok && grp * kVec + kVec <= len) {
+      float g[kVec];
+      reduced8<N, kFp32>(a, s, e0, g);
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) acc.add(g[e]);
+    } else {
+      for (int e = 0; e < kVec; ++e) {
+        if (grp * kVec + e < len) acc.add(reduced1(a, s, e0 + e));
+      }
+    }
+  }
+  const double total = block_sum<kStepThreads>(acc.total(), smem);
+  if (threadIdx.x == 0) a.partials[s.out_start + k] = total;
+}
+
+__global__ void __launch_bounds__(kFinalizeThreads) clip_finalize_kernel(char* ws, long long n, float max_norm) {
+  __shared__ double smem[kFinalizeThreads / 32];
+  const double* partials = reinterpret_cast<const double*>(ws + kClipHeaderBytes);
+  double d = 0.0;
+  for (long long i = threadIdx.x; i < n; i += kFinalizeThreads) d = __dadd_rn(d, partials[i]);
+  const double sum_sq = block_sum<kFinalizeThreads>(d, smem);
+  if (threadIdx.x == 0) {
+    const double norm = __dsqrt_rn(sum_sq);
+    const double coef = __ddiv_rn(static_cast<double>(max_norm), __dadd_rn(norm, 1e-6));
+    *reinterpret_cast<double*>(ws) = norm;
+    *reinterpret_cast<float*>(ws + 8) = coef < 1.0 ? __double2float_rn(coef) : 1.0f;
   }
 }
 
@@ -346,6 +497,44 @@ cudaError_t launch_step_scalar(const StepArgs& a, cudaStream_t stream) {
                                   reinterpret_cast<const void*>(step_scalar_kernel));
   const long long grid = grid_for(a.total_elems, sms, bps);
   step_scalar_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+using NormKernel = void (*)(NormArgs);
+
+template <bool kFp32>
+NormKernel norm_kernel_for(int n) {
+  switch (n) {
+    case 1: return grad_sq_kernel<1, kFp32>;
+    case 2: return grad_sq_kernel<2, kFp32>;
+    case 3: return grad_sq_kernel<3, kFp32>;
+    case 4: return grad_sq_kernel<4, kFp32>;
+    case 5: return grad_sq_kernel<5, kFp32>;
+    case 6: return grad_sq_kernel<6, kFp32>;
+    case 7: return grad_sq_kernel<7, kFp32>;
+    case 8: return grad_sq_kernel<8, kFp32>;
+    case 9: return grad_sq_kernel<9, kFp32>;
+    case 10: return grad_sq_kernel<10, kFp32>;
+    case 11: return grad_sq_kernel<11, kFp32>;
+    case 12: return grad_sq_kernel<12, kFp32>;
+    case 13: return grad_sq_kernel<13, kFp32>;
+    case 14: return grad_sq_kernel<14, kFp32>;
+    case 15: return grad_sq_kernel<15, kFp32>;
+    case 16: return grad_sq_kernel<16, kFp32>;
+    default: return nullptr;
+  }
+}
+
+cudaError_t launch_grad_sq(const NormArgs& a, long long chunks, cudaStream_t stream) {
+  if (chunks <= 0) return cudaSuccess;
+  NormKernel k = a.grad_fp32 ? norm_kernel_for<true>(a.n_ranks) : norm_kernel_for<false>(a.n_ranks);
+  if (!k) return cudaErrorInvalidValue;
+  k<<<static_cast<unsigned>(chunks), kStepThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_clip_finalize(void* workspace, long long n_partials, float max_norm, cudaStream_t stream) {
+  clip_finalize_kernel<<<1, kFinalizeThreads, 0, stream>>>(static_cast<char*>(workspace), n_partials, max_norm);
   return cudaGetLastError();
 }
 

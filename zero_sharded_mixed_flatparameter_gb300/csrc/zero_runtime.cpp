@@ -50,6 +50,11 @@ struct zero_ctx {
   std::vector<const void*> grads;
   std::vector<uint8_t> registered;
 
+  // Clipping: workspace of the clip pending for the next step (cleared by
+  // post_step) and of the last clip run (for zero_grad_norm).
+  char* clip_ws = nullptr;
+  char* last_clip_ws = nullptr;
+
   std::string error;
 };
 
@@ -251,6 +256,7 @@ zero_status launch_batches(zero_ctx* ctx, const std::vector<PlannedSeg>& segs, b
     a.m = ctx->bufs.exp_avg;
     a.v = ctx->bufs.exp_avg_sq;
     a.p16 = static_cast<uint16_t*>(ctx->bufs.param16);
+    a.clip = ctx->clip_ws ? reinterpret_cast<const float*>(ctx->clip_ws + 8) : nullptr;
     fill_scalars(ctx, t, &a);
     long long vecs = 0, elems = 0;
     int n = 0;
@@ -271,6 +277,31 @@ zero_status launch_batches(zero_ctx* ctx, const std::vector<PlannedSeg>& segs, b
     ++*launches;
   }
   return ZERO_OK;
+}
+
+// Norm chunks of unit i: ceil(numel / C) chunks over the real elements; the
+// last one also covers the unit's pads, so the chunking (and the sum) is the
+// same with or without padding.
+int64_t unit_chunks(const zero_ctx* ctx, int32_t i) {
+  if (ctx->unit_padded[i] == 0) return 0;
+  const int64_t n = (ctx->unit_numel[i] + zfs::kClipChunk - 1) / zfs::kClipChunk;
+  return n > 0 ? n : 1;
+}
+
+int64_t total_chunks(const zero_ctx* ctx) {
+  int64_t n = 0;
+  for (int32_t i = 0; i < ctx->n_units; ++i) n += unit_chunks(ctx, i);
+  return n;
+}
+
+bool all_registered(const zero_ctx* ctx, int32_t* missing) {
+  for (int32_t i = 0; i < ctx->n_units; ++i) {
+    if (!ctx->registered[i]) {
+      if (missing) *missing = i;
+      return false;
+    }
+  }
+  return true;
 }
 
 }  // namespace
@@ -484,6 +515,91 @@ zero_status zero_step(zero_ctx* ctx, void* stream) {
   return ZERO_OK;
 }
 
+zero_status zero_clip_workspace_bytes(const zero_ctx* ctx, int64_t* bytes) {
+  if (!ctx || !bytes) return fail(nullptr, ZERO_EINVAL, "NULL argument");
+  *bytes = zfs::kClipHeaderBytes + 8 * total_chunks(ctx);
+  return ZERO_OK;
+}
+
+zero_status zero_clip_grad_norm(zero_ctx* ctx, float max_norm, void* workspace, int64_t workspace_bytes,
+                                void* stream) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  zero_status st = require_bound(ctx);
+  if (st != ZERO_OK) return st;
+  if (ctx->phase == Phase::kStepped) return fail(ctx, ZERO_ESTATE, "clip after step: call post_step first");
+  int32_t missing = -1;
+  if (!all_registered(ctx, &missing)) return fail(ctx, ZERO_ESTATE, "unit %d has no registered gradients", missing);
+  if (!(max_norm > 0.0f) || !std::isfinite(max_norm)) return fail(ctx, ZERO_EINVAL, "max_norm must be finite and > 0");
+  const int64_t need = zfs::kClipHeaderBytes + 8 * total_chunks(ctx);
+  if (!workspace) return fail(ctx, ZERO_EINVAL, "workspace is NULL");
+  if (!aligned(workspace, 16)) return fail(ctx, ZERO_EINVAL, "workspace is not 16-byte aligned");
+  if (workspace_bytes < need)
+    return fail(ctx, ZERO_EINVAL, "workspace has %lld bytes, %lld needed", static_cast<long long>(workspace_bytes),
+                static_cast<long long>(need));
+  if (!is_device_pointer(workspace, nullptr)) return fail(ctx, ZERO_EINVAL, "workspace is not CUDA device memory");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  double* partials = reinterpret_cast<double*>(ws + zfs::kClipHeaderBytes);
+  const int N = ctx->cfg.n_ranks;
+  const size_t esz = grad_bytes(ctx->cfg);
+  int32_t launches = 0;
+  int64_t out = 0;
+  int32_t i = 0;
+  while (i < ctx->n_units) {
+    zfs::NormArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.n_ranks = N;
+    a.grad_fp32 = ctx->cfg.grad_dtype == ZERO_GRAD_FP32 ? 1 : 0;
+    a.inv_n = 1.0f / static_cast<float>(N);
+    a.partials = partials;
+    long long chunks = 0;
+    int n = 0;
+    for (; i < ctx->n_units && n < zfs::kMaxSegs; ++i) {
+      const int64_t c = unit_chunks(ctx, i);
+      if (c == 0) continue;
+      zfs::NormSeg& g = a.seg[n++];
+      g.len = ctx->unit_padded[i];
+      g.n_chunks = c;
+      g.chunk_start = chunks;
+      g.out_start = out;
+      g.vec_ok = 1;
+      for (int r = 0; r < N; ++r) {
+        g.g[r] = ctx->grads[static_cast<size_t>(i) * zfs::kMaxRanks + r];
+        if (!aligned(g.g[r], 16)) g.vec_ok = 0;
+      }
+      chunks += c;
+      out += c;
+    }
+    (void)esz;
+    a.nseg = n;
+    if (chunks > 0) {
+      const cudaError_t e = zfs::launch_grad_sq(a, chunks, s);
+      if (e != cudaSuccess) return fail_cuda(ctx, "norm kernel launch", e);
+      ++launches;
+    }
+  }
+  const cudaError_t e = zfs::launch_clip_finalize(ws, out, max_norm, s);
+  if (e != cudaSuccess) return fail_cuda(ctx, "clip finalize launch", e);
+  ctx->last_launches = launches + 1;
+  ctx->clip_ws = ws;
+  ctx->last_clip_ws = ws;
+  return ZERO_OK;
+}
+
+zero_status zero_grad_norm(zero_ctx* ctx, double* norm, void* stream) {
+  if (!ctx || !norm) return fail(nullptr, ZERO_EINVAL, "NULL argument");
+  zero_status st = require_bound(ctx);
+  if (st != ZERO_OK) return st;
+  if (!ctx->last_clip_ws) return fail(ctx, ZERO_ESTATE, "no zero_clip_grad_norm has run on this context");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  double host = 0.0;
+  cudaError_t e = cudaMemcpyAsync(&host, ctx->last_clip_ws, sizeof host, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(ctx, "reading the norm", e);
+  *norm = host;
+  return ZERO_OK;
+}
+
 zero_status zero_gather_weights(zero_ctx* ctx, int32_t unit, void* unit_buf, void* stream) {
   if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
   zero_status st = require_bound(ctx);
@@ -516,6 +632,7 @@ zero_status zero_post_step(zero_ctx* ctx, void* stream) {
   if (ctx->phase != Phase::kStepped) return fail(ctx, ZERO_ESTATE, "post_step without a step since the last post_step");
   std::fill(ctx->registered.begin(), ctx->registered.end(), 0);
   std::fill(ctx->grads.begin(), ctx->grads.end(), nullptr);
+  ctx->clip_ws = nullptr;
   ctx->phase = Phase::kReady;
   return ZERO_OK;
 }

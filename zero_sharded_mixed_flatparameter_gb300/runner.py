@@ -119,6 +119,19 @@ class FlatStep:
         B.zero_reduce_grads(self.ctx, unit, [g.data_ptr() for g in replica_grads], self.stream_handle(stream))
         self._registered.append(list(replica_grads))  # keep alive until post_step
 
+    def clip_grad_norm(self, max_norm: float, stream=None) -> None:
+        """Global-norm clipping of the registered gradients for the next step
+        (the workspace is allocated once, by torch, and reused)."""
+        need = B.zero_clip_workspace_bytes(self.ctx)
+        if getattr(self, "_clip_ws", None) is None or self._clip_ws.numel() < need:
+            self._clip_ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        B.zero_clip_grad_norm(self.ctx, max_norm, self._clip_ws.data_ptr(), self._clip_ws.numel(),
+                              self.stream_handle(stream))
+
+    def grad_norm(self, stream=None) -> float:
+        """Norm of the last clip (synchronizes the stream)."""
+        return B.zero_grad_norm(self.ctx, self.stream_handle(stream))
+
     def step(self, stream=None) -> None:
         B.zero_step(self.ctx, self.stream_handle(stream))
 
