@@ -224,6 +224,26 @@ zero_status zero_clip_grad_norm(zero_ctx* ctx, float max_norm, void* workspace, 
                                 void* stream);
 
 /*
+ * zero_clip_grad_norm_static — zero_clip_grad_norm for callers that cannot
+ * allocate device memory (for example code running inside an allocator or
+ * an out-of-memory handler, or in a loop where allocation is forbidden), so
+ * cannot hand in a workspace.  The pages have no counterpart: this is a
+ * property of this library's interface, not of the method.
+ * Same computation and result as zero_clip_grad_norm; the scratch is a fixed
+ * 1 MiB array in the library's own device memory (created on every GPU that
+ * loads the library, held until exit), so layouts needing more than that —
+ * about 2.1e9 padded elements — are rejected with ZERO_EINVAL.  The call
+ * allocates nothing.  Its first call on a device looks up the array's device
+ * address (set-up, once per device, for the current device); make that first
+ * call before any stream capture.  All calls on a device share the array and
+ * it keeps the last call's contents: calls whose device work can overlap race
+ * on it, and between a call and the same context's zero_step no other
+ * static-scratch clip may run unless all are ordered on one stream.
+ * Errors: as zero_clip_grad_norm; ZERO_EINVAL when the layout is too large.
+ */
+zero_status zero_clip_grad_norm_static(zero_ctx* ctx, float max_norm, void* stream);
+
+/*
  * zero_grad_norm — the norm computed by the last zero_clip_grad_norm on this
  * context, copied to the host.  Synchronizes `stream` (the stream the clip
  * ran on).  ZERO_ESTATE if no clip has run.

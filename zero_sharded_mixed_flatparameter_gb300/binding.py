@@ -27,7 +27,7 @@ EXPORTED = (
     "zero_param_offset", "zero_state_bytes", "zero_stage3_peak_bytes", "zero_reduce_grads",
     "zero_step", "zero_gather_weights", "zero_post_step", "zero_step_count", "zero_last_launches", "zero_set_lr",
     "zero_destroy", "zero_last_error", "zero_status_string", "zero_clip_workspace_bytes", "zero_clip_grad_norm",
-    "zero_grad_norm",
+    "zero_grad_norm", "zero_clip_grad_norm_static",
 )
 
 
@@ -85,6 +85,7 @@ def load(path: str = LIB_PATH):
             "zero_clip_workspace_bytes": [vp, P(i64)],
             "zero_clip_grad_norm": [vp, f32, vp, i64, vp],
             "zero_grad_norm": [vp, P(ctypes.c_double), vp],
+            "zero_clip_grad_norm_static": [vp, f32, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -222,6 +223,11 @@ def zero_clip_workspace_bytes(ctx: int) -> int:
 
 def zero_clip_grad_norm(ctx: int, max_norm: float, workspace: int, workspace_bytes: int, stream: int = 0) -> None:
     _check(load().zero_clip_grad_norm(ctx, max_norm, workspace or None, workspace_bytes, stream or None), ctx)
+
+
+def zero_clip_grad_norm_static(ctx: int, max_norm: float, stream: int = 0) -> None:
+    """zero_clip_grad_norm without a workspace: for callers that cannot allocate."""
+    _check(load().zero_clip_grad_norm_static(ctx, max_norm, stream or None), ctx)
 
 
 def zero_grad_norm(ctx: int, stream: int = 0) -> float:

@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(PKG, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "--fmad=false", "-Xcompiler", "-fPIC,-O2",
           "-I" + INCLUDE, "-I" + CSRC]
-SOURCES = ["zero_kernels.cu", "zero_runtime.cpp"]
+SOURCES = ["zero_kernels.cu", "zero_runtime.cpp", "zero_no_alloc.cu"]
 
 
 def _nvcc() -> str:

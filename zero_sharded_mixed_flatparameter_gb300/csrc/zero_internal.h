@@ -105,3 +105,8 @@ cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaS
 int sm_count();
 
 }  // namespace zfs
+
+struct zero_ctx;
+// Records `message` as the context's last error (or the calling thread's when
+// ctx is NULL) and returns `status`.  Defined by the host runtime.
+int zfs_report_error(zero_ctx* ctx, int status, const char* message);

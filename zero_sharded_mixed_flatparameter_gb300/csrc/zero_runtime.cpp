@@ -306,6 +306,10 @@ bool all_registered(const zero_ctx* ctx, int32_t* missing) {
 
 }  // namespace
 
+int zfs_report_error(zero_ctx* ctx, int status, const char* message) {
+  return fail(ctx, static_cast<zero_status>(status), "%s", message);
+}
+
 extern "C" {
 
 zero_status zero_plan(const zero_config* cfg, const int64_t* param_numel, const int32_t* param_unit,
