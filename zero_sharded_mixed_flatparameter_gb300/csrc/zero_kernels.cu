@@ -203,31 +203,64 @@ __global__ void __launch_bounds__(kStepThreads) step_scalar_kernel(const __grid_
 // Squares are accumulated per thread as an unevaluated fp32 pair (hi, lo):
 // the product's rounding error comes exactly from one fma, the sum's from
 // the two-sum identity, giving ~48-bit accuracy at fp32 throughput (fp64 is
-// scarce on this part).  Values outside [2^-40, 2^40] (and inf/NaN) take an
-// fp64 path, where their squares are exact.
+// scarce on this part: a per-element fp64 operation would cap the pass far
+// below HBM speed).  Both error terms are exact while |g| is in
+// [2^-51, 2^60] (or g = 0); other values (and inf/NaN) are summed exactly in
+// fp64 instead, on a separate, rarely taken path.  Elements are added in the
+// same order on every path, so the sum does not depend on which one ran.
 struct SqAcc {
   float hi = 0.0f, lo = 0.0f;
   double wide = 0.0;
 
-  __device__ __forceinline__ void add(float g) {
+  __device__ __forceinline__ static bool in_range(float g) {
     const float ag = fabsf(g);
-    if (ag == 0.0f || (ag >= 0x1p-40f && ag <= 0x1p40f)) {
-      const float p = __fmul_rn(g, g);
-      const float e = __fmaf_rn(g, g, -p);  // exact: g*g = p + e
-      const float t = __fadd_rn(hi, p);
-      const float bp = __fsub_rn(t, hi);
-      const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(t, bp)), __fsub_rn(p, bp));  // hi + p = t + err
-      hi = t;
-      lo = __fadd_rn(lo, __fadd_rn(err, e));
+    return ag == 0.0f || (ag >= 0x1p-51f && ag <= 0x1p60f);
+  }
+  __device__ __forceinline__ void add_pair(float g) {
+    const float p = __fmul_rn(g, g);
+    const float e = __fmaf_rn(g, g, -p);  // exact: g*g = p + e
+    const float t = __fadd_rn(hi, p);
+    const float bp = __fsub_rn(t, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(t, bp)), __fsub_rn(p, bp));  // hi + p = t + err
+    hi = t;
+    lo = __fadd_rn(lo, __fadd_rn(err, e));
+  }
+  __device__ __forceinline__ void add_wide(float g) {
+    const double d = static_cast<double>(g);
+    wide = __dadd_rn(wide, __dmul_rn(d, d));
+  }
+  // One element (tails and unaligned gradients).
+  __device__ __forceinline__ void add1(float g) {
+    if (in_range(g)) {
+      add_pair(g);
     } else {
-      const double d = static_cast<double>(g);
-      wide = __dadd_rn(wide, __dmul_rn(d, d));
+      add_wide(g);
     }
   }
+  // Eight consecutive elements: one range test for the group.
+  __device__ __forceinline__ void add8(const float* g);
   __device__ __forceinline__ double total() const {
     return __dadd_rn(__dadd_rn(static_cast<double>(hi), static_cast<double>(lo)), wide);
   }
 };
+
+// Out of line on purpose: inlined, the compiler may evaluate this path for
+// every group.
+__device__ __noinline__ void add8_mixed(SqAcc* acc, const float* g) {
+  for (int e = 0; e < kVec; ++e) acc->add1(g[e]);
+}
+
+__device__ __forceinline__ void SqAcc::add8(const float* g) {
+  bool ok = true;
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) ok = ok & in_range(g[e]);
+  if (ok) {
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) add_pair(g[e]);
+  } else {
+    add8_mixed(this, g);
+  }
+}
 
 // Fixed-order sum of one double per thread across the CTA (warp tree, then
 // warps in order).  Result valid in thread 0.
@@ -301,9 +334,11 @@ __device__ __forceinline__ float reduced1(const NormArgs& a, const NormSeg& s, l
 // One CTA per chunk.  Thread t takes the chunk's 8-element groups t, t+256,
 // ... in order and accumulates their elements in order; the vector and the
 // element-wise paths visit elements in the same order, so the chunk's sum does
-// not depend on the gradients' alignment.
+// not depend on the gradients' alignment.  Full groups are loaded two at a
+// time before either is accumulated (more bytes in flight per thread; the
+// loose register bound allows it), which does not change the order.
 template <int N, bool kFp32>
-__global__ void __launch_bounds__(kStepThreads) grad_sq_kernel(const __grid_constant__ NormArgs a) {
+__global__ void __launch_bounds__(kStepThreads, 1) grad_sq_kernel(const __grid_constant__ NormArgs a) {
   __shared__ double smem[kStepThreads / 32];
   const long long b = blockIdx.x;
   int si = 0;
@@ -314,16 +349,23 @@ __global__ void __launch_bounds__(kStepThreads) grad_sq_kernel(const __grid_cons
   const long long c1 = (k == s.n_chunks - 1) ? s.len : c0 + kClipChunk;
   const long long len = c1 - c0;
   SqAcc acc;
-  for (long long grp = threadIdx.x; grp * kVec < len; grp += kStepThreads) {
+  long long grp = threadIdx.x;
+  for (; s.vec_ok && (grp + kStepThreads) * kVec + kVec <= len; grp += 2 * kStepThreads) {
+    float g0[kVec], g1[kVec];
+    reduced8<N, kFp32>(a, s, c0 + grp * kVec, g0);
+    reduced8<N, kFp32>(a, s, c0 + (grp + kStepThreads) * kVec, g1);
+    acc.add8(g0);
+    acc.add8(g1);
+  }
+  for (; grp * kVec < len; grp += kStepThreads) {
     const long long e0 = c0 + grp * kVec;
     if (s.vec_ok && grp * kVec + kVec <= len) {
       float g[kVec];
       reduced8<N, kFp32>(a, s, e0, g);
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) acc.add(g[e]);
+      acc.add8(g);
     } else {
       for (int e = 0; e < kVec; ++e) {
-        if (grp * kVec + e < len) acc.add(reduced1(a, s, e0 + e));
+        if (grp * kVec + e < len) acc.add1(reduced1(a, s, e0 + e));
       }
     }
   }
