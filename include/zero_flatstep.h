@@ -175,6 +175,25 @@ zero_status zero_reduce_grads(zero_ctx* ctx, int32_t unit, const void* const* re
                               void* stream);
 
 /*
+ * zero_accumulate_grads — fp32 gradient accumulation of one micro-step
+ * (Femtotron dev log #5: no_sync micro-steps accumulate before the single
+ * reduce; the source guide's Megatron main_grad: fp32 accumulation, the
+ * 18 B/param case).  For each replica r and element j of the unit (unit >= 0:
+ * padded_i elements) or of the whole buffer (unit == -1: padded_numel):
+ *   acc[r][j] = (first ? 0 : acc[r][j]) + float(micro[r][j])
+ * one fp32 addition per micro-step, no scaling (scale the loss by
+ * 1/accum_steps, as the pages do).  micro: N bf16 device buffers (2-byte
+ * aligned); acc: N fp32 device buffers (4-byte aligned), caller-owned; both
+ * 16-byte aligned for the vector kernel.  The accumulators are then
+ * registered with zero_reduce_grads on a context whose grad_dtype is fp32.
+ * Enqueued on `stream`; no context state changes.
+ * Errors: ZERO_EINVAL (grad_dtype is not fp32, unit out of range, null or
+ * misaligned pointer); ZERO_ESTATE (no buffers bound); ZERO_ECUDA.
+ */
+zero_status zero_accumulate_grads(zero_ctx* ctx, int32_t unit, const void* const* micro_grads_bf16,
+                                  float* const* accumulators, int32_t first, void* stream);
+
+/*
  * zero_step — one optimizer step, t <- t + 1, in one fused pass over the
  * padded flat buffer (lecture notes §2.1-§3.3; Femtotron dev logs #4/#5 step
  * order).  For every element j of every rank's shard:

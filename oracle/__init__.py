@@ -15,6 +15,7 @@ taken where the pages are silent.
 from .oracle import (  # noqa: F401
     Hyper,
     OracleLayout,
+    accumulate,
     bf16_round,
     bf16_widen,
     build,

@@ -79,6 +79,8 @@ def _load():
         lib.oracle_clip_coef.argtypes = [ctypes.c_double, f32]
         lib.oracle_clip_coef.restype = f32
         lib.oracle_step_window.restype = None
+        lib.oracle_accumulate.argtypes = [i32, i64, vp, vp, i32]
+        lib.oracle_accumulate.restype = None
         lib.oracle_gather_unit.argtypes = [i64, i64, i32, vp, vp]
         lib.oracle_gather_unit.restype = None
         _lib = lib
@@ -265,6 +267,21 @@ def grad_norm(hyper: Hyper, grads) -> float:
 def clip_coef(norm: float, max_norm: float) -> float:
     """min(1, max_norm / (norm + 1e-6)) rounded to fp32."""
     return float(_load().oracle_clip_coef(norm, max_norm))
+
+
+def accumulate(micro, acc, first: bool) -> None:
+    """One micro-step of fp32 gradient accumulation in place: acc[r] (+)= widen(micro[r])."""
+    lib = _load()
+    if len(micro) != len(acc):
+        raise ValueError("one accumulator per replica")
+    ms = [np.ascontiguousarray(np.asarray(x, dtype=np.uint16).reshape(-1)) for x in micro]
+    for a in acc:
+        if a.dtype != np.float32 or not a.flags["C_CONTIGUOUS"]:
+            raise TypeError("accumulators must be contiguous float32 arrays (updated in place)")
+    n = ms[0].size if ms else 0
+    mp = (ctypes.c_void_p * max(len(ms), 1))(*[_ptr(x) for x in ms])
+    ap = (ctypes.c_void_p * max(len(acc), 1))(*[_ptr(a) for a in acc])
+    lib.oracle_accumulate(len(ms), n, mp, ap, 1 if first else 0)
 
 
 def gather_unit(param16, unit_base: int, unit_padded: int, n_ranks: int) -> np.ndarray:

@@ -41,6 +41,12 @@
 //    -ffp-contract=off); sqrt and division are IEEE correctly rounded.
 //  * bf16 cast: round to nearest, ties to even, from the IEEE bit patterns;
 //    NaN stays a (quiet) NaN of the same sign; overflow rounds to infinity.
+//  * Gradient accumulation over micro-steps (Femtotron #5: no_sync micro-steps
+//    accumulate into the gradient before the one reduce; the source guide's
+//    Megatron main_grad: fp32 accumulation, 18 B/param): per replica and
+//    element, acc = widen(micro) on the first micro-step, else
+//    acc = acc + widen(micro), one fp32 addition per micro-step in micro-step
+//    order.  No scaling: the pages scale the loss by 1/accum_steps instead.
 //  * Gradient clipping (Femtotron #4/#5: ClipGradNorm on the fp32 gradient,
 //    before AdamW; the source guide's --clip-grad / gradient_clipping): the
 //    global L2 norm of the reduced gradient, sqrt(sum_j g_j^2).  Each square
@@ -532,6 +538,19 @@ void oracle_step_window(const float* hyper_f, const int32_t* hyper_i, int64_t t,
     const float g = clip ? reduced * clip_coef : reduced;
     adam_element(h, s, g, &master[j], &m[j], &v[j]);
     param16[j] = narrow_bf16(master[j]);
+  }
+}
+
+// fp32 gradient accumulation of one micro-step for N replicas over n flat
+// elements: micro[r] are bf16, acc[r] fp32.  first != 0 starts the sum
+// (whatever acc held is discarded).
+void oracle_accumulate(int32_t n_ranks, int64_t n, const uint16_t* const* micro, float* const* acc,
+                       int32_t first) {
+  for (int32_t r = 0; r < n_ranks; ++r) {
+    for (int64_t j = 0; j < n; ++j) {
+      const float g = widen_bf16(micro[r][j]);
+      acc[r][j] = first ? g : acc[r][j] + g;
+    }
   }
 }
 

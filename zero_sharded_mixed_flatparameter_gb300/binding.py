@@ -27,7 +27,7 @@ EXPORTED = (
     "zero_param_offset", "zero_state_bytes", "zero_stage3_peak_bytes", "zero_reduce_grads",
     "zero_step", "zero_gather_weights", "zero_post_step", "zero_step_count", "zero_last_launches", "zero_set_lr",
     "zero_destroy", "zero_last_error", "zero_status_string", "zero_clip_workspace_bytes", "zero_clip_grad_norm",
-    "zero_grad_norm", "zero_clip_grad_norm_static",
+    "zero_grad_norm", "zero_clip_grad_norm_static", "zero_accumulate_grads",
 )
 
 
@@ -86,6 +86,7 @@ def load(path: str = LIB_PATH):
             "zero_clip_grad_norm": [vp, f32, vp, i64, vp],
             "zero_grad_norm": [vp, P(ctypes.c_double), vp],
             "zero_clip_grad_norm_static": [vp, f32, vp],
+            "zero_accumulate_grads": [vp, i32, vp, vp, i32, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -185,6 +186,12 @@ def zero_stage3_peak_bytes(ctx: int):
 
 def zero_reduce_grads(ctx: int, unit: int, replica_grads: Sequence[int], stream: int = 0) -> None:
     _check(load().zero_reduce_grads(ctx, unit, _ptrs(replica_grads), stream or None), ctx)
+
+
+def zero_accumulate_grads(ctx: int, unit: int, micro_grads: Sequence[int], accumulators: Sequence[int],
+                          first: bool, stream: int = 0) -> None:
+    _check(load().zero_accumulate_grads(ctx, unit, _ptrs(micro_grads), _ptrs(accumulators), 1 if first else 0,
+                                        stream or None), ctx)
 
 
 def zero_step(ctx: int, stream: int = 0) -> None:

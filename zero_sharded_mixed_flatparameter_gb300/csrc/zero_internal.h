@@ -98,6 +98,17 @@ cudaError_t launch_zero_fill(float* master, float* m, float* v, uint16_t* p16, l
 cudaError_t launch_copy_param(const float* src, float* master, uint16_t* p16, long long offset,
                               long long n, cudaStream_t stream);
 
+// fp32 gradient accumulation of one micro-step: for every replica r,
+// acc[r][j] = (first ? 0 : acc[r][j]) + widen(micro[r][j]), j < n.
+struct AccumArgs {
+  int n_ranks;
+  int first;
+  long long n;
+  const uint16_t* micro[kMaxRanks];
+  float* acc[kMaxRanks];
+};
+cudaError_t launch_accumulate(const AccumArgs& a, bool vec, cudaStream_t stream);
+
 // ZeRO-3 unit gather: copy n bf16 elements; *launches counts the kernels enqueued.
 cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaStream_t stream, int* launches);
 

@@ -388,6 +388,54 @@ __global__ void __launch_bounds__(kFinalizeThreads) clip_finalize_kernel(char* w
 }
 
 // ---------------------------------------------------------------------------
+// fp32 gradient accumulation (one micro-step).  The replicas' buffers form
+// one concatenated index space for the grid-stride loop; 8 elements per
+// thread-iteration: one 16-byte bf16 load, two 16-byte fp32 loads (none on
+// the first micro-step) and two 16-byte fp32 stores.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kStepThreads, 1) accumulate_vec_kernel(const __grid_constant__ AccumArgs a) {
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long nvec = a.n / kVec;
+  for (int r = 0; r < a.n_ranks; ++r) {
+    const uint4* micro = reinterpret_cast<const uint4*>(a.micro[r]);
+    float* acc = a.acc[r];
+    for (long long vi = first_index(tid, static_cast<long long>(r) * nvec, stride); vi < nvec; vi += stride) {
+      const uint4 raw = ld_stream(micro + vi);
+      float g[kVec] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
+                       bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
+      float* p = acc + vi * kVec;
+      if (!a.first) {
+        const float4 x0 = ld_stream_f4(p), x1 = ld_stream_f4(p + 4);
+        g[0] = __fadd_rn(x0.x, g[0]); g[1] = __fadd_rn(x0.y, g[1]);
+        g[2] = __fadd_rn(x0.z, g[2]); g[3] = __fadd_rn(x0.w, g[3]);
+        g[4] = __fadd_rn(x1.x, g[4]); g[5] = __fadd_rn(x1.y, g[5]);
+        g[6] = __fadd_rn(x1.z, g[6]); g[7] = __fadd_rn(x1.w, g[7]);
+      }
+      st_stream_f4(p, make_float4(g[0], g[1], g[2], g[3]));
+      st_stream_f4(p + 4, make_float4(g[4], g[5], g[6], g[7]));
+    }
+    // ragged end of this replica (fewer than 8 elements)
+    const long long k = nvec * kVec + (tid - static_cast<long long>(r) * kVec);
+    if (tid >= static_cast<long long>(r) * kVec && tid < static_cast<long long>(r + 1) * kVec && k < a.n) {
+      const float g = __uint_as_float(static_cast<uint32_t>(a.micro[r][k]) << 16);
+      acc[k] = a.first ? g : __fadd_rn(acc[k], g);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kStepThreads) accumulate_scalar_kernel(const __grid_constant__ AccumArgs a) {
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (int r = 0; r < a.n_ranks; ++r) {
+    for (long long k = first_index(tid, static_cast<long long>(r) * a.n, stride); k < a.n; k += stride) {
+      const float g = __uint_as_float(static_cast<uint32_t>(a.micro[r][k]) << 16);
+      a.acc[r][k] = a.first ? g : __fadd_rn(a.acc[r][k], g);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // make_master and gather.
 // ---------------------------------------------------------------------------
 __global__ void zero_fill_kernel(float* __restrict__ master, float* __restrict__ m, float* __restrict__ v,
@@ -577,6 +625,21 @@ cudaError_t launch_grad_sq(const NormArgs& a, long long chunks, cudaStream_t str
 
 cudaError_t launch_clip_finalize(void* workspace, long long n_partials, float max_norm, cudaStream_t stream) {
   clip_finalize_kernel<<<1, kFinalizeThreads, 0, stream>>>(static_cast<char*>(workspace), n_partials, max_norm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_accumulate(const AccumArgs& a, bool vec, cudaStream_t stream) {
+  if (a.n <= 0 || a.n_ranks <= 0) return cudaSuccess;
+  const int sms = sm_count();
+  if (vec) {
+    long long work = (a.n / kVec) * a.n_ranks;
+    if (work < static_cast<long long>(a.n_ranks) * kVec) work = static_cast<long long>(a.n_ranks) * kVec;
+    const long long grid = grid_for(work, sms, kStepCtasPerSm);
+    accumulate_vec_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(a);
+  } else {
+    const long long grid = grid_for(a.n * a.n_ranks, sms, 8);
+    accumulate_scalar_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -490,6 +490,42 @@ zero_status zero_reduce_grads(zero_ctx* ctx, int32_t unit, const void* const* re
   return ZERO_OK;
 }
 
+zero_status zero_accumulate_grads(zero_ctx* ctx, int32_t unit, const void* const* micro_grads_bf16,
+                                  float* const* accumulators, int32_t first, void* stream) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  zero_status st = require_bound(ctx);
+  if (st != ZERO_OK) return st;
+  if (ctx->cfg.grad_dtype != ZERO_GRAD_FP32)
+    return fail(ctx, ZERO_EINVAL, "accumulation needs a context with grad_dtype fp32 (the accumulators it steps on)");
+  if (unit < -1 || unit >= ctx->n_units) return fail(ctx, ZERO_EINVAL, "unit %d out of range", unit);
+  if (!micro_grads_bf16 || !accumulators) return fail(ctx, ZERO_EINVAL, "pointer arrays are NULL");
+  const int N = ctx->cfg.n_ranks;
+  const int64_t len = unit < 0 ? ctx->padded_total : ctx->unit_padded[unit];
+  zfs::AccumArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.n_ranks = N;
+  a.first = first ? 1 : 0;
+  a.n = len;
+  bool vec = true;
+  for (int r = 0; r < N; ++r) {
+    if (len > 0 && (!micro_grads_bf16[r] || !accumulators[r]))
+      return fail(ctx, ZERO_EINVAL, "replica %d buffer is NULL", r);
+    if (!aligned(micro_grads_bf16[r], 2) || !aligned(accumulators[r], 4))
+      return fail(ctx, ZERO_EINVAL, "replica %d buffer is misaligned for its element type", r);
+    if (!aligned(micro_grads_bf16[r], 16) || !aligned(accumulators[r], 16)) vec = false;
+    a.micro[r] = static_cast<const uint16_t*>(micro_grads_bf16[r]);
+    a.acc[r] = accumulators[r];
+  }
+  if (len == 0) {
+    ctx->last_launches = 0;
+    return ZERO_OK;
+  }
+  const cudaError_t e = zfs::launch_accumulate(a, vec, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(ctx, "accumulate kernel launch", e);
+  ctx->last_launches = 1;
+  return ZERO_OK;
+}
+
 zero_status zero_step(zero_ctx* ctx, void* stream) {
   if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
   zero_status st = require_bound(ctx);

@@ -132,6 +132,18 @@ class FlatStep:
         """Norm of the last clip (synchronizes the stream)."""
         return B.zero_grad_norm(self.ctx, self.stream_handle(stream))
 
+    def accumulate_grads(self, unit: int, micro_grads: Sequence[torch.Tensor], accumulators: Sequence[torch.Tensor],
+                         first: bool, stream=None) -> None:
+        """fp32 accumulation of one micro-step's bf16 replica gradients."""
+        for g in micro_grads:
+            if g.dtype != torch.bfloat16 or not g.is_contiguous() or g.device != self.device:
+                raise ValueError("micro gradients must be contiguous bf16 device tensors")
+        for a in accumulators:
+            if a.dtype != torch.float32 or not a.is_contiguous() or a.device != self.device:
+                raise ValueError("accumulators must be contiguous fp32 device tensors")
+        B.zero_accumulate_grads(self.ctx, unit, [g.data_ptr() for g in micro_grads],
+                                [a.data_ptr() for a in accumulators], first, self.stream_handle(stream))
+
     def step(self, stream=None) -> None:
         B.zero_step(self.ctx, self.stream_handle(stream))
 
