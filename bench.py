@@ -290,13 +290,26 @@ def run_ours(args):
     grads = si.replica_grads(n, padded, wl["grad_std"], 100 + rank, wl["grad_dtype"], device=device,
                              outlier_fraction=wl["outliers"])
     units = [fs.layout(i) for i in range(fs.n_units)]
+    micro = []
+    if args.accum > 0:
+        if wl["grad_dtype"] != "fp32":
+            raise SystemExit("--accum needs an fp32-gradient workload (the accumulators are the step's gradients)")
+        micro = si.replica_grads(n, padded, wl["grad_std"], 200 + rank, "bf16", device=device)
     gather_bufs = []
     if wl["stage"] == 3:
         gather_bufs = [torch.empty(max(u[1], 1), dtype=torch.bfloat16, device=device) for u in units]
     stream = torch.cuda.current_stream(device)
 
-    def one_step(ev_pair=None, clip_pair=None):
+    def one_step(ev_pair=None, clip_pair=None, accum_pair=None):
         launches = 0
+        if micro:
+            if accum_pair is not None:
+                accum_pair[0].record(stream)
+            for k in range(args.accum):
+                fs.accumulate_grads(-1, micro, grads, first=(k == 0))
+                launches += fs.last_launches()
+            if accum_pair is not None:
+                accum_pair[1].record(stream)
         if wl["per_unit"]:
             for i, (numel, pad, shard, base) in enumerate(units):
                 fs.reduce_grads(i, [g[base:base + pad] for g in grads])
@@ -335,6 +348,8 @@ def run_ours(args):
     pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clip_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(args.steps)] if args.clip > 0 else [None] * args.steps
+    accum_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)] if args.accum > 0 else [None] * args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
     with ClockSampler(device.index if device.index is not None else 0) as clocks:
@@ -343,7 +358,7 @@ def run_ours(args):
         t_region0 = time.time()
         start.record(stream)
         for k in range(args.steps):
-            launches += one_step(pairs[k], clip_pairs[k])
+            launches += one_step(pairs[k], clip_pairs[k], accum_pairs[k])
         end.record(stream)
         torch.cuda.synchronize(device)
         t_region1 = time.time()
@@ -352,6 +367,7 @@ def run_ours(args):
     total_ms = start.elapsed_time(end)
     step_kernel_ms = [a.elapsed_time(b) for a, b in pairs]
     clip_ms = [a.elapsed_time(b) for a, b in clip_pairs] if args.clip > 0 else None
+    accum_ms = [a.elapsed_time(b) for a, b in accum_pairs] if args.accum > 0 else None
     clock = clocks.summary()
 
     total_ms_max, kern_ms_max = aggregate([total_ms, statistics.mean(step_kernel_ms)], "max", world, device)
@@ -424,6 +440,11 @@ def run_ours(args):
                 "norm_pass_gbs": (2 if wl["grad_dtype"] == "bf16" else 4) * n * padded
                 / (statistics.mean(clip_ms) / 1e3) / 1e9,
                 "note": "the clipped step is the norm pass (grad_sq + finalize kernels) plus the step kernel"},
+            "accum": None if accum_ms is None else {
+                "micro_steps": args.accum, "accumulate_ms_mean": statistics.mean(accum_ms),
+                "accumulate_bytes": n * padded * (6 + 10 * (args.accum - 1)),
+                "accumulate_gbs": n * padded * (6 + 10 * (args.accum - 1)) / (statistics.mean(accum_ms) / 1e3) / 1e9,
+                "note": "K micro-steps of bf16 grads accumulated into the fp32 replica gradients, then the step"},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -484,6 +505,8 @@ def main():
     ap.add_argument("--workload", default="llama1024_zero2_n8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--accum", type=int, default=0,
+                    help="fp32 gradient accumulation of this many bf16 micro-steps before every step (fp32 workloads)")
     ap.add_argument("--clip", type=float, default=0.0,
                     help="global-norm clipping to this max norm before every step (0: off)")
     args = ap.parse_args()

@@ -288,6 +288,33 @@ zero_status zero_gather_weights(zero_ctx* ctx, int32_t unit, void* unit_buf, voi
  */
 zero_status zero_post_step(zero_ctx* ctx, void* stream);
 
+/*
+ * zero_export_state — checkpoint the optimizer state in a layout-free form
+ * (lecture notes §5.2: the pads are not parameters): the real elements of
+ * master, m and v, unit by unit with the pads dropped — i.e. the parameters
+ * back to back in caller order, numel_total elements per array — into
+ * caller-allocated device fp32 buffers (4-byte aligned), and the step count
+ * into *t.  Any context planned over the same parameter list, with any N,
+ * stage or unit grouping of the same order, can import it (resharding; the
+ * source guide's resharding checkpoints, Femtotron #5's dp_size change).
+ * Enqueued on `stream`.  Errors: ZERO_EINVAL (null/misaligned/host pointer);
+ * ZERO_ESTATE (no buffers); ZERO_ECUDA.
+ */
+zero_status zero_export_state(zero_ctx* ctx, float* master_out, float* exp_avg_out, float* exp_avg_sq_out,
+                              int64_t* t, void* stream);
+
+/*
+ * zero_import_state — restore state exported by zero_export_state (from this
+ * or any other layout of the same parameters): master, m and v are written
+ * into this context's padded layout with zero pads, param16 = bf16(master)
+ * (round to nearest even), and the step count set to t.  Not allowed while
+ * a step awaits its post_step.  Enqueued on `stream`; the inputs may be
+ * released once it completes.  Errors: ZERO_EINVAL (null/misaligned/host
+ * pointer, t < 0); ZERO_ESTATE; ZERO_ECUDA.
+ */
+zero_status zero_import_state(zero_ctx* ctx, const float* master_in, const float* exp_avg_in,
+                              const float* exp_avg_sq_in, int64_t t, void* stream);
+
 /* Number of steps taken (t). */
 zero_status zero_step_count(const zero_ctx* ctx, int64_t* t);
 

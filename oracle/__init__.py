@@ -21,8 +21,10 @@ from .oracle import (  # noqa: F401
     build,
     clip_coef,
     dp_step,
+    export_state,
     gather_unit,
     grad_norm,
+    import_state,
     layout,
     library_path,
     make_master,

@@ -79,6 +79,10 @@ def _load():
         lib.oracle_clip_coef.argtypes = [ctypes.c_double, f32]
         lib.oracle_clip_coef.restype = f32
         lib.oracle_step_window.restype = None
+        lib.oracle_export.argtypes = [i32, vp, vp, vp, vp]
+        lib.oracle_export.restype = None
+        lib.oracle_import.argtypes = [i32, vp, vp, i64, vp, vp]
+        lib.oracle_import.restype = None
         lib.oracle_accumulate.argtypes = [i32, i64, vp, vp, i32]
         lib.oracle_accumulate.restype = None
         lib.oracle_gather_unit.argtypes = [i64, i64, i32, vp, vp]
@@ -267,6 +271,27 @@ def grad_norm(hyper: Hyper, grads) -> float:
 def clip_coef(norm: float, max_norm: float) -> float:
     """min(1, max_norm / (norm + 1e-6)) rounded to fp32."""
     return float(_load().oracle_clip_coef(norm, max_norm))
+
+
+def export_state(lay: OracleLayout, padded) -> np.ndarray:
+    """Real elements of every unit, back to back (pads dropped)."""
+    lib = _load()
+    src = np.ascontiguousarray(np.asarray(padded, dtype=np.float32))
+    out = np.empty(int(lay.unit_numel.sum()), dtype=np.float32)
+    lib.oracle_export(lay.unit_numel.size, _ptr(lay.unit_numel), _ptr(lay.unit_base), _ptr(src), _ptr(out))
+    return out
+
+
+def import_state(lay: OracleLayout, compact) -> np.ndarray:
+    """Inverse of export_state into ``lay``'s padded layout (pads zero)."""
+    lib = _load()
+    src = np.ascontiguousarray(np.asarray(compact, dtype=np.float32))
+    if src.size != int(lay.unit_numel.sum()):
+        raise ValueError("compact state size does not match the layout")
+    out = np.empty(lay.total_padded, dtype=np.float32)
+    lib.oracle_import(lay.unit_numel.size, _ptr(lay.unit_numel), _ptr(lay.unit_base), lay.total_padded, _ptr(src),
+                      _ptr(out))
+    return out
 
 
 def accumulate(micro, acc, first: bool) -> None:

@@ -541,6 +541,31 @@ void oracle_step_window(const float* hyper_f, const int32_t* hyper_i, int64_t t,
   }
 }
 
+// Checkpoint export (lecture notes §5.2: the pads are not parameters; the
+// source guide's resharding checkpoints, Femtotron #5's dp_size change): the
+// real elements of each unit, in unit order, back to back (the parameters in
+// caller order), for one fp32 state array.
+void oracle_export(int32_t n_units, const int64_t* unit_numel, const int64_t* unit_base,
+                   const float* padded, float* compact) {
+  int64_t out = 0;
+  for (int32_t i = 0; i < n_units; ++i) {
+    for (int64_t e = 0; e < unit_numel[i]; ++e) compact[out + e] = padded[unit_base[i] + e];
+    out += unit_numel[i];
+  }
+}
+
+// Checkpoint import: the inverse into a padded layout of any shard count; the
+// pads are zero.
+void oracle_import(int32_t n_units, const int64_t* unit_numel, const int64_t* unit_base, int64_t total_padded,
+                   const float* compact, float* padded) {
+  for (int64_t j = 0; j < total_padded; ++j) padded[j] = 0.0f;
+  int64_t in = 0;
+  for (int32_t i = 0; i < n_units; ++i) {
+    for (int64_t e = 0; e < unit_numel[i]; ++e) padded[unit_base[i] + e] = compact[in + e];
+    in += unit_numel[i];
+  }
+}
+
 // fp32 gradient accumulation of one micro-step for N replicas over n flat
 // elements: micro[r] are bf16, acc[r] fp32.  first != 0 starts the sum
 // (whatever acc held is discarded).

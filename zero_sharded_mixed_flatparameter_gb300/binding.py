@@ -27,7 +27,8 @@ EXPORTED = (
     "zero_param_offset", "zero_state_bytes", "zero_stage3_peak_bytes", "zero_reduce_grads",
     "zero_step", "zero_gather_weights", "zero_post_step", "zero_step_count", "zero_last_launches", "zero_set_lr",
     "zero_destroy", "zero_last_error", "zero_status_string", "zero_clip_workspace_bytes", "zero_clip_grad_norm",
-    "zero_grad_norm", "zero_clip_grad_norm_static", "zero_accumulate_grads",
+    "zero_grad_norm", "zero_clip_grad_norm_static", "zero_accumulate_grads", "zero_export_state",
+    "zero_import_state",
 )
 
 
@@ -87,6 +88,8 @@ def load(path: str = LIB_PATH):
             "zero_grad_norm": [vp, P(ctypes.c_double), vp],
             "zero_clip_grad_norm_static": [vp, f32, vp],
             "zero_accumulate_grads": [vp, i32, vp, vp, i32, vp],
+            "zero_export_state": [vp, vp, vp, vp, P(i64), vp],
+            "zero_import_state": [vp, vp, vp, vp, i64, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -204,6 +207,20 @@ def zero_gather_weights(ctx: int, unit: int, unit_buf: int, stream: int = 0) -> 
 
 def zero_post_step(ctx: int, stream: int = 0) -> None:
     _check(load().zero_post_step(ctx, stream or None), ctx)
+
+
+def zero_export_state(ctx: int, master_out: int, exp_avg_out: int, exp_avg_sq_out: int, stream: int = 0) -> int:
+    """Enqueues the export; returns the step count t."""
+    t = ctypes.c_int64()
+    _check(load().zero_export_state(ctx, master_out or None, exp_avg_out or None, exp_avg_sq_out or None,
+                                    ctypes.byref(t), stream or None), ctx)
+    return t.value
+
+
+def zero_import_state(ctx: int, master_in: int, exp_avg_in: int, exp_avg_sq_in: int, t: int,
+                      stream: int = 0) -> None:
+    _check(load().zero_import_state(ctx, master_in or None, exp_avg_in or None, exp_avg_sq_in or None, t,
+                                    stream or None), ctx)
 
 
 def zero_step_count(ctx: int) -> int:

@@ -97,6 +97,8 @@ cudaError_t launch_zero_fill(float* master, float* m, float* v, uint16_t* p16, l
                              cudaStream_t stream);
 cudaError_t launch_copy_param(const float* src, float* master, uint16_t* p16, long long offset,
                               long long n, cudaStream_t stream);
+// Plain fp32 copy of n elements (checkpoint export/import).
+cudaError_t launch_copy_f32(const float* src, float* dst, long long n, cudaStream_t stream);
 
 // fp32 gradient accumulation of one micro-step: for every replica r,
 // acc[r][j] = (first ? 0 : acc[r][j]) + widen(micro[r][j]), j < n.

@@ -472,6 +472,12 @@ __global__ void copy_param_kernel(const float* __restrict__ src, float* __restri
   }
 }
 
+__global__ void copy_f32_kernel(const float* __restrict__ src, float* __restrict__ dst, long long n) {
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long k = tid; k < n; k += stride) dst[k] = src[k];
+}
+
 __global__ void gather_vec_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n16) {
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -656,6 +662,13 @@ cudaError_t launch_copy_param(const float* src, float* master, uint16_t* p16, lo
   if (n <= 0) return cudaSuccess;
   const long long grid = grid_for(n, sm_count(), 8);
   copy_param_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(src, master, p16, offset, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_f32(const float* src, float* dst, long long n, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const long long grid = grid_for(n, sm_count(), 8);
+  copy_f32_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(src, dst, n);
   return cudaGetLastError();
 }
 

@@ -677,6 +677,76 @@ zero_status zero_post_step(zero_ctx* ctx, void* stream) {
   return ZERO_OK;
 }
 
+namespace {
+
+zero_status check_state_buffers(zero_ctx* ctx, const void* const* ptrs, const char* const* names) {
+  if (ctx->numel_total == 0) return ZERO_OK;
+  for (int k = 0; k < 3; ++k) {
+    if (!ptrs[k]) return fail(ctx, ZERO_EINVAL, "%s is NULL", names[k]);
+    if (!aligned(ptrs[k], 4)) return fail(ctx, ZERO_EINVAL, "%s is not 4-byte aligned", names[k]);
+    if (!is_device_pointer(ptrs[k], nullptr)) return fail(ctx, ZERO_EINVAL, "%s is not CUDA device memory", names[k]);
+  }
+  return ZERO_OK;
+}
+
+}  // namespace
+
+zero_status zero_export_state(zero_ctx* ctx, float* master_out, float* exp_avg_out, float* exp_avg_sq_out,
+                              int64_t* t, void* stream) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  zero_status st = require_bound(ctx);
+  if (st != ZERO_OK) return st;
+  const void* ptrs[3] = {master_out, exp_avg_out, exp_avg_sq_out};
+  const char* names[3] = {"master_out", "exp_avg_out", "exp_avg_sq_out"};
+  st = check_state_buffers(ctx, ptrs, names);
+  if (st != ZERO_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float* src[3] = {ctx->bufs.master, ctx->bufs.exp_avg, ctx->bufs.exp_avg_sq};
+  float* dst[3] = {master_out, exp_avg_out, exp_avg_sq_out};
+  int32_t launches = 0;
+  int64_t out = 0;
+  for (int32_t i = 0; i < ctx->n_units; ++i) {
+    for (int k = 0; k < 3; ++k) {
+      const cudaError_t e = zfs::launch_copy_f32(src[k] + ctx->unit_base[i], dst[k] + out, ctx->unit_numel[i], s);
+      if (e != cudaSuccess) return fail_cuda(ctx, "export copy", e);
+      if (ctx->unit_numel[i] > 0) ++launches;
+    }
+    out += ctx->unit_numel[i];
+  }
+  ctx->last_launches = launches;
+  if (t) *t = ctx->t;
+  return ZERO_OK;
+}
+
+zero_status zero_import_state(zero_ctx* ctx, const float* master_in, const float* exp_avg_in,
+                              const float* exp_avg_sq_in, int64_t t, void* stream) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  zero_status st = require_bound(ctx);
+  if (st != ZERO_OK) return st;
+  if (ctx->phase == Phase::kStepped) return fail(ctx, ZERO_ESTATE, "import while a step awaits post_step");
+  if (t < 0) return fail(ctx, ZERO_EINVAL, "t is negative");
+  const void* ptrs[3] = {master_in, exp_avg_in, exp_avg_sq_in};
+  const char* names[3] = {"master_in", "exp_avg_in", "exp_avg_sq_in"};
+  st = check_state_buffers(ctx, ptrs, names);
+  if (st != ZERO_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint16_t* p16 = static_cast<uint16_t*>(ctx->bufs.param16);
+  cudaError_t e = zfs::launch_zero_fill(ctx->bufs.master, ctx->bufs.exp_avg, ctx->bufs.exp_avg_sq, p16,
+                                        ctx->padded_total, s);
+  if (e != cudaSuccess) return fail_cuda(ctx, "import zero fill", e);
+  int64_t in = 0;
+  for (int32_t i = 0; i < ctx->n_units; ++i) {
+    const int64_t n = ctx->unit_numel[i], base = ctx->unit_base[i];
+    e = zfs::launch_copy_param(master_in + in, ctx->bufs.master, p16, base, n, s);
+    if (e == cudaSuccess) e = zfs::launch_copy_f32(exp_avg_in + in, ctx->bufs.exp_avg + base, n, s);
+    if (e == cudaSuccess) e = zfs::launch_copy_f32(exp_avg_sq_in + in, ctx->bufs.exp_avg_sq + base, n, s);
+    if (e != cudaSuccess) return fail_cuda(ctx, "import copy", e);
+    in += n;
+  }
+  ctx->t = t;
+  return ZERO_OK;
+}
+
 zero_status zero_step_count(const zero_ctx* ctx, int64_t* t) {
   if (!ctx || !t) return fail(nullptr, ZERO_EINVAL, "NULL argument");
   *t = ctx->t;

@@ -154,6 +154,21 @@ class FlatStep:
         B.zero_post_step(self.ctx, self.stream_handle(stream))
         self._registered.clear()
 
+    def export_state(self, stream=None):
+        """Layout-free checkpoint: (master, exp_avg, exp_avg_sq) fp32 device
+        tensors of the real elements in parameter order, and the step count."""
+        out = [torch.empty(max(self.numel, 1), dtype=torch.float32, device=self.device) for _ in range(3)]
+        t = B.zero_export_state(self.ctx, *[o.data_ptr() for o in out], self.stream_handle(stream))
+        return [o[:self.numel] for o in out], t
+
+    def import_state(self, master, exp_avg, exp_avg_sq, t: int, stream=None) -> None:
+        for x in (master, exp_avg, exp_avg_sq):
+            if x.dtype != torch.float32 or not x.is_contiguous() or x.numel() != self.numel:
+                raise ValueError("state tensors must be contiguous fp32 of numel_total elements")
+        B.zero_import_state(self.ctx, master.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(), t,
+                            self.stream_handle(stream))
+        torch.cuda.current_stream(self.device).synchronize()
+
     def step_count(self) -> int:
         return B.zero_step_count(self.ctx)
 
