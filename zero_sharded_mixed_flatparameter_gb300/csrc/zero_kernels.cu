@@ -390,30 +390,61 @@ __global__ void __launch_bounds__(kFinalizeThreads) clip_finalize_kernel(char* w
 // ---------------------------------------------------------------------------
 // fp32 gradient accumulation (one micro-step).  The replicas' buffers form
 // one concatenated index space for the grid-stride loop; 8 elements per
-// thread-iteration: one 16-byte bf16 load, two 16-byte fp32 loads (none on
-// the first micro-step) and two 16-byte fp32 stores.
+// vector: one 16-byte bf16 load, two 16-byte fp32 loads (none on the first
+// micro-step) and two 16-byte fp32 stores.  A thread loads kAccumIlp vectors
+// before adding any (48 bytes per vector are too few to keep HBM busy at
+// 512 threads per SM).
 // ---------------------------------------------------------------------------
+constexpr int kAccumIlp = 4;
+
+__device__ __forceinline__ void accumulate8(const uint4 raw, const float4 x0, const float4 x1, bool first, float* p) {
+  float g[kVec] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
+                   bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
+  if (!first) {
+    g[0] = __fadd_rn(x0.x, g[0]); g[1] = __fadd_rn(x0.y, g[1]);
+    g[2] = __fadd_rn(x0.z, g[2]); g[3] = __fadd_rn(x0.w, g[3]);
+    g[4] = __fadd_rn(x1.x, g[4]); g[5] = __fadd_rn(x1.y, g[5]);
+    g[6] = __fadd_rn(x1.z, g[6]); g[7] = __fadd_rn(x1.w, g[7]);
+  }
+  st_stream_f4(p, make_float4(g[0], g[1], g[2], g[3]));
+  st_stream_f4(p + 4, make_float4(g[4], g[5], g[6], g[7]));
+}
+
 __global__ void __launch_bounds__(kStepThreads, 1) accumulate_vec_kernel(const __grid_constant__ AccumArgs a) {
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long nvec = a.n / kVec;
+  const bool first = a.first != 0;
   for (int r = 0; r < a.n_ranks; ++r) {
     const uint4* micro = reinterpret_cast<const uint4*>(a.micro[r]);
     float* acc = a.acc[r];
-    for (long long vi = first_index(tid, static_cast<long long>(r) * nvec, stride); vi < nvec; vi += stride) {
-      const uint4 raw = ld_stream(micro + vi);
-      float g[kVec] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
-                       bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
-      float* p = acc + vi * kVec;
-      if (!a.first) {
-        const float4 x0 = ld_stream_f4(p), x1 = ld_stream_f4(p + 4);
-        g[0] = __fadd_rn(x0.x, g[0]); g[1] = __fadd_rn(x0.y, g[1]);
-        g[2] = __fadd_rn(x0.z, g[2]); g[3] = __fadd_rn(x0.w, g[3]);
-        g[4] = __fadd_rn(x1.x, g[4]); g[5] = __fadd_rn(x1.y, g[5]);
-        g[6] = __fadd_rn(x1.z, g[6]); g[7] = __fadd_rn(x1.w, g[7]);
+    long long vi = first_index(tid, static_cast<long long>(r) * nvec, stride);
+    for (; vi + (kAccumIlp - 1) * stride < nvec; vi += kAccumIlp * stride) {
+      uint4 raw[kAccumIlp];
+      float4 x[kAccumIlp][2];
+#pragma unroll
+      for (int u = 0; u < kAccumIlp; ++u) {
+        raw[u] = ld_stream(micro + vi + u * stride);
+        if (!first) {
+          const float* p = acc + (vi + u * stride) * kVec;
+          x[u][0] = ld_stream_f4(p);
+          x[u][1] = ld_stream_f4(p + 4);
+        } else {
+          x[u][0] = x[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
-      st_stream_f4(p, make_float4(g[0], g[1], g[2], g[3]));
-      st_stream_f4(p + 4, make_float4(g[4], g[5], g[6], g[7]));
+#pragma unroll
+      for (int u = 0; u < kAccumIlp; ++u) accumulate8(raw[u], x[u][0], x[u][1], first, acc + (vi + u * stride) * kVec);
+    }
+    for (; vi < nvec; vi += stride) {
+      float* p = acc + vi * kVec;
+      const uint4 raw = ld_stream(micro + vi);
+      float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+      if (!first) {
+        x0 = ld_stream_f4(p);
+        x1 = ld_stream_f4(p + 4);
+      }
+      accumulate8(raw, x0, x1, first, p);
     }
     // ragged end of this replica (fewer than 8 elements)
     const long long k = nvec * kVec + (tid - static_cast<long long>(r) * kVec);
