@@ -300,7 +300,7 @@ def run_ours(args):
         gather_bufs = [torch.empty(max(u[1], 1), dtype=torch.bfloat16, device=device) for u in units]
     stream = torch.cuda.current_stream(device)
 
-    def one_step(ev_pair=None, clip_pair=None, accum_pair=None):
+    def one_step(ev_pair=None, clip_pair=None, accum_pair=None, gather_pair=None):
         launches = 0
         if micro:
             if accum_pair is not None:
@@ -328,9 +328,13 @@ def run_ours(args):
         if ev_pair is not None:
             ev_pair[1].record(stream)
         launches += fs.last_launches()
+        if gather_pair is not None and gather_bufs:
+            gather_pair[0].record(stream)
         for i, buf in enumerate(gather_bufs):
             fs.gather_weights(i, buf)
             launches += fs.last_launches()
+        if gather_pair is not None and gather_bufs:
+            gather_pair[1].record(stream)
         fs.post_step()
         return launches
 
@@ -350,6 +354,8 @@ def run_ours(args):
                   for _ in range(args.steps)] if args.clip > 0 else [None] * args.steps
     accum_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)] if args.accum > 0 else [None] * args.steps
+    gather_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(args.steps)] if gather_bufs else [None] * args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
     with ClockSampler(device.index if device.index is not None else 0) as clocks:
@@ -358,7 +364,7 @@ def run_ours(args):
         t_region0 = time.time()
         start.record(stream)
         for k in range(args.steps):
-            launches += one_step(pairs[k], clip_pairs[k], accum_pairs[k])
+            launches += one_step(pairs[k], clip_pairs[k], accum_pairs[k], gather_pairs[k])
         end.record(stream)
         torch.cuda.synchronize(device)
         t_region1 = time.time()
@@ -368,6 +374,7 @@ def run_ours(args):
     step_kernel_ms = [a.elapsed_time(b) for a, b in pairs]
     clip_ms = [a.elapsed_time(b) for a, b in clip_pairs] if args.clip > 0 else None
     accum_ms = [a.elapsed_time(b) for a, b in accum_pairs] if args.accum > 0 else None
+    gather_ms = [a.elapsed_time(b) for a, b in gather_pairs] if gather_bufs else None
     clock = clocks.summary()
 
     total_ms_max, kern_ms_max = aggregate([total_ms, statistics.mean(step_kernel_ms)], "max", world, device)
@@ -470,6 +477,10 @@ def run_ours(args):
                 "norm_pass_gbs": (2 if wl["grad_dtype"] == "bf16" else 4) * n * padded
                 / (statistics.mean(clip_ms) / 1e3) / 1e9,
                 "note": "the clipped step is the norm pass (grad_sq + finalize kernels) plus the step kernel"},
+            "gather": None if gather_ms is None else {
+                "units": len(gather_bufs), "gather_ms_mean": statistics.mean(gather_ms),
+                "gather_bytes": 4 * padded, "gather_gbs": 4 * padded / (statistics.mean(gather_ms) / 1e3) / 1e9,
+                "note": "ZeRO-3 per-unit gathers of the bf16 shards into unit buffers (2 B read + 2 B written)"},
             "accum": None if accum_ms is None else {
                 "micro_steps": args.accum, "accumulate_ms_mean": statistics.mean(accum_ms),
                 "accumulate_bytes": n * padded * (6 + 10 * (args.accum - 1)),
@@ -484,6 +495,71 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# Roofline sweep: one flat fp32 buffer of 1M..1B params x N = 1..16.
+# ---------------------------------------------------------------------------
+L2_BYTES = 129 * 1024 * 1024
+
+
+def run_sweep(args):
+    import torch
+    import synth_inputs as si
+    from zero_sharded_mixed_flatparameter_gb300 import build_lib
+    from zero_sharded_mixed_flatparameter_gb300.runner import FlatStep
+    build_lib.build()
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(device)
+    peak, peak_kind = measured_peaks()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+    sizes = [int(float(x)) for x in args.sweep_sizes.split(",")]
+    ranks = [int(x) for x in args.sweep_ranks.split(",")]
+    for numel in sizes:
+        for n in ranks:
+            init = si.normal_fp32(numel, 0.02, 1, device=device)
+            fs = FlatStep([numel], [0], stage=2, n_ranks=n, init_params=[init], device=device)
+            del init
+            grads = si.replica_grads(n, numel, 1e-2, 2, "bf16", device=device, outlier_fraction=0.001)
+            nbytes = bytes_per_param(n, "bf16") * fs.padded
+            reps = max(5, min(50, int(2e10 // max(nbytes, 1))))
+
+            def step():
+                fs.reduce_grads(-1, grads)
+                fs.step()
+                fs.post_step()
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize(device)
+            # Each timed step is queued behind ~0.1 ms of device work (a
+            # bounded spin), so its events bracket the kernel, not the host's
+            # launch latency.  "flushed": the 512 MB fill evicts the working
+            # set from L2 first; "l2_resident": a warm step runs just before.
+            flushed, warm = [], []
+            for mode, out in (("flushed", flushed), ("warm", warm)):
+                for _ in range(reps):
+                    if mode == "flushed":
+                        flush.fill_(1)
+                    else:
+                        step()
+                    torch.cuda._sleep(200_000)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    step()
+                    b.record(stream)
+                    torch.cuda.synchronize(device)
+                    out.append(a.elapsed_time(b))
+            mf, mw = statistics.median(flushed), statistics.median(warm)
+            print(json.dumps({
+                "sweep_point": f"flat:{numel}:{n}", "params": numel, "n_ranks_simulated": n,
+                "algorithmic_bytes": nbytes, "bytes_per_param": bytes_per_param(n, "bf16"), "reps": reps,
+                "kernel_ms_l2_flushed": mf, "gbs_l2_flushed": nbytes / mf / 1e6,
+                "frac_l2_flushed": nbytes / mf / 1e6 / peak, "params_per_s_l2_flushed": numel / mf * 1e3,
+                "kernel_ms_l2_resident": mw, "gbs_l2_resident": nbytes / mw / 1e6,
+                "working_set_fits_l2": nbytes <= L2_BYTES, "peak_gbs": peak, "peak_source": peak_kind}), flush=True)
+            fs.close()
+            del grads
+            torch.cuda.empty_cache()
 
 
 # ---------------------------------------------------------------------------
@@ -537,12 +613,18 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--accum", type=int, default=0,
                     help="fp32 gradient accumulation of this many bf16 micro-steps before every step (fp32 workloads)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="roofline sweep of flat buffers (one JSON line per point instead of the bench line)")
+    ap.add_argument("--sweep-sizes", default="1e6,16e6,128e6,512e6,1e9")
+    ap.add_argument("--sweep-ranks", default="1,2,4,8,16")
     ap.add_argument("--clip", type=float, default=0.0,
                     help="global-norm clipping to this max norm before every step (0: off)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
