@@ -153,3 +153,46 @@ def test_flat_sweep_points(numel, n):
     # single flat fp32 buffer, bf16 grads N(0, 1e-2) with 0.1% entries set to +-1, one step
     assert run_full(si.single_buffer(numel), n, 2, "bf16", 1, seed=5, grad_std=1e-2, outlier_fraction=0.001,
                     register_units=False) == 1
+
+
+def test_beyond_2_pow_31_elements():
+    # 2^31 + 4,105 elements in one unit: every index and pointer offset must be
+    # 64-bit (windows straddle 2^31 and the end), with the clip on as well
+    numel = 2 ** 31 + 4105
+    pl = si.single_buffer(numel)
+    n = 1
+    lay = oracle.layout(pl.numel, pl.unit, n, 1)
+    init_flat = si.normal_fp32(numel, 0.02, 61, device="cuda")
+    fs = FlatStep(pl.numel, pl.unit, stage=1, n_ranks=n, init_params=[init_flat])
+    starts = [0, 2 ** 31 - W // 2, 2 ** 31 + 1000, numel - W]
+    win = {a: [to_np(init_flat[a:a + W]), np.zeros(W, np.float32), np.zeros(W, np.float32),
+               np.zeros(W, np.uint16)] for a in starts}
+    del init_flat
+    h = oracle.Hyper(n_ranks=n)
+    try:
+        for t in (1, 2):
+            grads = si.replica_grads(n, numel, 1e-3, 62 + t, "bf16", device="cuda")
+            fs.reduce_grads(-1, grads)
+            ws = torch.empty(B_ws_bytes(fs), dtype=torch.uint8, device="cuda")
+            from zero_sharded_mixed_flatparameter_gb300 import binding as B
+            B.zero_clip_grad_norm(fs.ctx, 1e6, ws.data_ptr(), ws.numel(), fs.stream_handle())  # inactive clip
+            fs.step()
+            fs.post_step()
+            for a in starts:
+                oracle.step_window(h, t, [to_np(grads[0][a:a + W])], *win[a])
+            del grads, ws
+        torch.cuda.synchronize()
+        for a in starts:
+            got = (to_np(fs.master[a:a + W]), to_np(fs.exp_avg[a:a + W]), to_np(fs.exp_avg_sq[a:a + W]),
+                   to_np(fs.param16[a:a + W]))
+            for name, g, w in zip(("master", "m", "v", "param16"), got, win[a]):
+                assert_bit_exact(g, w, f"window@{a} {name}")
+        assert lay.total_padded == numel
+    finally:
+        fs.close()
+        torch.cuda.empty_cache()
+
+
+def B_ws_bytes(fs):
+    from zero_sharded_mixed_flatparameter_gb300 import binding as B
+    return B.zero_clip_workspace_bytes(fs.ctx)
