@@ -76,8 +76,10 @@ def measured_peaks():
 
 
 def kernel_source_sha() -> str:
+    """Hash of the step kernel's sources (the kernel whose traffic is recorded)."""
     h = hashlib.sha256()
-    for rel in ("zero_sharded_mixed_flatparameter_gb300/csrc/zero_kernels.cu",
+    for rel in ("zero_sharded_mixed_flatparameter_gb300/csrc/zero_step_kernels.cu",
+                "zero_sharded_mixed_flatparameter_gb300/csrc/zero_device.cuh",
                 "zero_sharded_mixed_flatparameter_gb300/csrc/zero_internal.h"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())

@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(PKG, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "--fmad=false", "-Xcompiler", "-fPIC,-O2",
           "-I" + INCLUDE, "-I" + CSRC]
-SOURCES = ["zero_kernels.cu", "zero_runtime.cpp", "zero_no_alloc.cu"]
+SOURCES = ["zero_step_kernels.cu", "zero_aux_kernels.cu", "zero_runtime.cpp", "zero_no_alloc.cu"]
 
 
 def _nvcc() -> str:
@@ -36,7 +36,8 @@ def _nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, s) for s in SOURCES]
-    files += [os.path.join(CSRC, "zero_internal.h"), os.path.join(INCLUDE, "zero_flatstep.h")]
+    files += [os.path.join(CSRC, "zero_internal.h"), os.path.join(CSRC, "zero_device.cuh"),
+              os.path.join(INCLUDE, "zero_flatstep.h")]
     return files
 
 

@@ -1,5 +1,6 @@
 // Internal interface between the host runtime (zero_runtime.cpp) and the
-// sm_103a kernels (zero_kernels.cu).  Not part of the public ABI.
+// sm_103a kernels (zero_step_kernels.cu, zero_aux_kernels.cu).  Not part of
+// the public ABI.
 #pragma once
 
 #include <cstdint>
@@ -116,6 +117,10 @@ cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaS
 
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
+
+// CTAs for a grid-stride launch of kStepThreads-thread CTAs over work_items
+// items: enough to cover them, at most blocks_per_sm per SM.
+long long grid_for(long long work_items, int sms, int blocks_per_sm);
 
 }  // namespace zfs
 

@@ -1,7 +1,7 @@
 // Host runtime of the ZeRO flat-parameter library: the C ABI declared in
 // include/zero_flatstep.h.  It owns only host metadata — the FlatParameter
 // layout, the registered gradient pointers, the step count and error text —
-// and enqueues the sm_103a kernels of zero_kernels.cu on the caller's stream.
+// and enqueues the sm_103a kernels (zero_step_kernels.cu, zero_aux_kernels.cu) on the caller's stream.
 //
 // Protocol: Femtotron dev log #6 (ShardingStrategy: make_master /
 // reduce_grads / gather_weights / post_step).  Layout: CMU 15-779 Lecture 13
