@@ -320,7 +320,7 @@ def run_ours(args):
         if args.clip > 0:
             if clip_pair is not None:
                 clip_pair[0].record(stream)
-            fs.clip_grad_norm(args.clip)
+            fs.clip_grad_norm(args.clip, keep_reduced=args.clip_keep)
             if clip_pair is not None:
                 clip_pair[1].record(stream)
             launches += fs.last_launches()
@@ -383,7 +383,8 @@ def run_ours(args):
     params_all = aggregate([float(pl.total * args.steps)], "sum", world, device)[0]
     value = params_all / (total_ms_max / 1e3)
 
-    bpp = bytes_per_param(n, wl["grad_dtype"])
+    # with the kept reduced gradient the step reads one fp32 gradient (4 B)
+    bpp = 4 + 26 if (args.clip > 0 and args.clip_keep) else bytes_per_param(n, wl["grad_dtype"])
     bytes_per_launch = bpp * padded
     achieved_gbs = bytes_per_launch / (kern_ms_max / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
@@ -475,8 +476,9 @@ def run_ours(args):
                          "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms)},
             "clip": None if clip_ms is None else {
                 "max_norm": args.clip, "norm_pass_ms_mean": statistics.mean(clip_ms),
-                "norm_pass_bytes": (2 if wl["grad_dtype"] == "bf16" else 4) * n * padded,
-                "norm_pass_gbs": (2 if wl["grad_dtype"] == "bf16" else 4) * n * padded
+                "keep_reduced": args.clip_keep,
+                "norm_pass_bytes": ((2 if wl["grad_dtype"] == "bf16" else 4) * n + (4 if args.clip_keep else 0)) * padded,
+                "norm_pass_gbs": ((2 if wl["grad_dtype"] == "bf16" else 4) * n + (4 if args.clip_keep else 0)) * padded
                 / (statistics.mean(clip_ms) / 1e3) / 1e9,
                 "note": "the clipped step is the norm pass (grad_sq + finalize kernels) plus the step kernel"},
             "gather": None if gather_ms is None else {
@@ -615,6 +617,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--accum", type=int, default=0,
                     help="fp32 gradient accumulation of this many bf16 micro-steps before every step (fp32 workloads)")
+    ap.add_argument("--clip-keep", action="store_true",
+                    help="with --clip: keep the reduced gradient for the step (fewer bytes for N > 4)")
     ap.add_argument("--sweep", action="store_true",
                     help="roofline sweep of flat buffers (one JSON line per point instead of the bench line)")
     ap.add_argument("--sweep-sizes", default="1e6,16e6,128e6,512e6,1e9")

@@ -243,6 +243,30 @@ zero_status zero_clip_grad_norm(zero_ctx* ctx, float max_norm, void* workspace, 
                                 void* stream);
 
 /*
+ * Flag of zero_clip_grad_norm_ex / zero_clip_workspace_bytes_ex: keep the
+ * reduced fp32 gradient in the workspace so that the next zero_step reads it
+ * (4 bytes per element) instead of the N replicas (2N or 4N bytes): the
+ * clipped step then moves 2N + 34 instead of 4N + 26 bytes per element (bf16
+ * replicas), fewer for N > 4.  Results are bit-identical either way.
+ */
+#define ZERO_CLIP_KEEP_REDUCED 1
+
+/* Workspace size of zero_clip_grad_norm_ex for `flags`: with
+ * ZERO_CLIP_KEEP_REDUCED, plus 4 bytes per padded element (256-byte aligned). */
+zero_status zero_clip_workspace_bytes_ex(const zero_ctx* ctx, int32_t flags, int64_t* bytes);
+
+/*
+ * zero_clip_grad_norm_ex — zero_clip_grad_norm with flags (0 or
+ * ZERO_CLIP_KEEP_REDUCED).  With ZERO_CLIP_KEEP_REDUCED the workspace must
+ * hold zero_clip_workspace_bytes_ex(ctx, ZERO_CLIP_KEEP_REDUCED) bytes and
+ * stay allocated and unchanged until the next zero_step has completed; the
+ * registered replica buffers are not read again by that step.
+ * Errors: as zero_clip_grad_norm; ZERO_EINVAL for unknown flags.
+ */
+zero_status zero_clip_grad_norm_ex(zero_ctx* ctx, float max_norm, int32_t flags, void* workspace,
+                                   int64_t workspace_bytes, void* stream);
+
+/*
  * zero_clip_grad_norm_static — zero_clip_grad_norm for callers that cannot
  * allocate device memory (for example code running inside an allocator or
  * an out-of-memory handler, or in a loop where allocation is forbidden), so

@@ -207,7 +207,7 @@ def check_guards(fs: FlatStep, what: str):
 
 
 def run_gpu(pb: Problem, mode: str = "units", every_step=None, guard: int = 64,
-            gather_check: bool = True, norms: Optional[list] = None) -> FlatStep:
+            gather_check: bool = True, norms: Optional[list] = None, clip_keep: bool = False) -> FlatStep:
     fs = gpu_flatstep(pb, guard=guard)
     try:
         for t in range(1, len(pb.grads) + 1):
@@ -215,7 +215,7 @@ def run_gpu(pb: Problem, mode: str = "units", every_step=None, guard: int = 64,
             keep = []
             register(fs, pb, flats, mode, keep)
             if pb.max_norm > 0:
-                fs.clip_grad_norm(pb.max_norm)
+                fs.clip_grad_norm(pb.max_norm, keep_reduced=clip_keep)
                 if norms is not None:
                     norms.append(fs.grad_norm())
             fs.step()

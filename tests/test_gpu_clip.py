@@ -26,13 +26,13 @@ def _built():
     ensure_built()
 
 
-def _clip_parity(pb, mode="units"):
+def _clip_parity(pb, mode="units", keep=False):
     ref_states, ref_norms, gpu_norms = {}, [], []
     oracle_run(pb, every_step=lambda t, s: ref_states.__setitem__(t, s), norms=ref_norms)
 
     def check(t, fs):
         compare_state(fs, ref_states[t], f"clipped step {t}")
-    fs = run_gpu(pb, mode=mode, every_step=check, norms=gpu_norms)
+    fs = run_gpu(pb, mode=mode, every_step=check, norms=gpu_norms, clip_keep=keep)
     fs.close()
     for a, b in zip(gpu_norms, ref_norms):
         assert abs(a - b) <= 1e-12 * abs(b), (a, b)
@@ -193,3 +193,37 @@ def test_full_size_llama_1024_clipped():
     finally:
         fs.close()
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("n,gd,stage", [(8, "bf16", 2), (3, "fp32", 3), (16, "bf16", 0), (5, "bf16", 1)])
+def test_keep_reduced_gradient(n, gd, stage):
+    # the step reads the kept reduced gradient instead of the replicas; the
+    # results are the oracle's bit for bit.  Units of 1,552 at N = 3 or 5 give
+    # unit bases that are not multiples of 4, i.e. unaligned kept stores.
+    pl = si.from_units([16384 * 2 + 5, 1552, 7, 4099])
+    pb = make_problem(pl, n, stage, grad_dtype=gd, steps=3, seed=48 + n, max_norm=0.2)
+    _clip_parity(pb, mode="separate", keep=True)
+    _clip_parity(pb, mode="units", keep=True)
+
+
+def test_keep_reduced_errors():
+    pb = make_problem(si.toy_mlp(), 4, 2, steps=1, seed=49)
+    fs = gpu_flatstep(pb)
+    try:
+        register(fs, pb, upload_grads(pb, 1), "units", [])
+        small = B.zero_clip_workspace_bytes(fs.ctx)
+        big = B.zero_clip_workspace_bytes_ex(fs.ctx, B.ZERO_CLIP_KEEP_REDUCED)
+        assert big >= small + 4 * fs.padded
+        ws = torch.empty(big, dtype=torch.uint8, device="cuda")
+        for flags, nbytes in ((2, big), (B.ZERO_CLIP_KEEP_REDUCED, big - 4)):
+            with pytest.raises(B.ZeroError) as e:
+                B.zero_clip_grad_norm_ex(fs.ctx, 1.0, flags, ws.data_ptr(), nbytes, 0)
+            assert e.value.status == B.ZERO_EINVAL
+        with pytest.raises(B.ZeroError):
+            B.zero_clip_workspace_bytes_ex(fs.ctx, 4)
+        B.zero_clip_grad_norm_ex(fs.ctx, 1.0, B.ZERO_CLIP_KEEP_REDUCED, ws.data_ptr(), big, fs.stream_handle())
+        fs.step()
+        assert B.zero_last_launches(fs.ctx) == 1
+        fs.post_step()
+    finally:
+        fs.close()

@@ -28,8 +28,9 @@ EXPORTED = (
     "zero_step", "zero_gather_weights", "zero_post_step", "zero_step_count", "zero_last_launches", "zero_set_lr",
     "zero_destroy", "zero_last_error", "zero_status_string", "zero_clip_workspace_bytes", "zero_clip_grad_norm",
     "zero_grad_norm", "zero_clip_grad_norm_static", "zero_accumulate_grads", "zero_export_state",
-    "zero_import_state",
+    "zero_import_state", "zero_clip_workspace_bytes_ex", "zero_clip_grad_norm_ex",
 )
+ZERO_CLIP_KEEP_REDUCED = 1
 
 
 class zero_config(ctypes.Structure):
@@ -90,6 +91,8 @@ def load(path: str = LIB_PATH):
             "zero_accumulate_grads": [vp, i32, vp, vp, i32, vp],
             "zero_export_state": [vp, vp, vp, vp, P(i64), vp],
             "zero_import_state": [vp, vp, vp, vp, i64, vp],
+            "zero_clip_workspace_bytes_ex": [vp, i32, P(i64)],
+            "zero_clip_grad_norm_ex": [vp, f32, i32, vp, i64, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -247,6 +250,18 @@ def zero_clip_workspace_bytes(ctx: int) -> int:
 
 def zero_clip_grad_norm(ctx: int, max_norm: float, workspace: int, workspace_bytes: int, stream: int = 0) -> None:
     _check(load().zero_clip_grad_norm(ctx, max_norm, workspace or None, workspace_bytes, stream or None), ctx)
+
+
+def zero_clip_workspace_bytes_ex(ctx: int, flags: int) -> int:
+    n = ctypes.c_int64()
+    _check(load().zero_clip_workspace_bytes_ex(ctx, flags, ctypes.byref(n)), ctx)
+    return n.value
+
+
+def zero_clip_grad_norm_ex(ctx: int, max_norm: float, flags: int, workspace: int, workspace_bytes: int,
+                           stream: int = 0) -> None:
+    _check(load().zero_clip_grad_norm_ex(ctx, max_norm, flags, workspace or None, workspace_bytes,
+                                         stream or None), ctx)
 
 
 def zero_clip_grad_norm_static(ctx: int, max_norm: float, stream: int = 0) -> None:

@@ -37,6 +37,7 @@ def _nvcc() -> str:
 def _inputs():
     files = [os.path.join(CSRC, s) for s in SOURCES]
     files += [os.path.join(CSRC, "zero_internal.h"), os.path.join(CSRC, "zero_device.cuh"),
+              os.path.join(CSRC, "zero_aux_internal.h"),
               os.path.join(INCLUDE, "zero_flatstep.h")]
     return files
 

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "zero_device.cuh"
+#include "zero_aux_internal.h"
 #include "zero_internal.h"
 
 namespace zfs {
@@ -145,6 +146,17 @@ __device__ __forceinline__ float reduced1(const NormArgs& a, const NormSeg& s, l
   return __fmul_rn(acc, a.inv_n);
 }
 
+// Stores 8 reduced gradients of a unit at unit-relative element e0.
+__device__ __forceinline__ void keep8(const NormSeg& s, long long e0, const float* g) {
+  float* p = s.keep + e0;
+  if (s.keep_vec) {
+    st_stream_f4(p, make_float4(g[0], g[1], g[2], g[3]));
+    st_stream_f4(p + 4, make_float4(g[4], g[5], g[6], g[7]));
+  } else {
+    for (int e = 0; e < kVec; ++e) p[e] = g[e];
+  }
+}
+
 // One CTA per chunk.  Thread t takes the chunk's 8-element groups t, t+256,
 // ... in order and accumulates their elements in order; the vector and the
 // element-wise paths visit elements in the same order, so the chunk's sum does
@@ -168,6 +180,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) grad_sq_kernel(const __grid_c
     float g0[kVec], g1[kVec];
     reduced8<N, kFp32>(a, s, c0 + grp * kVec, g0);
     reduced8<N, kFp32>(a, s, c0 + (grp + kStepThreads) * kVec, g1);
+    if (s.keep) {
+      keep8(s, c0 + grp * kVec, g0);
+      keep8(s, c0 + (grp + kStepThreads) * kVec, g1);
+    }
     acc.add8(g0);
     acc.add8(g1);
   }
@@ -176,10 +192,15 @@ __global__ void __launch_bounds__(kStepThreads, 1) grad_sq_kernel(const __grid_c
     if (s.vec_ok && grp * kVec + kVec <= len) {
       float g[kVec];
       reduced8<N, kFp32>(a, s, e0, g);
+      if (s.keep) keep8(s, e0, g);
       acc.add8(g);
     } else {
       for (int e = 0; e < kVec; ++e) {
-        if (grp * kVec + e < len) acc.add1(reduced1(a, s, e0 + e));
+        if (grp * kVec + e < len) {
+          const float g = reduced1(a, s, e0 + e);
+          if (s.keep) s.keep[e0 + e] = g;
+          acc.add1(g);
+        }
       }
     }
   }

@@ -51,69 +51,12 @@ struct StepArgs {
   Seg seg[kMaxSegs];
 };
 
-// Global-norm clipping.  The squared norm of the reduced gradient is summed
-// over fixed unit-relative chunks of kClipChunk elements (the last chunk of a
-// unit also takes the unit's zero pads), each chunk in a fixed order, then
-// the chunk sums in chunk order: the result does not depend on the stage
-// (padding) or on how the grid is scheduled.
-constexpr long long kClipChunk = 16384;
-constexpr int kFinalizeThreads = 1024;
-
-// Workspace layout: [0] double norm, [8] float coefficient, [32..] double chunk partials.
-constexpr long long kClipHeaderBytes = 32;
-
-struct NormSeg {
-  long long len;          // padded unit length (elements)
-  long long n_chunks;     // chunks of this unit
-  long long chunk_start;  // first chunk's index within this launch
-  long long out_start;    // first chunk's index in the workspace partials
-  int vec_ok;             // 16-byte aligned gradients: vector loads allowed
-  const void* g[kMaxRanks];
-};
-
-struct NormArgs {
-  int n_ranks;
-  int grad_fp32;
-  float inv_n;
-  int nseg;
-  double* partials;
-  NormSeg seg[kMaxSegs];
-};
-
-// Norm pass: one CTA per chunk; writes one partial per chunk.
-cudaError_t launch_grad_sq(const NormArgs& a, long long chunks, cudaStream_t stream);
-// Sums n partials in a fixed order and writes the norm and the clip
-// coefficient min(1, max_norm / (norm + 1e-6)) into the workspace header.
-cudaError_t launch_clip_finalize(void* workspace, long long n_partials, float max_norm, cudaStream_t stream);
-
 // Launchers.  Each returns the cudaError_t of its launch.
 // Vector kernel: every segment has base % kVec == 0 and 16-byte aligned
 // gradient pointers; the last kVec-1 elements of a segment may be ragged.
 cudaError_t launch_step_vec(const StepArgs& a, cudaStream_t stream);
 // Scalar kernel: any alignment (used for segments the vector kernel cannot take).
 cudaError_t launch_step_scalar(const StepArgs& a, cudaStream_t stream);
-
-// make_master pieces.
-cudaError_t launch_zero_fill(float* master, float* m, float* v, uint16_t* p16, long long n,
-                             cudaStream_t stream);
-cudaError_t launch_copy_param(const float* src, float* master, uint16_t* p16, long long offset,
-                              long long n, cudaStream_t stream);
-// Plain fp32 copy of n elements (checkpoint export/import).
-cudaError_t launch_copy_f32(const float* src, float* dst, long long n, cudaStream_t stream);
-
-// fp32 gradient accumulation of one micro-step: for every replica r,
-// acc[r][j] = (first ? 0 : acc[r][j]) + widen(micro[r][j]), j < n.
-struct AccumArgs {
-  int n_ranks;
-  int first;
-  long long n;
-  const uint16_t* micro[kMaxRanks];
-  float* acc[kMaxRanks];
-};
-cudaError_t launch_accumulate(const AccumArgs& a, bool vec, cudaStream_t stream);
-
-// ZeRO-3 unit gather: copy n bf16 elements; *launches counts the kernels enqueued.
-cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaStream_t stream, int* launches);
 
 // Multiprocessor count of the current device (cached per device).
 int sm_count();

@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include "zero_flatstep.h"
+#include "zero_aux_internal.h"
 #include "zero_internal.h"
 
 namespace {
@@ -54,6 +55,9 @@ struct zero_ctx {
   // post_step) and of the last clip run (for zero_grad_norm).
   char* clip_ws = nullptr;
   char* last_clip_ws = nullptr;
+  // With ZERO_CLIP_KEEP_REDUCED: the reduced fp32 gradient (padded_total
+  // elements) the pending step reads instead of the replicas.
+  float* clip_keep = nullptr;
 
   std::string error;
 };
@@ -535,42 +539,95 @@ zero_status zero_step(zero_ctx* ctx, void* stream) {
     if (!ctx->registered[i]) return fail(ctx, ZERO_ESTATE, "unit %d has no registered gradients", i);
   }
   const int64_t t = ctx->t + 1;
-  std::vector<PlannedSeg> vec_segs, scalar_segs;
-  try {
-    for (const PlannedSeg& s : build_segments(ctx)) {
-      (vector_ok(s, ctx->cfg.n_ranks) ? vec_segs : scalar_segs).push_back(s);
-    }
-  } catch (const std::bad_alloc&) {
-    return fail(ctx, ZERO_ENOMEM, "cannot allocate segment list");
-  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t launches = 0;
-  st = launch_batches(ctx, vec_segs, true, t, s, &launches);
-  if (st != ZERO_OK) return st;
-  st = launch_batches(ctx, scalar_segs, false, t, s, &launches);
-  if (st != ZERO_OK) return st;
+  if (ctx->clip_keep) {
+    // The clip kept the reduced gradient: one fp32 "replica" over the whole
+    // padded buffer, already scaled by 1/N (x 1 below is exact).
+    if (ctx->padded_total > 0) {
+      zfs::StepArgs a;
+      std::memset(&a, 0, sizeof a);
+      a.master = ctx->bufs.master;
+      a.m = ctx->bufs.exp_avg;
+      a.v = ctx->bufs.exp_avg_sq;
+      a.p16 = static_cast<uint16_t*>(ctx->bufs.param16);
+      a.clip = reinterpret_cast<const float*>(ctx->clip_ws + 8);
+      fill_scalars(ctx, t, &a);
+      a.inv_n = 1.0f;
+      a.n_ranks = 1;
+      a.grad_fp32 = 1;
+      a.nseg = 1;
+      a.seg[0].base = 0;
+      a.seg[0].len = ctx->padded_total;
+      a.seg[0].vec_start = 0;
+      a.seg[0].g[0] = ctx->clip_keep;
+      a.total_vec = ctx->padded_total / zfs::kVec;
+      a.total_elems = ctx->padded_total;
+      const cudaError_t e = zfs::launch_step_vec(a, s);
+      if (e != cudaSuccess) return fail_cuda(ctx, "step kernel launch", e);
+      launches = 1;
+    }
+  } else {
+    std::vector<PlannedSeg> vec_segs, scalar_segs;
+    try {
+      for (const PlannedSeg& sg : build_segments(ctx)) {
+        (vector_ok(sg, ctx->cfg.n_ranks) ? vec_segs : scalar_segs).push_back(sg);
+      }
+    } catch (const std::bad_alloc&) {
+      return fail(ctx, ZERO_ENOMEM, "cannot allocate segment list");
+    }
+    st = launch_batches(ctx, vec_segs, true, t, s, &launches);
+    if (st != ZERO_OK) return st;
+    st = launch_batches(ctx, scalar_segs, false, t, s, &launches);
+    if (st != ZERO_OK) return st;
+  }
   ctx->last_launches = launches;
   ctx->t = t;
   ctx->phase = Phase::kStepped;
   return ZERO_OK;
 }
 
+namespace {
+
+int64_t clip_partials_end(const zero_ctx* ctx) { return zfs::kClipHeaderBytes + 8 * total_chunks(ctx); }
+
+// Byte offset of the kept reduced gradient inside the workspace.
+int64_t clip_keep_offset(const zero_ctx* ctx) { return (clip_partials_end(ctx) + 255) / 256 * 256; }
+
+int64_t clip_bytes(const zero_ctx* ctx, int32_t flags) {
+  return (flags & ZERO_CLIP_KEEP_REDUCED) ? clip_keep_offset(ctx) + 4 * ctx->padded_total : clip_partials_end(ctx);
+}
+
+}  // namespace
+
 zero_status zero_clip_workspace_bytes(const zero_ctx* ctx, int64_t* bytes) {
+  return zero_clip_workspace_bytes_ex(ctx, 0, bytes);
+}
+
+zero_status zero_clip_workspace_bytes_ex(const zero_ctx* ctx, int32_t flags, int64_t* bytes) {
   if (!ctx || !bytes) return fail(nullptr, ZERO_EINVAL, "NULL argument");
-  *bytes = zfs::kClipHeaderBytes + 8 * total_chunks(ctx);
+  if (flags & ~ZERO_CLIP_KEEP_REDUCED) return fail(const_cast<zero_ctx*>(ctx), ZERO_EINVAL, "unknown clip flags");
+  *bytes = clip_bytes(ctx, flags);
   return ZERO_OK;
 }
 
 zero_status zero_clip_grad_norm(zero_ctx* ctx, float max_norm, void* workspace, int64_t workspace_bytes,
                                 void* stream) {
+  return zero_clip_grad_norm_ex(ctx, max_norm, 0, workspace, workspace_bytes, stream);
+}
+
+zero_status zero_clip_grad_norm_ex(zero_ctx* ctx, float max_norm, int32_t flags, void* workspace,
+                                   int64_t workspace_bytes, void* stream) {
   if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  if (flags & ~ZERO_CLIP_KEEP_REDUCED) return fail(ctx, ZERO_EINVAL, "unknown clip flags");
+  const bool keep = (flags & ZERO_CLIP_KEEP_REDUCED) != 0;
   zero_status st = require_bound(ctx);
   if (st != ZERO_OK) return st;
   if (ctx->phase == Phase::kStepped) return fail(ctx, ZERO_ESTATE, "clip after step: call post_step first");
   int32_t missing = -1;
   if (!all_registered(ctx, &missing)) return fail(ctx, ZERO_ESTATE, "unit %d has no registered gradients", missing);
   if (!(max_norm > 0.0f) || !std::isfinite(max_norm)) return fail(ctx, ZERO_EINVAL, "max_norm must be finite and > 0");
-  const int64_t need = zfs::kClipHeaderBytes + 8 * total_chunks(ctx);
+  const int64_t need = clip_bytes(ctx, flags);
   if (!workspace) return fail(ctx, ZERO_EINVAL, "workspace is NULL");
   if (!aligned(workspace, 16)) return fail(ctx, ZERO_EINVAL, "workspace is not 16-byte aligned");
   if (workspace_bytes < need)
@@ -580,6 +637,7 @@ zero_status zero_clip_grad_norm(zero_ctx* ctx, float max_norm, void* workspace, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   double* partials = reinterpret_cast<double*>(ws + zfs::kClipHeaderBytes);
+  float* keep_base = keep ? reinterpret_cast<float*>(ws + clip_keep_offset(ctx)) : nullptr;
   const int N = ctx->cfg.n_ranks;
   const size_t esz = grad_bytes(ctx->cfg);
   int32_t launches = 0;
@@ -603,6 +661,8 @@ zero_status zero_clip_grad_norm(zero_ctx* ctx, float max_norm, void* workspace, 
       g.chunk_start = chunks;
       g.out_start = out;
       g.vec_ok = 1;
+      g.keep = keep ? keep_base + ctx->unit_base[i] : nullptr;
+      g.keep_vec = keep && aligned(g.keep, 16) ? 1 : 0;
       for (int r = 0; r < N; ++r) {
         g.g[r] = ctx->grads[static_cast<size_t>(i) * zfs::kMaxRanks + r];
         if (!aligned(g.g[r], 16)) g.vec_ok = 0;
@@ -623,6 +683,7 @@ zero_status zero_clip_grad_norm(zero_ctx* ctx, float max_norm, void* workspace, 
   ctx->last_launches = launches + 1;
   ctx->clip_ws = ws;
   ctx->last_clip_ws = ws;
+  ctx->clip_keep = keep_base;
   return ZERO_OK;
 }
 
@@ -673,6 +734,7 @@ zero_status zero_post_step(zero_ctx* ctx, void* stream) {
   std::fill(ctx->registered.begin(), ctx->registered.end(), 0);
   std::fill(ctx->grads.begin(), ctx->grads.end(), nullptr);
   ctx->clip_ws = nullptr;
+  ctx->clip_keep = nullptr;
   ctx->phase = Phase::kReady;
   return ZERO_OK;
 }

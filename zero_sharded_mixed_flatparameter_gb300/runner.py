@@ -119,14 +119,17 @@ class FlatStep:
         B.zero_reduce_grads(self.ctx, unit, [g.data_ptr() for g in replica_grads], self.stream_handle(stream))
         self._registered.append(list(replica_grads))  # keep alive until post_step
 
-    def clip_grad_norm(self, max_norm: float, stream=None) -> None:
+    def clip_grad_norm(self, max_norm: float, keep_reduced: bool = False, stream=None) -> None:
         """Global-norm clipping of the registered gradients for the next step
-        (the workspace is allocated once, by torch, and reused)."""
-        need = B.zero_clip_workspace_bytes(self.ctx)
+        (the workspace is allocated once, by torch, and reused).  keep_reduced
+        lets the next step read the kept reduced gradient instead of the N
+        replicas (more workspace, fewer bytes moved for N > 4)."""
+        flags = B.ZERO_CLIP_KEEP_REDUCED if keep_reduced else 0
+        need = B.zero_clip_workspace_bytes_ex(self.ctx, flags)
         if getattr(self, "_clip_ws", None) is None or self._clip_ws.numel() < need:
             self._clip_ws = torch.empty(need, dtype=torch.uint8, device=self.device)
-        B.zero_clip_grad_norm(self.ctx, max_norm, self._clip_ws.data_ptr(), self._clip_ws.numel(),
-                              self.stream_handle(stream))
+        B.zero_clip_grad_norm_ex(self.ctx, max_norm, flags, self._clip_ws.data_ptr(), self._clip_ws.numel(),
+                                 self.stream_handle(stream))
 
     def grad_norm(self, stream=None) -> float:
         """Norm of the last clip (synchronizes the stream)."""
