@@ -226,11 +226,13 @@ __global__ void __launch_bounds__(kFinalizeThreads) clip_finalize_kernel(char* w
 // fp32 gradient accumulation (one micro-step).  The replicas' buffers form
 // one concatenated index space for the grid-stride loop; 8 elements per
 // vector: one 16-byte bf16 load, two 16-byte fp32 loads (none on the first
-// micro-step) and two 16-byte fp32 stores.  A thread loads kAccumIlp vectors
-// before adding any (48 bytes per vector are too few to keep HBM busy at
-// 512 threads per SM).
+// micro-step) and two 16-byte fp32 stores.  A thread loads kIlp vectors
+// before adding any.  Measured on GB300 (2 CTAs/SM): 2 vectors give 6741 GB/s
+// on later micro-steps (4 gave 5861, 8 gave 6314); the write-heavy first
+// micro-step does best with 8 (6245 GB/s; 2 gave 5833).
 // ---------------------------------------------------------------------------
-constexpr int kAccumIlp = 4;
+constexpr int kAccumIlpFirst = 8;
+constexpr int kAccumIlpLater = 2;
 
 __device__ __forceinline__ void accumulate8(const uint4 raw, const float4 x0, const float4 x1, bool first, float* p) {
   float g[kVec] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
@@ -245,6 +247,7 @@ __device__ __forceinline__ void accumulate8(const uint4 raw, const float4 x0, co
   st_stream_f4(p + 4, make_float4(g[4], g[5], g[6], g[7]));
 }
 
+template <int kAccumIlp>
 __global__ void __launch_bounds__(kStepThreads, 1) accumulate_vec_kernel(const __grid_constant__ AccumArgs a) {
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -404,7 +407,11 @@ cudaError_t launch_accumulate(const AccumArgs& a, bool vec, cudaStream_t stream)
     long long work = (a.n / kVec) * a.n_ranks;
     if (work < static_cast<long long>(a.n_ranks) * kVec) work = static_cast<long long>(a.n_ranks) * kVec;
     const long long grid = grid_for(work, sms, kStepCtasPerSm);
-    accumulate_vec_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(a);
+    if (a.first) {
+      accumulate_vec_kernel<kAccumIlpFirst><<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(a);
+    } else {
+      accumulate_vec_kernel<kAccumIlpLater><<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(a);
+    }
   } else {
     const long long grid = grid_for(a.n * a.n_ranks, sms, 8);
     accumulate_scalar_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(a);
