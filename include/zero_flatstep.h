@@ -168,8 +168,9 @@ zero_status zero_stage3_peak_bytes(const zero_ctx* ctx, int64_t* peak_bytes, int
  * until the zero_step that consumes them has completed on its stream.
  * Registering a unit again replaces its pointers.
  * Errors: ZERO_EINVAL (unit out of range, null pointer, pointer not aligned to
- * the element size); ZERO_ESTATE if no buffers are bound or a step is pending
- * its post_step.
+ * the element size); ZERO_ESTATE if no buffers are bound, a step is pending
+ * its post_step, or a clip is pending (zero_clip_grad_norm ran on the
+ * gradients registered before it: register every unit first, then clip).
  */
 zero_status zero_reduce_grads(zero_ctx* ctx, int32_t unit, const void* const* replica_grads,
                               void* stream);
@@ -207,7 +208,10 @@ zero_status zero_accumulate_grads(zero_ctx* ctx, int32_t unit, const void* const
  * g is multiplied by the clip coefficient before Adam.  Requires every unit's
  * gradients registered since the last post_step.
  * Errors: ZERO_ESTATE (no buffers, missing gradients, step already taken
- * without post_step); ZERO_ECUDA (launch failure; t is left unchanged).
+ * without post_step); ZERO_ECUDA (a launch failed; t is left unchanged, but
+ * when a step needs more than one launch — more than 48 gradient segments, or
+ * both aligned and unaligned ones — launches enqueued before the failing one
+ * have updated their elements).
  */
 zero_status zero_step(zero_ctx* ctx, void* stream);
 

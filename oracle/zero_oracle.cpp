@@ -24,7 +24,7 @@
 //  * Femtotron dev logs #4/#5 (mixed-precision step order: bf16 grad -> fp32,
 //    AdamW on the fp32 master, master -> bf16 compute copy).
 //
-// Readings taken where the pages are silent (each is listed in the design doc):
+// Readings taken where the pages are silent:
 //  * Reduce: each replica's gradient is widened exactly to fp32 and summed in
 //    rank order 0..N-1 starting from replica 0's value, then multiplied by
 //    fp32(1/N) (= 1.0f / N).  Never rounded back to bf16.

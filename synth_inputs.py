@@ -6,7 +6,7 @@ how they group into FlatParameter units) and draws seeded random values.  It
 contains none of the method's arithmetic (no padding, reduction, Adam or
 rounding of results).
 
-Value recipe (every draw is seeded; see DESIGN.md "Inputs"):
+Value recipe (every draw is seeded):
   * fp32 initial parameters ~ N(0, 0.02)
   * replica gradients ~ N(0, sigma), stored as bf16 (torch's round-to-nearest
     conversion of the fp32 draw) or as fp32; optional outliers: a seeded

@@ -227,3 +227,22 @@ def test_keep_reduced_errors():
         fs.post_step()
     finally:
         fs.close()
+
+
+def test_registration_after_clip_is_refused():
+    pb = make_problem(si.toy_mlp(), 4, 2, steps=1, seed=50, max_norm=0.5)
+    fs = gpu_flatstep(pb)
+    try:
+        flats = upload_grads(pb, 1)
+        register(fs, pb, flats, "units", [])
+        fs.clip_grad_norm(0.5)
+        with pytest.raises(B.ZeroError) as e:
+            fs.reduce_grads(-1, flats)
+        assert e.value.status == B.ZERO_ESTATE and "clip" in B.zero_last_error(fs.ctx)
+        fs.step()   # the pending clip and the earlier registration still stand
+        fs.post_step()
+        register(fs, pb, flats, "all", [])   # allowed again after post_step
+        fs.step()
+        fs.post_step()
+    finally:
+        fs.close()

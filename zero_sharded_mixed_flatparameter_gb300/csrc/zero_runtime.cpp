@@ -469,6 +469,9 @@ zero_status zero_reduce_grads(zero_ctx* ctx, int32_t unit, const void* const* re
   zero_status st = require_bound(ctx);
   if (st != ZERO_OK) return st;
   if (ctx->phase == Phase::kStepped) return fail(ctx, ZERO_ESTATE, "reduce_grads after step: call post_step first");
+  if (ctx->clip_ws)
+    return fail(ctx, ZERO_ESTATE, "reduce_grads after zero_clip_grad_norm: the clip was computed from the "
+                                  "gradients registered before it; register all units, then clip");
   if (unit < -1 || unit >= ctx->n_units) return fail(ctx, ZERO_EINVAL, "unit %d out of range", unit);
   if (!replica_grads) return fail(ctx, ZERO_EINVAL, "replica_grads is NULL");
   const int N = ctx->cfg.n_ranks;
