@@ -75,6 +75,16 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def step_kernel_name(n: int, grad_dtype: str, clip_keep: bool) -> str:
+    """The step kernel the library launches for this workload: the tile-staged
+    one for N >= 14 bf16 or N = 8, 9 fp32 replicas, the register-staged one
+    otherwise (a kept fp32 reduced gradient is one fp32 replica)."""
+    if clip_keep:
+        n, grad_dtype = 1, "fp32"
+    staged = n >= 14 if grad_dtype == "bf16" else n in (8, 9)
+    return "step_tma_kernel" if staged else "step_vec_kernel"
+
+
 def kernel_source_sha() -> str:
     """Hash of the step kernel's sources (the kernel whose traffic is recorded)."""
     h = hashlib.sha256()
@@ -472,7 +482,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                          "frac": achieved_gbs / peak, "peak_source": f"hbm_gbs {peak_kind}",
                          "traffic": traffic, "algorithmic_bytes_per_launch": bytes_per_launch,
-                         "bytes_per_param": bpp, "kernel": "step_vec_kernel",
+                         "bytes_per_param": bpp, "kernel": step_kernel_name(n, wl["grad_dtype"], args.clip_keep),
                          "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms)},
             "clip": None if clip_ms is None else {
                 "max_norm": args.clip, "norm_pass_ms_mean": statistics.mean(clip_ms),

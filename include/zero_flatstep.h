@@ -343,6 +343,16 @@ zero_status zero_export_state(zero_ctx* ctx, float* master_out, float* exp_avg_o
 zero_status zero_import_state(zero_ctx* ctx, const float* master_in, const float* exp_avg_in,
                               const float* exp_avg_sq_in, int64_t t, void* stream);
 
+/*
+ * zero_kernel_timeouts — how many bounded waits of the tile-staged step
+ * kernel (used for N >= 14 bf16 or N = 8, 9 fp32 replicas) gave up on the
+ * current device since the library was loaded.  A wait gives up only if a
+ * bulk copy never lands; the CTA then leaves the rest of its tiles unchanged,
+ * so a non-zero count means some step is incomplete.  Reads a device counter:
+ * synchronizes with the device.  ctx may be NULL.
+ */
+zero_status zero_kernel_timeouts(const zero_ctx* ctx, uint32_t* count);
+
 /* Number of steps taken (t). */
 zero_status zero_step_count(const zero_ctx* ctx, int64_t* t);
 

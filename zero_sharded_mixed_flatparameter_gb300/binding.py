@@ -28,7 +28,7 @@ EXPORTED = (
     "zero_step", "zero_gather_weights", "zero_post_step", "zero_step_count", "zero_last_launches", "zero_set_lr",
     "zero_destroy", "zero_last_error", "zero_status_string", "zero_clip_workspace_bytes", "zero_clip_grad_norm",
     "zero_grad_norm", "zero_clip_grad_norm_static", "zero_accumulate_grads", "zero_export_state",
-    "zero_import_state", "zero_clip_workspace_bytes_ex", "zero_clip_grad_norm_ex",
+    "zero_import_state", "zero_clip_workspace_bytes_ex", "zero_clip_grad_norm_ex", "zero_kernel_timeouts",
 )
 ZERO_CLIP_KEEP_REDUCED = 1
 
@@ -93,6 +93,7 @@ def load(path: str = LIB_PATH):
             "zero_import_state": [vp, vp, vp, vp, i64, vp],
             "zero_clip_workspace_bytes_ex": [vp, i32, P(i64)],
             "zero_clip_grad_norm_ex": [vp, f32, i32, vp, i64, vp],
+            "zero_kernel_timeouts": [vp, P(ctypes.c_uint32)],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -224,6 +225,12 @@ def zero_import_state(ctx: int, master_in: int, exp_avg_in: int, exp_avg_sq_in: 
                       stream: int = 0) -> None:
     _check(load().zero_import_state(ctx, master_in or None, exp_avg_in or None, exp_avg_sq_in or None, t,
                                     stream or None), ctx)
+
+
+def zero_kernel_timeouts(ctx: int | None = None) -> int:
+    n = ctypes.c_uint32()
+    _check(load().zero_kernel_timeouts(ctx, ctypes.byref(n)), ctx)
+    return n.value
 
 
 def zero_step_count(ctx: int) -> int:

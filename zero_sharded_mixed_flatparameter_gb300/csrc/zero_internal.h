@@ -14,6 +14,11 @@ constexpr int kMaxSegs = 48;      // gradient segments per step launch
 constexpr int kVec = 8;           // elements per thread-iteration (16 B of bf16)
 constexpr int kStepThreads = 256; // threads per CTA of the step kernels
 constexpr int kStepCtasPerSm = 2; // resident CTAs per SM of the vector step kernel
+// Tile-staged (TMA bulk copy) step kernel: used from this many replicas on.
+constexpr int kTmaMinRanks = 14;     // bf16 replicas
+constexpr int kTmaMinRanksFp32 = 8;  // fp32 replicas (8 and 9 only)
+constexpr long long kTmaTile = 2048; // elements per tile (one 8-element vector per thread)
+constexpr int kTmaStages = 2;        // tiles in flight per CTA
 
 // A run of consecutive flat elements whose N replica gradients are
 // contiguous buffers: element base + k reads g[r][k].
@@ -60,6 +65,10 @@ cudaError_t launch_step_scalar(const StepArgs& a, cudaStream_t stream);
 
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
+
+// Bounded waits of the tile-staged step kernel that gave up on the current
+// device since the library was loaded (0xFFFFFFFF if it cannot be read).
+unsigned int step_timeouts();
 
 // CTAs for a grid-stride launch of kStepThreads-thread CTAs over work_items
 // items: enough to cover them, at most blocks_per_sm per SM.

@@ -812,6 +812,14 @@ zero_status zero_import_state(zero_ctx* ctx, const float* master_in, const float
   return ZERO_OK;
 }
 
+zero_status zero_kernel_timeouts(const zero_ctx* ctx, uint32_t* count) {
+  if (!count) return fail(const_cast<zero_ctx*>(ctx), ZERO_EINVAL, "count is NULL");
+  const unsigned int v = zfs::step_timeouts();
+  if (v == 0xFFFFFFFFu) return fail(const_cast<zero_ctx*>(ctx), ZERO_ECUDA, "cannot read the timeout counter");
+  *count = v;
+  return ZERO_OK;
+}
+
 zero_status zero_step_count(const zero_ctx* ctx, int64_t* t) {
   if (!ctx || !t) return fail(nullptr, ZERO_EINVAL, "NULL argument");
   *t = ctx->t;

@@ -152,6 +152,211 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
 }
 
 // ---------------------------------------------------------------------------
+// Staged kernel for many replicas: TMA (1-D bulk copy) of whole tiles.
+//
+// With N >= kTmaMinRanks bf16 replicas (N = 8 or 9 fp32) the step is
+// read-heavy and has 3 + N input streams.  Here one thread per CTA moves each
+// kTmaTile-element tile of every input stream into shared memory with one
+// cp.async.bulk per stream (4-8 KB contiguous requests), completing on an
+// mbarrier; kTmaStages tiles are in flight per CTA.  Measured on GB300 over a
+// 100 M-element buffer (GB/s, staged against register-staged): bf16 N = 14
+// 6988 / 6645, N = 15 7097 / 6632, N = 16 7146 / 6618; fp32 N = 8 7164 /
+// 6651, N = 9 7190 / 6634.  At bf16 N <= 13, fp32 N = 7 and fp32 N >= 10 the
+// register-staged kernel is as fast or faster, so it stays the default there.
+// The arithmetic and its order are those of step_vec8, so the results are
+// bit-identical.  Every wait is bounded: a CTA that gives up (which needs a
+// copy that never lands) counts it in g_step_timeouts and
+// leaves; the host can read the counter with zero_kernel_timeouts.
+// ---------------------------------------------------------------------------
+__device__ unsigned int g_step_timeouts = 0;
+
+constexpr long long kTmaWaitLimit = 1LL << 22;  // try_wait attempts before giving up
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Global -> this CTA's shared memory; completes `bytes` on the mbarrier.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+template <int N, bool kFp32>
+struct TmaTile {
+  static constexpr uint32_t kGradBytes = kTmaTile * (kFp32 ? 4 : 2);
+  static constexpr uint32_t kStateBytes = kTmaTile * 4;
+  static constexpr uint32_t kStageBytes = N * kGradBytes + 3 * kStateBytes;
+  static constexpr uint32_t kSmemBytes = kStageBytes * kTmaStages;
+};
+
+// Full tiles of a launch, segment after segment: tile id -> (segment, tile).
+__device__ __forceinline__ void locate_tile(const StepArgs& a, long long id, int* si, long long* ti) {
+  int s = 0;
+  while (id >= a.seg[s].len / kTmaTile) {
+    id -= a.seg[s].len / kTmaTile;
+    ++s;
+  }
+  *si = s;
+  *ti = id;
+}
+
+template <int N, bool kFp32>
+__global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_constant__ StepArgs a) {
+  using L = TmaTile<N, kFp32>;
+  static_assert(kTmaTile == kStepThreads * kVec, "one 8-element vector per thread per tile");
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t bars[kTmaStages];
+  long long n_tiles = 0;
+  for (int s = 0; s < a.nseg; ++s) n_tiles += a.seg[s].len / kTmaTile;
+  const float clip = a.clip ? *a.clip : 1.0f;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTmaStages; ++s) mbar_init(&bars[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  auto issue = [&](long long id, int stage) {  // thread 0 only
+    int si;
+    long long ti;
+    locate_tile(a, id, &si, &ti);
+    const Seg& sg = a.seg[si];
+    unsigned char* st = smem + static_cast<size_t>(stage) * L::kStageBytes;
+    const long long e0 = ti * kTmaTile;
+    mbar_expect_tx(&bars[stage], L::kStageBytes);
+    for (int r = 0; r < N; ++r)
+      bulk_load(st + r * L::kGradBytes, static_cast<const char*>(sg.g[r]) + e0 * (kFp32 ? 4 : 2), L::kGradBytes,
+                &bars[stage]);
+    const long long j0 = sg.base + e0;
+    bulk_load(st + N * L::kGradBytes, a.master + j0, L::kStateBytes, &bars[stage]);
+    bulk_load(st + N * L::kGradBytes + L::kStateBytes, a.m + j0, L::kStateBytes, &bars[stage]);
+    bulk_load(st + N * L::kGradBytes + 2 * L::kStateBytes, a.v + j0, L::kStateBytes, &bars[stage]);
+  };
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kTmaStages; ++i) {
+      const long long id = blockIdx.x + static_cast<long long>(i) * gridDim.x;
+      if (id < n_tiles) issue(id, i);
+    }
+  }
+  bool gave_up = false;
+  for (long long k = 0;; ++k) {
+    const long long id = blockIdx.x + k * gridDim.x;
+    if (id >= n_tiles) break;
+    const int stage = static_cast<int>(k % kTmaStages);
+    const uint32_t parity = static_cast<uint32_t>((k / kTmaStages) & 1);
+    long long tries = 0;
+    bool mine = false;
+    while (!mbar_try_wait(&bars[stage], parity)) {
+      if (++tries > kTmaWaitLimit) {
+        mine = true;
+        break;
+      }
+    }
+    // Every thread reaches this barrier; the CTA gives up together or not at all.
+    if (__syncthreads_or(mine ? 1 : 0)) {
+      gave_up = true;
+      if (threadIdx.x == 0) atomicAdd(&g_step_timeouts, 1u);
+      break;
+    }
+    const unsigned char* st = smem + static_cast<size_t>(stage) * L::kStageBytes;
+    const int t8 = threadIdx.x * kVec;
+    float g[kVec];
+    if constexpr (!kFp32) {
+      const uint4 r0 = *reinterpret_cast<const uint4*>(st + t8 * 2);
+      g[0] = bf16_lo(r0.x); g[1] = bf16_hi(r0.x); g[2] = bf16_lo(r0.y); g[3] = bf16_hi(r0.y);
+      g[4] = bf16_lo(r0.z); g[5] = bf16_hi(r0.z); g[6] = bf16_lo(r0.w); g[7] = bf16_hi(r0.w);
+#pragma unroll
+      for (int r = 1; r < N; ++r) {
+        const uint4 x = *reinterpret_cast<const uint4*>(st + r * L::kGradBytes + t8 * 2);
+        g[0] = __fadd_rn(g[0], bf16_lo(x.x)); g[1] = __fadd_rn(g[1], bf16_hi(x.x));
+        g[2] = __fadd_rn(g[2], bf16_lo(x.y)); g[3] = __fadd_rn(g[3], bf16_hi(x.y));
+        g[4] = __fadd_rn(g[4], bf16_lo(x.z)); g[5] = __fadd_rn(g[5], bf16_hi(x.z));
+        g[6] = __fadd_rn(g[6], bf16_lo(x.w)); g[7] = __fadd_rn(g[7], bf16_hi(x.w));
+      }
+    } else {
+      const float* g0 = reinterpret_cast<const float*>(st) + t8;
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) g[e] = g0[e];
+#pragma unroll
+      for (int r = 1; r < N; ++r) {
+        const float* gr = reinterpret_cast<const float*>(st + r * L::kGradBytes) + t8;
+        const float4 x0 = *reinterpret_cast<const float4*>(gr), x1 = *reinterpret_cast<const float4*>(gr + 4);
+        g[0] = __fadd_rn(g[0], x0.x); g[1] = __fadd_rn(g[1], x0.y); g[2] = __fadd_rn(g[2], x0.z);
+        g[3] = __fadd_rn(g[3], x0.w); g[4] = __fadd_rn(g[4], x1.x); g[5] = __fadd_rn(g[5], x1.y);
+        g[6] = __fadd_rn(g[6], x1.z); g[7] = __fadd_rn(g[7], x1.w);
+      }
+    }
+    const float* sw = reinterpret_cast<const float*>(st + N * L::kGradBytes) + t8;
+    const float* sm = reinterpret_cast<const float*>(st + N * L::kGradBytes + L::kStateBytes) + t8;
+    const float* sv = reinterpret_cast<const float*>(st + N * L::kGradBytes + 2 * L::kStateBytes) + t8;
+    float w[kVec], m[kVec], v[kVec];
+#pragma unroll
+    for (int e = 0; e < kVec; e += 4) {
+      *reinterpret_cast<float4*>(w + e) = *reinterpret_cast<const float4*>(sw + e);
+      *reinterpret_cast<float4*>(m + e) = *reinterpret_cast<const float4*>(sm + e);
+      *reinterpret_cast<float4*>(v + e) = *reinterpret_cast<const float4*>(sv + e);
+    }
+    __syncthreads();  // every thread holds its operands: the stage can be refilled
+    if (threadIdx.x == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      const long long next = id + static_cast<long long>(kTmaStages) * gridDim.x;
+      if (next < n_tiles) issue(next, stage);
+    }
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) adam(a, __fmul_rn(__fmul_rn(g[e], a.inv_n), clip), w[e], m[e], v[e]);
+    int si;
+    long long ti;
+    locate_tile(a, id, &si, &ti);
+    const long long j = a.seg[si].base + ti * kTmaTile + t8;
+    st_stream_f4(a.master + j, make_float4(w[0], w[1], w[2], w[3]));
+    st_stream_f4(a.master + j + 4, make_float4(w[4], w[5], w[6], w[7]));
+    st_stream_f4(a.m + j, make_float4(m[0], m[1], m[2], m[3]));
+    st_stream_f4(a.m + j + 4, make_float4(m[4], m[5], m[6], m[7]));
+    st_stream_f4(a.v + j, make_float4(v[0], v[1], v[2], v[3]));
+    st_stream_f4(a.v + j + 4, make_float4(v[4], v[5], v[6], v[7]));
+    uint4 out;
+    out.x = pack_bf16x2(w[0], w[1]);
+    out.y = pack_bf16x2(w[2], w[3]);
+    out.z = pack_bf16x2(w[4], w[5]);
+    out.w = pack_bf16x2(w[6], w[7]);
+    st_stream(a.p16 + j, out);
+  }
+  if (gave_up) {
+    // Bounded drain of copies that may still land in this CTA's shared memory.
+    for (int s = 0; s < kTmaStages; ++s) {
+      long long tries = 0;
+      while (!mbar_try_wait(&bars[s], 0) && !mbar_try_wait(&bars[s], 1) && ++tries < (1LL << 20)) {
+      }
+    }
+    return;
+  }
+  // The part of each segment after its last full tile (fewer than kTmaTile
+  // elements), element by element.
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (int s = 0; s < a.nseg; ++s) {
+    const Seg& sg = a.seg[s];
+    for (long long k = (sg.len / kTmaTile) * kTmaTile + tid; k < sg.len; k += stride) {
+      step_scalar_element(a, sg, k, clip);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Scalar kernel: one element per thread-iteration, any alignment, any N.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kStepThreads) step_scalar_kernel(const __grid_constant__ StepArgs a) {
@@ -202,7 +407,12 @@ struct DeviceInfo {
   int sms = 0;
   int vec_blocks_per_sm[2][kMaxRanks + 1] = {};
   int scalar_blocks_per_sm = 0;
+  int tma_smem_set[2][kMaxRanks + 1] = {};
 };
+
+// Shared memory of one SM usable by CTAs, and what each CTA reserves.
+constexpr long long kMaxSmemPerSm = 228 * 1024;
+constexpr long long kSmemReservedPerCta = 1024;
 
 std::mutex g_info_mutex;
 DeviceInfo g_info[kMaxDevices];
@@ -245,7 +455,61 @@ long long grid_for(long long work_items, int sms, int blocks_per_sm) {
 
 int sm_count() { return cached_sms(current_device()); }
 
+unsigned int step_timeouts() {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_step_timeouts, sizeof v) != cudaSuccess) return 0xFFFFFFFFu;
+  return v;
+}
+
+template <int N, bool kFp32>
+cudaError_t launch_tma(const StepArgs& a, cudaStream_t stream) {
+  constexpr uint32_t kSmem = TmaTile<N, kFp32>::kSmemBytes;
+  static_assert(kSmem + 128 <= 227 * 1024, "staged tiles must fit one CTA's shared memory (227 KB)");
+  const int dev = current_device();
+  {
+    std::lock_guard<std::mutex> lock(g_info_mutex);
+    int& done = g_info[dev].tma_smem_set[kFp32 ? 1 : 0][N];
+    if (!done) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(step_tma_kernel<N, kFp32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      if (e != cudaSuccess) return e;
+      done = 1;
+    }
+  }
+  int per_sm = static_cast<int>(kMaxSmemPerSm / (kSmem + kSmemReservedPerCta));
+  if (per_sm < 1) per_sm = 1;
+  if (per_sm > kStepCtasPerSm) per_sm = kStepCtasPerSm;
+  step_tma_kernel<N, kFp32><<<static_cast<unsigned>(cached_sms(dev) * per_sm), kStepThreads, kSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// The staged kernel where it measured faster and its tiles fit in shared memory.
+cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launched) {
+  *launched = true;
+  if (!a.grad_fp32) {
+    switch (a.n_ranks) {
+      case 14: return launch_tma<14, false>(a, stream);
+      case 15: return launch_tma<15, false>(a, stream);
+      case 16: return launch_tma<16, false>(a, stream);
+      default: break;
+    }
+  } else {
+    switch (a.n_ranks) {
+      case 8: return launch_tma<8, true>(a, stream);
+      case 9: return launch_tma<9, true>(a, stream);
+      default: break;
+    }
+  }
+  *launched = false;
+  return cudaSuccess;
+}
+
 cudaError_t launch_step_vec(const StepArgs& a, cudaStream_t stream) {
+  if (a.n_ranks >= (a.grad_fp32 ? kTmaMinRanksFp32 : kTmaMinRanks)) {
+    bool launched = false;
+    const cudaError_t e = try_launch_tma(a, stream, &launched);
+    if (launched) return e;
+  }
   StepKernel k = a.grad_fp32 ? vec_kernel_for<true>(a.n_ranks) : vec_kernel_for<false>(a.n_ranks);
   if (!k) return cudaErrorInvalidValue;
   const int dev = current_device();
