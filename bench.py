@@ -75,13 +75,14 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def step_kernel_name(n: int, grad_dtype: str, clip_keep: bool) -> str:
+def step_kernel_name(n: int, grad_dtype: str, clip_keep: bool, elems: int) -> str:
     """The step kernel the library launches for this workload: the tile-staged
-    one for N >= 14 bf16 or N = 8, 9 fp32 replicas, the register-staged one
-    otherwise (a kept fp32 reduced gradient is one fp32 replica)."""
+    one for N >= 14 bf16 or N = 8, 9 fp32 replicas over >= 2^23 elements, the
+    register-staged one otherwise (a kept fp32 reduced gradient is one fp32
+    replica)."""
     if clip_keep:
         n, grad_dtype = 1, "fp32"
-    staged = n >= 14 if grad_dtype == "bf16" else n in (8, 9)
+    staged = elems >= 2 ** 23 and (n >= 14 if grad_dtype == "bf16" else n in (8, 9))
     return "step_tma_kernel" if staged else "step_vec_kernel"
 
 
@@ -482,7 +483,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                          "frac": achieved_gbs / peak, "peak_source": f"hbm_gbs {peak_kind}",
                          "traffic": traffic, "algorithmic_bytes_per_launch": bytes_per_launch,
-                         "bytes_per_param": bpp, "kernel": step_kernel_name(n, wl["grad_dtype"], args.clip_keep),
+                         "bytes_per_param": bpp, "kernel": step_kernel_name(n, wl["grad_dtype"], args.clip_keep, padded),
                          "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms)},
             "clip": None if clip_ms is None else {
                 "max_norm": args.clip, "norm_pass_ms_mean": statistics.mean(clip_ms),
@@ -566,6 +567,7 @@ def run_sweep(args):
             mf, mw = statistics.median(flushed), statistics.median(warm)
             print(json.dumps({
                 "sweep_point": f"flat:{numel}:{n}", "params": numel, "n_ranks_simulated": n,
+                "kernel": step_kernel_name(n, "bf16", False, fs.padded),
                 "algorithmic_bytes": nbytes, "bytes_per_param": bytes_per_param(n, "bf16"), "reps": reps,
                 "kernel_ms_l2_flushed": mf, "gbs_l2_flushed": nbytes / mf / 1e6,
                 "frac_l2_flushed": nbytes / mf / 1e6 / peak, "params_per_s_l2_flushed": numel / mf * 1e3,

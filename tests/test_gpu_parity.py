@@ -150,21 +150,32 @@ def test_set_lr_between_steps():
     fs.close()
 
 
-@pytest.mark.parametrize("n,gd", [(13, "bf16"), (14, "bf16"), (15, "bf16"), (16, "bf16"), (7, "fp32"), (8, "fp32"),
-                                  (9, "fp32"), (10, "fp32")])
+@pytest.mark.parametrize("n,gd", [(13, "bf16"), (14, "bf16"), (16, "bf16"), (7, "fp32"), (8, "fp32"), (9, "fp32"),
+                                  (10, "fp32")])
 def test_tile_staged_kernel(n, gd):
-    # N >= 14 bf16 / N = 8, 9 fp32 replicas take the tile-staged (bulk copy)
-    # kernel, the neighbours of those thresholds the register-staged one:
-    # several segments, each with full 2,048-element tiles and a ragged part
-    # after them, plus units too small for one tile
+    # N >= 14 bf16 / N = 8, 9 fp32 replicas over >= 2^23 elements per launch
+    # take the tile-staged (bulk copy) kernel, the neighbours of those rank
+    # thresholds the register-staged one: 8.7 M elements in several segments,
+    # each with full 2,048-element tiles and a ragged part after them, plus
+    # units too small for one tile
     from zero_sharded_mixed_flatparameter_gb300 import binding as B
-    pl = si.from_units([2048 * 3 + 5, 1552, 2048 * 5, 7, 2048 * 2])
-    pb = make_problem(pl, n, 3, grad_dtype=gd, steps=3, seed=14 + n)
+    pl = si.from_units([4_200_005, 1552, 2_500_000, 7, 2_000_000])
+    pb = make_problem(pl, n, 3, grad_dtype=gd, steps=2, seed=14 + n)
     _per_step(pb, mode="separate")
-    _per_step(pb, mode="all")
     pb = make_problem(pl, n, 2, grad_dtype=gd, steps=2, seed=15 + n, max_norm=0.1)
     ref = oracle_run(pb)
-    fs = run_gpu(pb)
+    fs = run_gpu(pb, mode="all")
     compare_state(fs, ref, "tile-staged, clipped")
     fs.close()
     assert B.zero_kernel_timeouts() == 0
+
+
+def test_tile_staged_threshold_neighbours():
+    # padded to 2^23 - 16 elements the register-staged kernel runs, to
+    # 2^23 + 16 the tile-staged one; both agree with the oracle
+    for total in (2 ** 23 - 21, 2 ** 23 + 5):
+        pb = make_problem(si.from_units([total]), 16, 2, steps=1, seed=77)
+        ref = oracle_run(pb)
+        fs = run_gpu(pb, mode="all")
+        compare_state(fs, ref, f"{total} elements")
+        fs.close()

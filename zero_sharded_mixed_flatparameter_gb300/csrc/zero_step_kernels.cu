@@ -162,7 +162,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
 // 100 M-element buffer (GB/s, staged against register-staged): bf16 N = 14
 // 6988 / 6645, N = 15 7097 / 6632, N = 16 7146 / 6618; fp32 N = 8 7164 /
 // 6651, N = 9 7190 / 6634.  At bf16 N <= 13, fp32 N = 7 and fp32 N >= 10 the
-// register-staged kernel is as fast or faster, so it stays the default there.
+// register-staged kernel is as fast or faster, so it stays the default there;
+// so it does for launches of fewer than kTmaMinElems elements, where one CTA
+// per SM works through too few tiles to hide the latency of each (N = 16
+// bf16: 2363 / 3152 GB/s at 1 M elements, 5481 / 5479 at 6 M, 6179 / 5962
+// at 12 M).
 // The arithmetic and its order are those of step_vec8, so the results are
 // bit-identical.  Every wait is bounded: a CTA that gives up (which needs a
 // copy that never lands) counts it in g_step_timeouts and
@@ -505,7 +509,7 @@ cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launche
 }
 
 cudaError_t launch_step_vec(const StepArgs& a, cudaStream_t stream) {
-  if (a.n_ranks >= (a.grad_fp32 ? kTmaMinRanksFp32 : kTmaMinRanks)) {
+  if (a.total_elems >= kTmaMinElems && a.n_ranks >= (a.grad_fp32 ? kTmaMinRanksFp32 : kTmaMinRanks)) {
     bool launched = false;
     const cudaError_t e = try_launch_tma(a, stream, &launched);
     if (launched) return e;
