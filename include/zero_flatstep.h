@@ -325,8 +325,9 @@ zero_status zero_post_step(zero_ctx* ctx, void* stream);
  * into *t.  Any context planned over the same parameter list, with any N,
  * stage or unit grouping of the same order, can import it (resharding; the
  * source guide's resharding checkpoints, Femtotron #5's dp_size change).
- * Enqueued on `stream`.  Errors: ZERO_EINVAL (null/misaligned/host pointer);
- * ZERO_ESTATE (no buffers); ZERO_ECUDA.
+ * Enqueued on `stream` (in an offload context: copies up from the host state,
+ * which must not change until they complete).  Errors: ZERO_EINVAL
+ * (null/misaligned/host pointer); ZERO_ESTATE (no buffers); ZERO_ECUDA.
  */
 zero_status zero_export_state(zero_ctx* ctx, float* master_out, float* exp_avg_out, float* exp_avg_sq_out,
                               int64_t* t, void* stream);
@@ -337,15 +338,93 @@ zero_status zero_export_state(zero_ctx* ctx, float* master_out, float* exp_avg_o
  * into this context's padded layout with zero pads, param16 = bf16(master)
  * (round to nearest even), and the step count set to t.  Not allowed while
  * a step awaits its post_step.  Enqueued on `stream`; the inputs may be
- * released once it completes.  Errors: ZERO_EINVAL (null/misaligned/host
- * pointer, t < 0); ZERO_ESTATE; ZERO_ECUDA.
+ * released once it completes (in an offload context the host state is
+ * written and the call synchronizes `stream`).  Errors: ZERO_EINVAL
+ * (null/misaligned/host pointer, t < 0); ZERO_ESTATE; ZERO_ECUDA.
  */
 zero_status zero_import_state(zero_ctx* ctx, const float* master_in, const float* exp_avg_in,
                               const float* exp_avg_sq_in, int64_t t, void* stream);
 
+/* ---- ZeRO-Offload -------------------------------------------------------
+ * CMU 15-779 Lecture 13 notes §7.1-7.2 (ZeRO-Offload's partition and its
+ * timeline): only the 16-bit parameters stay on the GPU; the fp32 master,
+ * m and v live in host memory and a multi-threaded CPU Adam updates them
+ * chunk by chunk while the GPU produces the next chunk's gradient, the new
+ * bf16 parameters going back up chunk by chunk.  Here the gradient that goes
+ * down is the reduced fp32 one (sum of the N replicas in rank order x 1/N,
+ * times a pending clip coefficient): the host update is the device step's
+ * arithmetic, bit for bit, so an offloaded run equals a GPU-resident one.
+ */
+
+/*
+ * zero_make_master_offload — zero_make_master for an offload context:
+ * bufs->master, exp_avg, exp_avg_sq are HOST memory (pageable or pinned,
+ * padded_numel floats each, 16-byte aligned, caller-owned), bufs->param16 is
+ * device memory as before; init_params are device fp32 buffers.  The host
+ * master gets the init params at their offsets (pads, m, v zero), param16 =
+ * bf16(init) on the device.  Synchronizes `stream`.  The context then steps
+ * with zero_offload_step only (zero_step returns ZERO_ESTATE); registration,
+ * clipping (without ZERO_CLIP_KEEP_REDUCED: ZERO_ENOTSUP), accumulation,
+ * gather, export/import and post_step work as for any context.
+ * Errors: as zero_make_master, plus ZERO_EINVAL for a device state buffer.
+ */
+zero_status zero_make_master_offload(const zero_config* cfg, const int64_t* param_numel,
+                                     const int32_t* param_unit, int32_t n_params,
+                                     const float* const* init_params, const zero_buffers* bufs,
+                                     void* stream, zero_ctx** out);
+
+/*
+ * zero_offload_workspace_bytes — sizes of the two workspaces of
+ * zero_offload_step for chunks of `chunk` elements: *host_bytes of pinned
+ * host memory (3 chunk slots of fp32 gradient + bf16 parameters) and
+ * *device_bytes of device memory (3 slots of fp32 gradient).
+ * Errors: ZERO_EINVAL (NULL, chunk < 1).
+ */
+zero_status zero_offload_workspace_bytes(const zero_ctx* ctx, int64_t chunk, int64_t* host_bytes,
+                                         int64_t* device_bytes);
+
+/*
+ * zero_offload_step — one optimizer step of an offload context, t += 1.  The
+ * padded buffer is processed in chunks of `chunk` elements through a ring of
+ * 3 workspace slots: on `stream` a kernel writes chunk c's reduced (clipped)
+ * fp32 gradient into a device slot and it is copied to a pinned host slot;
+ * the host waits for it, runs Adam / AdamW over the chunk's host master, m, v
+ * on n_threads threads (0: one per hardware thread; the calling thread is one
+ * of them), writing bf16 parameters into a host slot that is copied into
+ * param16 on `copy_stream` (NULL: `stream`) — so the GPU reduction and the
+ * copies of other chunks overlap each chunk's host update.  param16 is
+ * rewritten only after the work enqueued on `stream` before the call, and
+ * work enqueued on `stream` after it sees the new param16.  Blocks the
+ * calling thread until every chunk's host update is done.  Workspaces: see
+ * zero_offload_workspace_bytes; host_workspace must be page-locked,
+ * device_workspace memory of the context's device, both 16-byte aligned.
+ * Not thread-safe on one context.  Errors: ZERO_EINVAL (chunk, threads,
+ * workspaces); ZERO_ESTATE (not an offload context, unregistered unit,
+ * step pending post_step); ZERO_ENOMEM (threads cannot start); ZERO_ECUDA
+ * (the chunks done before the failure stay updated on the host).
+ */
+zero_status zero_offload_step(zero_ctx* ctx, int64_t chunk, void* host_workspace, int64_t host_bytes,
+                              void* device_workspace, int64_t device_bytes, int32_t n_threads,
+                              void* stream, void* copy_stream);
+
+/*
+ * zero_cpu_adam — the CPU Adam of the offload step on its own, over host
+ * arrays of n elements: given the reduced fp32 gradient `grad`, updates
+ * master, exp_avg, exp_avg_sq in place with step t (>= 1) of cfg's
+ * optimizer and writes param16 = bf16(master) (bit patterns, round to
+ * nearest even).  Same arithmetic as the device step.  n_threads as above;
+ * threads are started and joined inside the call.  No CUDA call is made.
+ * Errors: ZERO_EINVAL (config, t < 1, n < 0, NULL or misaligned pointer);
+ * ZERO_ENOMEM.
+ */
+zero_status zero_cpu_adam(const zero_config* cfg, int64_t t, const float* grad, float* master,
+                          float* exp_avg, float* exp_avg_sq, uint16_t* param16, int64_t n,
+                          int32_t n_threads);
+
 /*
  * zero_kernel_timeouts — how many bounded waits of the tile-staged step
- * kernel (used for N >= 14 bf16 or N = 8, 9 fp32 replicas) gave up on the
+ * kernel (used for N >= 14 bf16 or N = 8, 9 fp32 replicas when a launch covers at
+ * least 2^23 elements) gave up on the
  * current device since the library was loaded.  A wait gives up only if a
  * bulk copy never lands; the CTA then leaves the rest of its tiles unchanged,
  * so a non-zero count means some step is incomplete.  Reads a device counter:

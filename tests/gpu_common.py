@@ -167,12 +167,17 @@ def oracle_run(pb: Problem, steps: Optional[int] = None, every_step=None, norms:
     return master, m, v, p16
 
 
-def gpu_flatstep(pb: Problem, guard: int = 64, device="cuda") -> FlatStep:
+def gpu_flatstep(pb: Problem, guard: int = 64, device="cuda", offload: Optional[dict] = None) -> FlatStep:
+    """offload: None, or dict(chunk=..., threads=...) for a ZeRO-Offload context."""
     init = [torch.from_numpy(a).to(device) for a in pb.init]
     h = pb.hyper
+    extra = {}
+    if offload is not None:
+        extra = dict(offload=True, offload_chunk=offload.get("chunk", 1 << 22),
+                     offload_threads=offload.get("threads", 0))
     return FlatStep(pb.pl.numel, pb.pl.unit, stage=pb.stage, n_ranks=pb.n, grad_dtype=pb.grad_dtype,
                     lr=h.lr, beta1=h.beta1, beta2=h.beta2, eps=h.eps, weight_decay=h.weight_decay,
-                    adamw=h.adamw, init_params=init, device=device, guard=guard)
+                    adamw=h.adamw, init_params=init, device=device, guard=guard, **extra)
 
 
 def upload_grads(pb: Problem, t: int, device="cuda") -> List[torch.Tensor]:
@@ -207,8 +212,9 @@ def check_guards(fs: FlatStep, what: str):
 
 
 def run_gpu(pb: Problem, mode: str = "units", every_step=None, guard: int = 64,
-            gather_check: bool = True, norms: Optional[list] = None, clip_keep: bool = False) -> FlatStep:
-    fs = gpu_flatstep(pb, guard=guard)
+            gather_check: bool = True, norms: Optional[list] = None, clip_keep: bool = False,
+            offload: Optional[dict] = None) -> FlatStep:
+    fs = gpu_flatstep(pb, guard=guard, offload=offload)
     try:
         for t in range(1, len(pb.grads) + 1):
             flats = upload_grads(pb, t)

@@ -29,6 +29,7 @@ EXPORTED = (
     "zero_destroy", "zero_last_error", "zero_status_string", "zero_clip_workspace_bytes", "zero_clip_grad_norm",
     "zero_grad_norm", "zero_clip_grad_norm_static", "zero_accumulate_grads", "zero_export_state",
     "zero_import_state", "zero_clip_workspace_bytes_ex", "zero_clip_grad_norm_ex", "zero_kernel_timeouts",
+    "zero_make_master_offload", "zero_offload_workspace_bytes", "zero_offload_step", "zero_cpu_adam",
 )
 ZERO_CLIP_KEEP_REDUCED = 1
 
@@ -94,6 +95,10 @@ def load(path: str = LIB_PATH):
             "zero_clip_workspace_bytes_ex": [vp, i32, P(i64)],
             "zero_clip_grad_norm_ex": [vp, f32, i32, vp, i64, vp],
             "zero_kernel_timeouts": [vp, P(ctypes.c_uint32)],
+            "zero_make_master_offload": [P(zero_config), vp, vp, i32, vp, P(zero_buffers), vp, P(vp)],
+            "zero_offload_workspace_bytes": [vp, i64, P(i64), P(i64)],
+            "zero_offload_step": [vp, i64, vp, i64, vp, i64, i32, vp, vp],
+            "zero_cpu_adam": [P(zero_config), i64, vp, vp, vp, vp, vp, i64, i32],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -152,6 +157,37 @@ def zero_make_master(cfg: zero_config, param_numel: Sequence[int], param_unit: S
     _check(lib.zero_make_master(ctypes.byref(cfg), _i64(param_numel), _i32(param_unit), len(param_numel),
                                 _ptrs(init_params), ctypes.byref(bufs), stream or None, ctypes.byref(out)))
     return out.value
+
+
+def zero_make_master_offload(cfg: zero_config, param_numel: Sequence[int], param_unit: Sequence[int],
+                             init_params: Sequence[int], master: int, exp_avg: int, exp_avg_sq: int,
+                             param16: int, stream: int = 0) -> int:
+    """master / exp_avg / exp_avg_sq are host addresses, param16 a device one."""
+    lib = load()
+    out = ctypes.c_void_p()
+    bufs = zero_buffers(master, exp_avg, exp_avg_sq, param16)
+    _check(lib.zero_make_master_offload(ctypes.byref(cfg), _i64(param_numel), _i32(param_unit), len(param_numel),
+                                        _ptrs(init_params), ctypes.byref(bufs), stream or None, ctypes.byref(out)))
+    return out.value
+
+
+def zero_offload_workspace_bytes(ctx: int, chunk: int):
+    """(host bytes, device bytes) of zero_offload_step's workspaces."""
+    h, d = ctypes.c_int64(), ctypes.c_int64()
+    _check(load().zero_offload_workspace_bytes(ctx, chunk, ctypes.byref(h), ctypes.byref(d)), ctx)
+    return h.value, d.value
+
+
+def zero_offload_step(ctx: int, chunk: int, host_ws: int, host_bytes: int, dev_ws: int, dev_bytes: int,
+                      n_threads: int = 0, stream: int = 0, copy_stream: int = 0) -> None:
+    _check(load().zero_offload_step(ctx, chunk, host_ws, host_bytes, dev_ws, dev_bytes, n_threads, stream or None,
+                                    copy_stream or None), ctx)
+
+
+def zero_cpu_adam(cfg: zero_config, t: int, grad: int, master: int, exp_avg: int, exp_avg_sq: int, param16: int,
+                  n: int, n_threads: int = 0) -> None:
+    """Host Adam over host arrays (addresses of fp32 grad/master/m/v and uint16 param16)."""
+    _check(load().zero_cpu_adam(ctypes.byref(cfg), t, grad, master, exp_avg, exp_avg_sq, param16, n, n_threads))
 
 
 def zero_num_units(ctx: int) -> int:

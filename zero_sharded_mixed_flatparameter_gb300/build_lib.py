@@ -1,9 +1,11 @@
 """Build of the CUDA library (``libzero_flatstep.so``) for sm_103a.
 
-Two translation units compiled in parallel with nvcc, then linked into a
-shared library next to this file's package (in-tree, git-ignored).  No
-fast-math and no FMA contraction: the step's arithmetic is reproducible bit
-for bit.
+The CUDA and runtime translation units are compiled in parallel with nvcc,
+the host CPU-Adam unit with the host C++ compiler (portable flags only, so it
+builds the same on x86-64 and aarch64), then all are linked into a shared
+library next to this file's package (in-tree, git-ignored).  No fast-math
+and no FMA contraction anywhere: the step's arithmetic is reproducible bit
+for bit, on the device and on the host.
 """
 
 from __future__ import annotations
@@ -25,6 +27,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "--fmad=false", "-Xcompiler", "-fPIC,-O2",
           "-I" + INCLUDE, "-I" + CSRC]
 SOURCES = ["zero_step_kernels.cu", "zero_aux_kernels.cu", "zero_runtime.cpp", "zero_no_alloc.cu"]
+HOST_SOURCES = ["zero_host_adam.cpp"]
+HOST_FLAGS = ["-std=c++17", "-O3", "-ffp-contract=off", "-fno-math-errno", "-fPIC", "-pthread", "-I" + CSRC]
 
 
 def _nvcc() -> str:
@@ -34,10 +38,17 @@ def _nvcc() -> str:
     return nvcc
 
 
+def _cxx() -> str:
+    cxx = os.environ.get("CXX") or shutil.which("g++") or shutil.which("c++")
+    if not cxx:
+        raise RuntimeError("no host C++ compiler (g++) found")
+    return cxx
+
+
 def _inputs():
-    files = [os.path.join(CSRC, s) for s in SOURCES]
+    files = [os.path.join(CSRC, s) for s in SOURCES + HOST_SOURCES]
     files += [os.path.join(CSRC, "zero_internal.h"), os.path.join(CSRC, "zero_device.cuh"),
-              os.path.join(CSRC, "zero_aux_internal.h"),
+              os.path.join(CSRC, "zero_aux_internal.h"), os.path.join(CSRC, "zero_host.h"),
               os.path.join(INCLUDE, "zero_flatstep.h")]
     return files
 
@@ -55,22 +66,27 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
 
+    cxx = _cxx()
+
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc, *ARCH, *COMMON, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
+        if src in HOST_SOURCES:
+            cmd = [cxx, *HOST_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        else:
+            cmd = [nvcc, *ARCH, *COMMON, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"compiling {src} failed:\n{r.stdout}\n{r.stderr}")
         if verbose and (r.stdout or r.stderr):
             print(r.stdout + r.stderr, flush=True)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES) + len(HOST_SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES + HOST_SOURCES))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
+    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -51,6 +51,8 @@ cudaError_t launch_clip_finalize(void* workspace, long long n_partials, float ma
 // make_master pieces.
 cudaError_t launch_zero_fill(float* master, float* m, float* v, uint16_t* p16, long long n,
                              cudaStream_t stream);
+// master[offset + k] = src[k] (skipped when master is nullptr) and
+// p16[offset + k] = bf16(src[k]), k < n.
 cudaError_t launch_copy_param(const float* src, float* master, uint16_t* p16, long long offset,
                               long long n, cudaStream_t stream);
 // Plain fp32 copy of n elements (checkpoint export/import).
@@ -66,6 +68,30 @@ struct AccumArgs {
   float* acc[kMaxRanks];
 };
 cudaError_t launch_accumulate(const AccumArgs& a, bool vec, cudaStream_t stream);
+
+// ZeRO-Offload: the reduced gradient of one chunk of the flat buffer,
+// out[out_off + k] = ((G_0 + G_1) + ... + G_{N-1})[k] * fp32(1/N) * clip for
+// k < len of every segment (clip = 1 without a pending clip), for the host
+// Adam to read.  Segments are walked as one index space of 8-element groups.
+struct ReduceSeg {
+  long long out_off;      // element offset of this segment in out
+  long long len;          // elements
+  long long group_start;  // first 8-element group of this segment in the launch
+  int vec_ok;             // gradients and out + out_off 16-byte aligned
+  const void* g[kMaxRanks];
+};
+
+struct ReduceArgs {
+  float* out;
+  const float* clip;  // device clip coefficient, or nullptr
+  float inv_n;
+  int n_ranks;
+  int grad_fp32;
+  int nseg;
+  long long total_groups;
+  ReduceSeg seg[kMaxSegs];
+};
+cudaError_t launch_reduce_out(const ReduceArgs& a, cudaStream_t stream);
 
 // ZeRO-3 unit gather: copy n bf16 elements; *launches counts the kernels enqueued.
 cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaStream_t stream, int* launches);

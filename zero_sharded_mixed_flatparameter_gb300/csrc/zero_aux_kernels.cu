@@ -336,7 +336,7 @@ __global__ void copy_param_kernel(const float* __restrict__ src, float* __restri
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long k = tid; k < n; k += stride) {
     const float x = src[k];
-    master[offset + k] = x;
+    if (master) master[offset + k] = x;  // no device master in an offload context
     p16[offset + k] = to_bf16_bits(x);
   }
 }
@@ -360,7 +360,69 @@ __global__ void gather_scalar_kernel(const uint16_t* __restrict__ src, uint16_t*
   for (long long k = begin + tid; k < n; k += stride) dst[k] = src[k];
 }
 
+// ---------------------------------------------------------------------------
+// ZeRO-Offload: reduced gradient of one chunk, written for the host.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float reduce_one(const ReduceArgs& a, const ReduceSeg& s, long long k) {
+  float acc;
+  if (a.grad_fp32) {
+    acc = __ldcs(static_cast<const float*>(s.g[0]) + k);
+    for (int r = 1; r < a.n_ranks; ++r) acc = __fadd_rn(acc, __ldcs(static_cast<const float*>(s.g[r]) + k));
+  } else {
+    acc = __uint_as_float(static_cast<uint32_t>(__ldcs(static_cast<const unsigned short*>(s.g[0]) + k)) << 16);
+    for (int r = 1; r < a.n_ranks; ++r) {
+      acc = __fadd_rn(acc, __uint_as_float(static_cast<uint32_t>(__ldcs(static_cast<const unsigned short*>(s.g[r]) + k)) << 16));
+    }
+  }
+  return acc;
+}
+
+__global__ void __launch_bounds__(kStepThreads) reduce_out_kernel(const __grid_constant__ ReduceArgs a) {
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const float clip = a.clip ? *a.clip : 1.0f;
+  int s = 0;
+  for (long long q = tid; q < a.total_groups; q += stride) {
+    while (s + 1 < a.nseg && q >= a.seg[s + 1].group_start) ++s;
+    const ReduceSeg& sg = a.seg[s];
+    const long long k = (q - sg.group_start) * kVec;
+    float* out = a.out + sg.out_off + k;
+    if (sg.vec_ok && k + kVec <= sg.len) {
+      float acc[kVec];
+      for (int r = 0; r < a.n_ranks; ++r) {
+        float x[kVec];
+        if (a.grad_fp32) {
+          const float* gp = static_cast<const float*>(sg.g[r]) + k;
+          const float4 lo = ld_stream_f4(gp), hi = ld_stream_f4(gp + 4);
+          x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+          x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
+        } else {
+          const uint4 h = ld_stream(static_cast<const uint16_t*>(sg.g[r]) + k);
+          x[0] = bf16_lo(h.x); x[1] = bf16_hi(h.x); x[2] = bf16_lo(h.y); x[3] = bf16_hi(h.y);
+          x[4] = bf16_lo(h.z); x[5] = bf16_hi(h.z); x[6] = bf16_lo(h.w); x[7] = bf16_hi(h.w);
+        }
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) acc[e] = r == 0 ? x[e] : __fadd_rn(acc[e], x[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) acc[e] = __fmul_rn(__fmul_rn(acc[e], a.inv_n), clip);
+      st_stream_f4(out, make_float4(acc[0], acc[1], acc[2], acc[3]));
+      st_stream_f4(out + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+    } else {
+      const long long end = k + kVec < sg.len ? k + kVec : sg.len;
+      for (long long e = k; e < end; ++e) out[e - k] = __fmul_rn(__fmul_rn(reduce_one(a, sg, e), a.inv_n), clip);
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_reduce_out(const ReduceArgs& a, cudaStream_t stream) {
+  if (a.total_groups <= 0 || a.nseg <= 0) return cudaSuccess;
+  const long long grid = grid_for(a.total_groups, sm_count(), 8);
+  reduce_out_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
 
 using NormKernel = void (*)(NormArgs);
 

@@ -10,6 +10,8 @@
 
 #include <algorithm>
 #include <cmath>
+#include <functional>
+#include <thread>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -22,6 +24,7 @@
 
 #include "zero_flatstep.h"
 #include "zero_aux_internal.h"
+#include "zero_host.h"
 #include "zero_internal.h"
 
 namespace {
@@ -59,7 +62,14 @@ struct zero_ctx {
   // elements) the pending step reads instead of the replicas.
   float* clip_keep = nullptr;
 
+  // ZeRO-Offload: master / m / v are host memory, the step runs through
+  // zero_offload_step with this worker pool (created on first use).
+  bool offload = false;
+  zfs_host::Pool* pool = nullptr;
+
   std::string error;
+
+  ~zero_ctx() { zfs_host::pool_destroy(pool); }
 };
 
 namespace {
@@ -189,19 +199,34 @@ zero_status require_bound(zero_ctx* ctx) {
 
 // Scalars of step t, each from its definition (evaluated in double where the
 // definition has a power or a product of hyper-parameters, rounded once).
+zfs_host::AdamScalars adam_scalars(const zero_config& c, int64_t t) {
+  zfs_host::AdamScalars s;
+  s.lr = c.lr;
+  s.beta1 = c.beta1;
+  s.beta2 = c.beta2;
+  s.omb1 = 1.0f - c.beta1;
+  s.omb2 = 1.0f - c.beta2;
+  s.eps = c.eps;
+  s.bc1 = static_cast<float>(1.0 - std::pow(static_cast<double>(c.beta1), static_cast<double>(t)));
+  s.bc2 = static_cast<float>(1.0 - std::pow(static_cast<double>(c.beta2), static_cast<double>(t)));
+  s.decay = c.adamw ? static_cast<float>(1.0 - static_cast<double>(c.lr) * static_cast<double>(c.weight_decay))
+                    : 1.0f;
+  return s;
+}
+
 void fill_scalars(const zero_ctx* ctx, int64_t t, zfs::StepArgs* a) {
   const zero_config& c = ctx->cfg;
+  const zfs_host::AdamScalars s = adam_scalars(c, t);
   a->inv_n = 1.0f / static_cast<float>(c.n_ranks);
-  a->lr = c.lr;
-  a->beta1 = c.beta1;
-  a->beta2 = c.beta2;
-  a->omb1 = 1.0f - c.beta1;
-  a->omb2 = 1.0f - c.beta2;
-  a->eps = c.eps;
-  a->bc1 = static_cast<float>(1.0 - std::pow(static_cast<double>(c.beta1), static_cast<double>(t)));
-  a->bc2 = static_cast<float>(1.0 - std::pow(static_cast<double>(c.beta2), static_cast<double>(t)));
-  a->decay = c.adamw ? static_cast<float>(1.0 - static_cast<double>(c.lr) * static_cast<double>(c.weight_decay))
-                     : 1.0f;
+  a->lr = s.lr;
+  a->beta1 = s.beta1;
+  a->beta2 = s.beta2;
+  a->omb1 = s.omb1;
+  a->omb2 = s.omb2;
+  a->eps = s.eps;
+  a->bc1 = s.bc1;
+  a->bc2 = s.bc2;
+  a->decay = s.decay;
   a->n_ranks = c.n_ranks;
   a->grad_fp32 = c.grad_dtype == ZERO_GRAD_FP32 ? 1 : 0;
 }
@@ -388,6 +413,67 @@ zero_status zero_make_master(const zero_config* cfg, const int64_t* param_numel,
   return ZERO_OK;
 }
 
+zero_status zero_make_master_offload(const zero_config* cfg, const int64_t* param_numel, const int32_t* param_unit,
+                                     int32_t n_params, const float* const* init_params, const zero_buffers* bufs,
+                                     void* stream, zero_ctx** out) {
+  if (!out) return fail(nullptr, ZERO_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!bufs) return fail(nullptr, ZERO_EINVAL, "bufs is NULL");
+  zero_ctx* ctx = nullptr;
+  zero_status st = zero_plan(cfg, param_numel, param_unit, n_params, &ctx);
+  if (st != ZERO_OK) return st;
+  auto bail = [&](zero_status s) {
+    g_thread_error = ctx->error;
+    delete ctx;
+    return s;
+  };
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return bail(fail(ctx, ZERO_ECUDA, "no CUDA device"));
+  float* host[3] = {bufs->master, bufs->exp_avg, bufs->exp_avg_sq};
+  const char* names[3] = {"master", "exp_avg", "exp_avg_sq"};
+  for (int k = 0; k < 3; ++k) {
+    if (!host[k]) return bail(fail(ctx, ZERO_EINVAL, "buffer %s is NULL", names[k]));
+    if (!aligned(host[k], 16)) return bail(fail(ctx, ZERO_EINVAL, "buffer %s is not 16-byte aligned", names[k]));
+    if (is_device_pointer(host[k], nullptr))
+      return bail(fail(ctx, ZERO_EINVAL, "buffer %s must be host memory in an offload context", names[k]));
+  }
+  int pdev = -1;
+  if (!bufs->param16) return bail(fail(ctx, ZERO_EINVAL, "buffer param16 is NULL"));
+  if (!aligned(bufs->param16, 16)) return bail(fail(ctx, ZERO_EINVAL, "buffer param16 is not 16-byte aligned"));
+  if (!is_device_pointer(bufs->param16, &pdev)) return bail(fail(ctx, ZERO_EINVAL, "buffer param16 is not CUDA device memory"));
+  if (pdev != dev) return bail(fail(ctx, ZERO_EINVAL, "buffer param16 is on device %d, current is %d", pdev, dev));
+  for (int32_t p = 0; p < n_params; ++p) {
+    if (param_numel[p] == 0) continue;
+    if (!init_params || !init_params[p]) return bail(fail(ctx, ZERO_EINVAL, "init param %d is NULL", p));
+    if (!aligned(init_params[p], 4)) return bail(fail(ctx, ZERO_EINVAL, "init param %d is not 4-byte aligned", p));
+    if (!is_device_pointer(init_params[p], nullptr))
+      return bail(fail(ctx, ZERO_EINVAL, "init param %d is not CUDA device memory", p));
+  }
+  ctx->bufs = *bufs;
+  ctx->device = dev;
+  ctx->offload = true;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint16_t* p16 = static_cast<uint16_t*>(bufs->param16);
+  // Host master = init params at their offsets, pads / m / v = 0; device
+  // param16 = bf16(init params), pads 0.
+  cudaError_t e = cudaStreamSynchronize(s);
+  for (int k = 0; k < 3 && e == cudaSuccess; ++k)
+    std::memset(host[k], 0, static_cast<size_t>(ctx->padded_total) * sizeof(float));
+  if (e == cudaSuccess && ctx->padded_total > 0) e = cudaMemsetAsync(p16, 0, static_cast<size_t>(ctx->padded_total) * 2, s);
+  for (int32_t p = 0; p < n_params && e == cudaSuccess; ++p) {
+    if (param_numel[p] == 0) continue;
+    e = cudaMemcpyAsync(host[0] + ctx->param_offset[p], init_params[p], param_numel[p] * sizeof(float),
+                        cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = zfs::launch_copy_param(init_params[p], nullptr, p16, ctx->param_offset[p], param_numel[p], s);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return bail(fail_cuda(ctx, "make_master_offload", e));
+  ctx->phase = Phase::kReady;
+  ctx->t = 0;
+  *out = ctx;
+  return ZERO_OK;
+}
+
 zero_status zero_num_units(const zero_ctx* ctx, int32_t* n_units) {
   if (!ctx || !n_units) return fail(nullptr, ZERO_EINVAL, "NULL argument");
   *n_units = ctx->n_units;
@@ -537,6 +623,7 @@ zero_status zero_step(zero_ctx* ctx, void* stream) {
   if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
   zero_status st = require_bound(ctx);
   if (st != ZERO_OK) return st;
+  if (ctx->offload) return fail(ctx, ZERO_ESTATE, "offload context: its step is zero_offload_step");
   if (ctx->phase == Phase::kStepped) return fail(ctx, ZERO_ESTATE, "step already taken: call post_step first");
   for (int32_t i = 0; i < ctx->n_units; ++i) {
     if (!ctx->registered[i]) return fail(ctx, ZERO_ESTATE, "unit %d has no registered gradients", i);
@@ -590,6 +677,230 @@ zero_status zero_step(zero_ctx* ctx, void* stream) {
   return ZERO_OK;
 }
 
+// ---------------------------------------------------------------------------
+// ZeRO-Offload step.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kOffloadRing = 3;  // chunks in flight between the GPU and the host
+
+int64_t offload_slot_elems(const zero_ctx* ctx, int64_t chunk) {
+  const int64_t c = std::min<int64_t>(chunk, std::max<int64_t>(ctx->padded_total, 1));
+  return (c + 63) / 64 * 64;
+}
+
+// One chunk of host Adam work; the pool's callback captures only a
+// reference to it (small enough for std::function to store without allocating).
+struct HostAdamJob {
+  zfs_host::AdamScalars sc;
+  const float* g;
+  float* w;
+  float* m;
+  float* v;
+  uint16_t* p16;
+  void operator()(int64_t lo, int64_t hi) const {
+    zfs_host::adam_range(sc, g + lo, w + lo, m + lo, v + lo, p16 + lo, hi - lo);
+  }
+};
+
+struct EventSet {
+  std::vector<cudaEvent_t> ev;
+  ~EventSet() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  }
+  cudaError_t make(int n) {
+    for (int i = 0; i < n; ++i) {
+      cudaEvent_t e = nullptr;
+      const cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+      if (r != cudaSuccess) return r;
+      ev.push_back(e);
+    }
+    return cudaSuccess;
+  }
+};
+
+// Launches of the reduced gradient of [c0, c1) into out (slot of the device
+// workspace): the registered segments intersected with the chunk.
+cudaError_t enqueue_chunk_reduce(const zero_ctx* ctx, const std::vector<PlannedSeg>& segs, int64_t c0, int64_t c1,
+                                 float* out, const float* clip, cudaStream_t s, int32_t* launches) {
+  const int N = ctx->cfg.n_ranks;
+  const size_t esz = grad_bytes(ctx->cfg);
+  zfs::ReduceArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.out = out;
+  a.clip = clip;
+  a.inv_n = 1.0f / static_cast<float>(N);
+  a.n_ranks = N;
+  a.grad_fp32 = ctx->cfg.grad_dtype == ZERO_GRAD_FP32 ? 1 : 0;
+  auto flush = [&]() -> cudaError_t {
+    if (a.nseg == 0) return cudaSuccess;
+    const cudaError_t e = zfs::launch_reduce_out(a, s);
+    if (e == cudaSuccess) ++*launches;
+    a.nseg = 0;
+    a.total_groups = 0;
+    return e;
+  };
+  for (const PlannedSeg& sg : segs) {
+    const int64_t lo = std::max(sg.base, c0), hi = std::min(sg.base + sg.len, c1);
+    if (lo >= hi) continue;
+    if (a.nseg == zfs::kMaxSegs) {
+      const cudaError_t e = flush();
+      if (e != cudaSuccess) return e;
+    }
+    zfs::ReduceSeg& r = a.seg[a.nseg++];
+    r.out_off = lo - c0;
+    r.len = hi - lo;
+    r.group_start = a.total_groups;
+    bool vec = r.out_off % 4 == 0;
+    for (int k = 0; k < N; ++k) {
+      r.g[k] = static_cast<const char*>(sg.g[k]) + (lo - sg.base) * esz;
+      vec = vec && aligned(r.g[k], 16);
+    }
+    r.vec_ok = vec ? 1 : 0;
+    a.total_groups += (r.len + zfs::kVec - 1) / zfs::kVec;
+  }
+  return flush();
+}
+
+}  // namespace
+
+zero_status zero_offload_workspace_bytes(const zero_ctx* ctx, int64_t chunk, int64_t* host_bytes,
+                                         int64_t* device_bytes) {
+  if (!ctx || !host_bytes || !device_bytes) return fail(nullptr, ZERO_EINVAL, "NULL argument");
+  if (chunk < 1) return fail(const_cast<zero_ctx*>(ctx), ZERO_EINVAL, "chunk must be >= 1 element");
+  const int64_t slot = offload_slot_elems(ctx, chunk);
+  *host_bytes = kOffloadRing * slot * (4 + 2);
+  *device_bytes = kOffloadRing * slot * 4;
+  return ZERO_OK;
+}
+
+zero_status zero_offload_step(zero_ctx* ctx, int64_t chunk, void* host_workspace, int64_t host_bytes,
+                              void* device_workspace, int64_t device_bytes, int32_t n_threads, void* stream,
+                              void* copy_stream) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  zero_status st = require_bound(ctx);
+  if (st != ZERO_OK) return st;
+  if (!ctx->offload) return fail(ctx, ZERO_ESTATE, "not an offload context (see zero_make_master_offload)");
+  if (ctx->phase == Phase::kStepped) return fail(ctx, ZERO_ESTATE, "step already taken: call post_step first");
+  int32_t missing = -1;
+  if (!all_registered(ctx, &missing)) return fail(ctx, ZERO_ESTATE, "unit %d has no registered gradients", missing);
+  if (chunk < 1) return fail(ctx, ZERO_EINVAL, "chunk must be >= 1 element");
+  if (n_threads < 0 || n_threads > 1024) return fail(ctx, ZERO_EINVAL, "n_threads %d not in 0..1024", n_threads);
+  const int64_t slot = offload_slot_elems(ctx, chunk);
+  if (host_bytes < kOffloadRing * slot * 6) return fail(ctx, ZERO_EINVAL, "host workspace too small");
+  if (device_bytes < kOffloadRing * slot * 4) return fail(ctx, ZERO_EINVAL, "device workspace too small");
+  if (!host_workspace || !aligned(host_workspace, 16)) return fail(ctx, ZERO_EINVAL, "host workspace NULL or not 16-byte aligned");
+  if (!device_workspace || !aligned(device_workspace, 16))
+    return fail(ctx, ZERO_EINVAL, "device workspace NULL or not 16-byte aligned");
+  {
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, host_workspace) != cudaSuccess || attr.type != cudaMemoryTypeHost) {
+      cudaGetLastError();
+      return fail(ctx, ZERO_EINVAL, "host workspace is not page-locked (pinned) host memory");
+    }
+    int wdev = -1;
+    if (!is_device_pointer(device_workspace, &wdev) || wdev != ctx->device)
+      return fail(ctx, ZERO_EINVAL, "device workspace is not memory of the context's device");
+  }
+  int threads = n_threads > 0 ? n_threads : static_cast<int>(std::thread::hardware_concurrency());
+  if (threads < 1) threads = 1;
+  if (!ctx->pool || zfs_host::pool_threads(ctx->pool) != threads) {
+    zfs_host::pool_destroy(ctx->pool);
+    ctx->pool = zfs_host::pool_create(threads);
+    if (!ctx->pool) return fail(ctx, ZERO_ENOMEM, "cannot start %d host threads", threads);
+  }
+  std::vector<PlannedSeg> segs;
+  try {
+    segs = build_segments(ctx);
+  } catch (const std::bad_alloc&) {
+    return fail(ctx, ZERO_ENOMEM, "cannot allocate segment list");
+  }
+  const int64_t t = ctx->t + 1;
+  const zfs_host::AdamScalars sc = adam_scalars(ctx->cfg, t);
+  const float* clip = ctx->clip_ws ? reinterpret_cast<const float*>(ctx->clip_ws + 8) : nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t cs = copy_stream ? static_cast<cudaStream_t>(copy_stream) : s;
+  float* dev_g = static_cast<float*>(device_workspace);
+  float* host_g = static_cast<float*>(host_workspace);
+  uint16_t* host_p = reinterpret_cast<uint16_t*>(host_g + kOffloadRing * slot);
+  uint16_t* p16 = static_cast<uint16_t*>(ctx->bufs.param16);
+  const int64_t P = ctx->padded_total;
+  const int64_t n_chunks = (P + chunk - 1) / chunk;
+
+  // Events: [0, R) gradients of a slot on the host, [R, 2R) a slot's
+  // parameters on the device, 2R: start of the step on `stream`, 2R+1: end.
+  EventSet evs;
+  cudaError_t e = evs.make(2 * kOffloadRing + 2);
+  if (e != cudaSuccess) return fail_cuda(ctx, "offload events", e);
+  cudaEvent_t* ev_g = evs.ev.data();
+  cudaEvent_t* ev_p = evs.ev.data() + kOffloadRing;
+  int32_t launches = 0;
+  // param16 is rewritten on the copy stream: only after the caller's earlier work on `stream`.
+  e = cudaEventRecord(evs.ev[2 * kOffloadRing], s);
+  if (e == cudaSuccess && cs != s) e = cudaStreamWaitEvent(cs, evs.ev[2 * kOffloadRing], 0);
+  auto enqueue = [&](int64_t c) -> cudaError_t {
+    const int k = static_cast<int>(c % kOffloadRing);
+    const int64_t c0 = c * chunk, c1 = std::min(P, c0 + chunk);
+    cudaError_t r = enqueue_chunk_reduce(ctx, segs, c0, c1, dev_g + k * slot, clip, s, &launches);
+    if (r == cudaSuccess)
+      r = cudaMemcpyAsync(host_g + k * slot, dev_g + k * slot, (c1 - c0) * sizeof(float), cudaMemcpyDeviceToHost, s);
+    if (r == cudaSuccess) r = cudaEventRecord(ev_g[k], s);
+    return r;
+  };
+  for (int64_t c = 0; c < std::min<int64_t>(kOffloadRing, n_chunks) && e == cudaSuccess; ++c) e = enqueue(c);
+  for (int64_t c = 0; c < n_chunks && e == cudaSuccess; ++c) {
+    const int k = static_cast<int>(c % kOffloadRing);
+    const int64_t c0 = c * chunk, c1 = std::min(P, c0 + chunk);
+    e = cudaEventSynchronize(ev_g[k]);                       // this chunk's gradients are on the host
+    if (e == cudaSuccess && c >= kOffloadRing) e = cudaEventSynchronize(ev_p[k]);  // slot's last upload done
+    if (e != cudaSuccess) break;
+    const HostAdamJob job{sc, host_g + k * slot, ctx->bufs.master + c0, ctx->bufs.exp_avg + c0,
+                          ctx->bufs.exp_avg_sq + c0, host_p + k * slot};
+    zfs_host::pool_run(ctx->pool, c1 - c0, [&job](int64_t lo, int64_t hi) { job(lo, hi); });
+    e = cudaMemcpyAsync(p16 + c0, job.p16, (c1 - c0) * 2, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_p[k], cs);
+    if (e == cudaSuccess && c + kOffloadRing < n_chunks) e = enqueue(c + kOffloadRing);
+  }
+  // Later work on `stream` sees the new param16.
+  if (e == cudaSuccess && cs != s) e = cudaEventRecord(evs.ev[2 * kOffloadRing + 1], cs);
+  if (e == cudaSuccess && cs != s) e = cudaStreamWaitEvent(s, evs.ev[2 * kOffloadRing + 1], 0);
+  if (e != cudaSuccess) {
+    // Chunks already updated on the host stay updated: the state is partial.
+    cudaStreamSynchronize(cs);
+    cudaStreamSynchronize(s);
+    return fail_cuda(ctx, "offload step (state partially updated)", e);
+  }
+  ctx->last_launches = launches;
+  ctx->t = t;
+  ctx->phase = Phase::kStepped;
+  return ZERO_OK;
+}
+
+zero_status zero_cpu_adam(const zero_config* cfg, int64_t t, const float* grad, float* master, float* exp_avg,
+                          float* exp_avg_sq, uint16_t* param16, int64_t n, int32_t n_threads) {
+  zero_status st = check_config(cfg, nullptr);
+  if (st != ZERO_OK) return st;
+  if (t < 1) return fail(nullptr, ZERO_EINVAL, "t must be >= 1");
+  if (n < 0) return fail(nullptr, ZERO_EINVAL, "n is negative");
+  if (n_threads < 0 || n_threads > 1024) return fail(nullptr, ZERO_EINVAL, "n_threads %d not in 0..1024", n_threads);
+  if (n == 0) return ZERO_OK;
+  const void* ptrs[5] = {grad, master, exp_avg, exp_avg_sq, param16};
+  const char* names[5] = {"grad", "master", "exp_avg", "exp_avg_sq", "param16"};
+  for (int k = 0; k < 5; ++k) {
+    if (!ptrs[k]) return fail(nullptr, ZERO_EINVAL, "%s is NULL", names[k]);
+    if (!aligned(ptrs[k], k == 4 ? 2 : 4)) return fail(nullptr, ZERO_EINVAL, "%s is misaligned", names[k]);
+  }
+  int threads = n_threads > 0 ? n_threads : static_cast<int>(std::thread::hardware_concurrency());
+  if (threads < 1) threads = 1;
+  const zfs_host::AdamScalars sc = adam_scalars(*cfg, t);
+  zfs_host::Pool* pool = zfs_host::pool_create(threads);
+  if (!pool) return fail(nullptr, ZERO_ENOMEM, "cannot start %d host threads", threads);
+  const HostAdamJob job{sc, grad, master, exp_avg, exp_avg_sq, param16};
+  zfs_host::pool_run(pool, n, [&job](int64_t lo, int64_t hi) { job(lo, hi); });
+  zfs_host::pool_destroy(pool);
+  return ZERO_OK;
+}
+
 namespace {
 
 int64_t clip_partials_end(const zero_ctx* ctx) { return zfs::kClipHeaderBytes + 8 * total_chunks(ctx); }
@@ -626,6 +937,8 @@ zero_status zero_clip_grad_norm_ex(zero_ctx* ctx, float max_norm, int32_t flags,
   const bool keep = (flags & ZERO_CLIP_KEEP_REDUCED) != 0;
   zero_status st = require_bound(ctx);
   if (st != ZERO_OK) return st;
+  if (keep && ctx->offload)
+    return fail(ctx, ZERO_ENOTSUP, "ZERO_CLIP_KEEP_REDUCED is not available in an offload context");
   if (ctx->phase == Phase::kStepped) return fail(ctx, ZERO_ESTATE, "clip after step: call post_step first");
   int32_t missing = -1;
   if (!all_registered(ctx, &missing)) return fail(ctx, ZERO_ESTATE, "unit %d has no registered gradients", missing);
@@ -754,6 +1067,32 @@ zero_status check_state_buffers(zero_ctx* ctx, const void* const* ptrs, const ch
   return ZERO_OK;
 }
 
+// Offload import: host state zeroed (pads), each unit's real elements copied
+// down, param16 = bf16(master) on the device; synchronizes the stream.
+zero_status import_offload(zero_ctx* ctx, const float* master_in, const float* exp_avg_in,
+                           const float* exp_avg_sq_in, int64_t t, cudaStream_t s) {
+  uint16_t* p16 = static_cast<uint16_t*>(ctx->bufs.param16);
+  float* dst[3] = {ctx->bufs.master, ctx->bufs.exp_avg, ctx->bufs.exp_avg_sq};
+  const float* src[3] = {master_in, exp_avg_in, exp_avg_sq_in};
+  cudaError_t e = cudaStreamSynchronize(s);  // no earlier work still reading the host state
+  if (e != cudaSuccess) return fail_cuda(ctx, "import synchronize", e);
+  for (int k = 0; k < 3; ++k) std::memset(dst[k], 0, static_cast<size_t>(ctx->padded_total) * sizeof(float));
+  if (ctx->padded_total > 0) e = cudaMemsetAsync(p16, 0, static_cast<size_t>(ctx->padded_total) * 2, s);
+  int64_t in = 0;
+  for (int32_t i = 0; i < ctx->n_units && e == cudaSuccess; ++i) {
+    const int64_t n = ctx->unit_numel[i], base = ctx->unit_base[i];
+    for (int k = 0; k < 3 && e == cudaSuccess && n > 0; ++k) {
+      e = cudaMemcpyAsync(dst[k] + base, src[k] + in, n * sizeof(float), cudaMemcpyDeviceToHost, s);
+    }
+    if (e == cudaSuccess) e = zfs::launch_copy_param(master_in + in, nullptr, p16, base, n, s);
+    in += n;
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(ctx, "import copy", e);
+  ctx->t = t;
+  return ZERO_OK;
+}
+
 }  // namespace
 
 zero_status zero_export_state(zero_ctx* ctx, float* master_out, float* exp_avg_out, float* exp_avg_sq_out,
@@ -772,9 +1111,14 @@ zero_status zero_export_state(zero_ctx* ctx, float* master_out, float* exp_avg_o
   int64_t out = 0;
   for (int32_t i = 0; i < ctx->n_units; ++i) {
     for (int k = 0; k < 3; ++k) {
-      const cudaError_t e = zfs::launch_copy_f32(src[k] + ctx->unit_base[i], dst[k] + out, ctx->unit_numel[i], s);
+      const int64_t n = ctx->unit_numel[i];
+      const float* from = src[k] + ctx->unit_base[i];
+      // Offload: the state is host memory, copied up in the same order.
+      const cudaError_t e = ctx->offload
+          ? (n > 0 ? cudaMemcpyAsync(dst[k] + out, from, n * sizeof(float), cudaMemcpyHostToDevice, s) : cudaSuccess)
+          : zfs::launch_copy_f32(from, dst[k] + out, n, s);
       if (e != cudaSuccess) return fail_cuda(ctx, "export copy", e);
-      if (ctx->unit_numel[i] > 0) ++launches;
+      if (n > 0 && !ctx->offload) ++launches;
     }
     out += ctx->unit_numel[i];
   }
@@ -796,6 +1140,7 @@ zero_status zero_import_state(zero_ctx* ctx, const float* master_in, const float
   if (st != ZERO_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint16_t* p16 = static_cast<uint16_t*>(ctx->bufs.param16);
+  if (ctx->offload) return import_offload(ctx, master_in, exp_avg_in, exp_avg_sq_in, t, s);
   cudaError_t e = zfs::launch_zero_fill(ctx->bufs.master, ctx->bufs.exp_avg, ctx->bufs.exp_avg_sq, p16,
                                         ctx->padded_total, s);
   if (e != cudaSuccess) return fail_cuda(ctx, "import zero fill", e);

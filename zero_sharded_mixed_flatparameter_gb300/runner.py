@@ -5,6 +5,12 @@ owns the stream; every step of the path runs in the library's kernels.
 and the bf16 parameter buffer of ``padded_numel`` elements on the device,
 builds the master with ``zero_make_master`` and then drives the protocol:
 ``reduce_grads`` -> ``step`` -> ``gather_weights`` -> ``post_step``.
+
+With ``offload=True`` (ZeRO-Offload) master / m / v are host tensors instead,
+the context comes from ``zero_make_master_offload`` and ``step`` runs
+``zero_offload_step``: the reduced gradient goes down to the host chunk by
+chunk, the library's multi-threaded CPU Adam updates the host state and the
+bf16 parameters come back up, on a second (copy) stream.
 """
 
 from __future__ import annotations
@@ -21,7 +27,8 @@ class FlatStep:
                  grad_dtype: str = "bf16", lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999,
                  eps: float = 1e-8, weight_decay: float = 0.0, adamw: bool = False,
                  init_params: Sequence[torch.Tensor] = (), device: str | torch.device = "cuda",
-                 guard: int = 0, guard_value: float = float("nan")):
+                 guard: int = 0, guard_value: float = float("nan"), offload: bool = False,
+                 offload_chunk: int = 1 << 22, offload_threads: int = 0):
         self.param_numel = [int(x) for x in param_numel]
         self.param_unit = [int(x) for x in param_unit]
         self.stage, self.n_ranks, self.grad_dtype = stage, n_ranks, grad_dtype
@@ -41,23 +48,31 @@ class FlatStep:
         self.guard = guard
         n = self.padded + 2 * guard
 
-        def alloc(dtype):
-            t = torch.empty(max(n, 1), dtype=dtype, device=self.device)
+        def alloc(dtype, device):
+            t = torch.empty(max(n, 1), dtype=dtype, device=device)
             t.fill_(guard_value)
             return t
 
-        self._master, self._m, self._v = alloc(torch.float32), alloc(torch.float32), alloc(torch.float32)
-        self._p16 = alloc(torch.bfloat16)
+        self.offload = bool(offload)
+        state_device = torch.device("cpu") if self.offload else self.device
+        self._master, self._m, self._v = (alloc(torch.float32, state_device) for _ in range(3))
+        self._p16 = alloc(torch.bfloat16, self.device)
         if len(init_params) != len(self.param_numel):
             raise ValueError("need one fp32 init tensor per parameter")
         self._init = [p.contiguous() for p in init_params]
         for p, k in zip(self._init, self.param_numel):
             if p.dtype != torch.float32 or p.numel() != k:
                 raise ValueError("init params must be fp32 tensors of the declared sizes")
-        self.ctx = B.zero_make_master(self.cfg, self.param_numel, self.param_unit,
-                                      [p.data_ptr() for p in self._init],
-                                      self._ptr(self._master), self._ptr(self._m), self._ptr(self._v),
-                                      self._ptr(self._p16), self.stream_handle())
+        make = B.zero_make_master_offload if self.offload else B.zero_make_master
+        self.ctx = make(self.cfg, self.param_numel, self.param_unit, [p.data_ptr() for p in self._init],
+                        self._ptr(self._master), self._ptr(self._m), self._ptr(self._v),
+                        self._ptr(self._p16), self.stream_handle())
+        if self.offload:
+            self.offload_chunk, self.offload_threads = int(offload_chunk), int(offload_threads)
+            hb, db = B.zero_offload_workspace_bytes(self.ctx, self.offload_chunk)
+            self._host_ws = torch.empty(hb, dtype=torch.uint8, pin_memory=True)
+            self._dev_ws = torch.empty(db, dtype=torch.uint8, device=self.device)
+            self._copy_stream = torch.cuda.Stream(self.device)
         # make_master reads the init params on the stream; once it has run they
         # may be released.
         torch.cuda.current_stream(self.device).synchronize()
@@ -148,7 +163,12 @@ class FlatStep:
                                 [a.data_ptr() for a in accumulators], first, self.stream_handle(stream))
 
     def step(self, stream=None) -> None:
-        B.zero_step(self.ctx, self.stream_handle(stream))
+        if self.offload:
+            B.zero_offload_step(self.ctx, self.offload_chunk, self._host_ws.data_ptr(), self._host_ws.numel(),
+                                self._dev_ws.data_ptr(), self._dev_ws.numel(), self.offload_threads,
+                                self.stream_handle(stream), self.stream_handle(self._copy_stream))
+        else:
+            B.zero_step(self.ctx, self.stream_handle(stream))
 
     def gather_weights(self, unit: int, out: Optional[torch.Tensor], stream=None) -> None:
         B.zero_gather_weights(self.ctx, unit, out.data_ptr() if out is not None else 0, self.stream_handle(stream))
