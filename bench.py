@@ -269,6 +269,49 @@ def cpu_baseline(wl, sample_params: int = 4_000_000, min_seconds: float = 10.0):
                        f"of the workload (N={wl['n']}, {wl['grad_dtype']} grads), {dt:.1f} s single-threaded")}
 
 
+def cpu_adam_baseline(sample_params: int = 16_000_000, min_seconds: float = 3.0):
+    """The library's ZeRO-Offload CPU Adam (zero_cpu_adam) on host arrays, all
+    host cores: the second, optimised CPU baseline."""
+    import ctypes
+    import numpy as np
+    from zero_sharded_mixed_flatparameter_gb300 import binding as B
+    rng = np.random.default_rng(7)
+    g = rng.normal(0, 1e-3, sample_params).astype(np.float32)
+    w = rng.normal(0, 0.02, sample_params).astype(np.float32)
+    m, v = np.zeros_like(w), np.zeros_like(w)
+    p16 = np.zeros(sample_params, np.uint16)
+    ptr = [a.ctypes.data_as(ctypes.c_void_p).value for a in (g, w, m, v, p16)]
+    cfg = B.make_config(2, 1, "fp32")
+    threads = os.cpu_count() or 1
+    B.zero_cpu_adam(cfg, 1, *ptr, sample_params, threads)  # first touch, warm-up
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        B.zero_cpu_adam(cfg, steps + 2, *ptr, sample_params, threads)
+        steps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    value = sample_params * steps / dt
+    return {"value": value, "unit": UNIT, "cores": threads, "kind": "library host Adam (zero_cpu_adam)",
+            "host_gbs": value * 30 / 1e9,
+            "sample": (f"{steps} host Adam steps over {sample_params:,} params (fp32 grad, master, m, v; bf16 out: "
+                       f"30 B/param of host memory traffic), {dt:.1f} s on {threads} threads")}
+
+
+def host_copy_gbs(n: int = 128 * 1024 * 1024, reps: int = 5) -> float:
+    """Host memory copy bandwidth (bytes read + written) with torch's CPU threads."""
+    import torch
+    a = torch.ones(n, dtype=torch.float32)
+    b = torch.empty_like(a)
+    b.copy_(a)
+    best = 0.0
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        b.copy_(a)
+        best = max(best, 8 * n / (time.perf_counter() - t0) / 1e9)
+    return best
+
+
 # ---------------------------------------------------------------------------
 # Our arm.
 # ---------------------------------------------------------------------------
@@ -296,8 +339,11 @@ def run_ours(args):
     for k in pl.numel:
         offs.append(offs[-1] + k)
     init = [init_flat[offs[p]:offs[p + 1]] for p in range(len(pl.numel))]
+    offload_kw = {}
+    if args.offload:
+        offload_kw = dict(offload=True, offload_chunk=args.offload_chunk, offload_threads=args.offload_threads)
     fs = FlatStep(pl.numel, pl.unit, stage=wl["stage"], n_ranks=n, grad_dtype=wl["grad_dtype"], init_params=init,
-                  device=device)
+                  device=device, **offload_kw)
     del init, init_flat
     padded = fs.padded
     grads = si.replica_grads(n, padded, wl["grad_std"], 100 + rank, wl["grad_dtype"], device=device,
@@ -408,7 +454,7 @@ def run_ours(args):
     # stream into the second of two device buffer sets while step k runs and
     # its parameters are read back on the compute stream.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.offload:
         host_grads = [g.to("cpu").pin_memory() for g in grads]
         host_out = torch.empty(padded, dtype=torch.bfloat16).pin_memory()
         bufs = [grads, [torch.empty_like(g) for g in grads]]
@@ -465,9 +511,34 @@ def run_ours(args):
     del grads
     torch.cuda.empty_cache()
 
-    cpu = None
+    cpu = cpu_adam = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
+        cpu_adam = cpu_adam_baseline()
+
+    roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                "frac": achieved_gbs / peak, "peak_source": f"hbm_gbs {peak_kind}",
+                "traffic": traffic, "algorithmic_bytes_per_launch": bytes_per_launch,
+                "bytes_per_param": bpp, "kernel": step_kernel_name(n, wl["grad_dtype"], args.clip_keep, padded),
+                "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms)}
+    offload = None
+    if args.offload:
+        # The offloaded step is bound by the host: its Adam moves 30 B/param of
+        # host memory (fp32 grad, master, m, v read; master, m, v, bf16 written),
+        # against the host's own copy bandwidth.  The link carries 4 B/param
+        # down (reduced fp32 gradient) and 2 B/param up (bf16 parameters).
+        host_peak = host_copy_gbs()
+        host_gbs = 30 * padded / (kern_ms_max / 1e3) / 1e9
+        roofline = {"bound": "host", "achieved": host_gbs, "peak": host_peak, "unit": "GB/s",
+                    "frac": host_gbs / host_peak, "peak_source": "host memory copy measured in this run (torch CPU copy)",
+                    "traffic": None, "algorithmic_bytes_per_launch": 30 * padded, "bytes_per_param": 30,
+                    "kernel": "zero_offload_step (host Adam; reduce_out_kernel on the GPU)",
+                    "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms)}
+        offload = {"chunk": args.offload_chunk, "threads": args.offload_threads or os.cpu_count(),
+                   "d2h_bytes_per_step": 4 * padded, "h2d_bytes_per_step": 2 * padded,
+                   "link_gbs": 6 * padded / (kern_ms_max / 1e3) / 1e9,
+                   "note": "fp32 master/m/v in host memory; per chunk: GPU reduce -> D2H -> host Adam -> H2D, "
+                           "3 chunks in flight"}
 
     if rank == 0:
         line = {
@@ -479,12 +550,10 @@ def run_ours(args):
                        "grad_dtype": wl["grad_dtype"], "optimizer": "Adam fp32 (lr 1e-3, betas 0.9/0.999, eps 1e-8)",
                        "parallelism": f"{world} GPU replica(s); N={n} DP ranks simulated per GPU",
                        "l2": f"inputs larger than L2: {bytes_per_launch / 1e9:.2f} GB moved per step (L2 129 MB)"},
-            "hbm_gbs": achieved_gbs, "hbm_frac_of_peak": achieved_gbs / peak,
-            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
-                         "frac": achieved_gbs / peak, "peak_source": f"hbm_gbs {peak_kind}",
-                         "traffic": traffic, "algorithmic_bytes_per_launch": bytes_per_launch,
-                         "bytes_per_param": bpp, "kernel": step_kernel_name(n, wl["grad_dtype"], args.clip_keep, padded),
-                         "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms)},
+            "hbm_gbs": None if args.offload else achieved_gbs,
+            "hbm_frac_of_peak": None if args.offload else achieved_gbs / peak,
+            "roofline": roofline,
+            "offload": offload,
             "clip": None if clip_ms is None else {
                 "max_norm": args.clip, "norm_pass_ms_mean": statistics.mean(clip_ms),
                 "keep_reduced": args.clip_keep,
@@ -502,6 +571,7 @@ def run_ours(args):
                 "accumulate_gbs": n * padded * (6 + 10 * (args.accum - 1)) / (statistics.mean(accum_ms) / 1e3) / 1e9,
                 "note": "K micro-steps of bf16 grads accumulated into the fp32 replica gradients, then the step"},
             "cpu_baseline": cpu,
+            "cpu_adam": cpu_adam,
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clock,
@@ -621,12 +691,16 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default 2000; 50 with --offload)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama1024_zero2_n8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--offload", action="store_true",
+                    help="ZeRO-Offload: fp32 state in host memory, the step through zero_offload_step")
+    ap.add_argument("--offload-chunk", type=int, default=1 << 22)
+    ap.add_argument("--offload-threads", type=int, default=0)
     ap.add_argument("--accum", type=int, default=0,
                     help="fp32 gradient accumulation of this many bf16 micro-steps before every step (fp32 workloads)")
     ap.add_argument("--clip-keep", action="store_true",
@@ -638,6 +712,8 @@ def main():
     ap.add_argument("--clip", type=float, default=0.0,
                     help="global-norm clipping to this max norm before every step (0: off)")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 50 if args.offload else 2000
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
     if args.sweep:

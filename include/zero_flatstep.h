@@ -413,7 +413,8 @@ zero_status zero_offload_step(zero_ctx* ctx, int64_t chunk, void* host_workspace
  * master, exp_avg, exp_avg_sq in place with step t (>= 1) of cfg's
  * optimizer and writes param16 = bf16(master) (bit patterns, round to
  * nearest even).  Same arithmetic as the device step.  n_threads as above;
- * threads are started and joined inside the call.  No CUDA call is made.
+ * the threads belong to one process-wide pool kept between calls (calls from
+ * several threads take turns).  No CUDA call is made.
  * Errors: ZERO_EINVAL (config, t < 1, n < 0, NULL or misaligned pointer);
  * ZERO_ENOMEM.
  */

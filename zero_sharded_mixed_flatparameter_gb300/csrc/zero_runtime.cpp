@@ -11,6 +11,8 @@
 #include <algorithm>
 #include <cmath>
 #include <functional>
+#include <memory>
+#include <mutex>
 #include <thread>
 #include <cstdarg>
 #include <cstdint>
@@ -893,11 +895,19 @@ zero_status zero_cpu_adam(const zero_config* cfg, int64_t t, const float* grad, 
   int threads = n_threads > 0 ? n_threads : static_cast<int>(std::thread::hardware_concurrency());
   if (threads < 1) threads = 1;
   const zfs_host::AdamScalars sc = adam_scalars(*cfg, t);
-  zfs_host::Pool* pool = zfs_host::pool_create(threads);
-  if (!pool) return fail(nullptr, ZERO_ENOMEM, "cannot start %d host threads", threads);
+  // One process-wide pool for these context-free calls (kept between calls:
+  // starting the threads costs about as much as updating a few million
+  // elements); concurrent callers take turns.
+  static std::mutex pool_mutex;
+  static std::unique_ptr<zfs_host::Pool, void (*)(zfs_host::Pool*)> pool(nullptr, zfs_host::pool_destroy);
+  std::lock_guard<std::mutex> lock(pool_mutex);
+  if (!pool || zfs_host::pool_threads(pool.get()) != threads) {
+    pool.reset();
+    pool.reset(zfs_host::pool_create(threads));
+    if (!pool) return fail(nullptr, ZERO_ENOMEM, "cannot start %d host threads", threads);
+  }
   const HostAdamJob job{sc, grad, master, exp_avg, exp_avg_sq, param16};
-  zfs_host::pool_run(pool, n, [&job](int64_t lo, int64_t hi) { job(lo, hi); });
-  zfs_host::pool_destroy(pool);
+  zfs_host::pool_run(pool.get(), n, [&job](int64_t lo, int64_t hi) { job(lo, hi); });
   return ZERO_OK;
 }
 
