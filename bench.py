@@ -523,15 +523,16 @@ def run_ours(args):
                 "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms)}
     offload = None
     if args.offload:
-        # The offloaded step is bound by the host: its Adam moves 30 B/param of
-        # host memory (fp32 grad, master, m, v read; master, m, v, bf16 written),
-        # against the host's own copy bandwidth.  The link carries 4 B/param
-        # down (reduced fp32 gradient) and 2 B/param up (bf16 parameters).
+        # The offloaded step is bound by host memory: the host Adam moves
+        # 30 B/param (fp32 grad, master, m, v read; master, m, v, bf16 written)
+        # and the copies another 6 (the fp32 gradient written by the D2H copy,
+        # the bf16 parameters read by the H2D copy), against the host's own copy
+        # bandwidth.  The link carries 4 B/param down and 2 B/param up.
         host_peak = host_copy_gbs()
-        host_gbs = 30 * padded / (kern_ms_max / 1e3) / 1e9
+        host_gbs = 36 * padded / (kern_ms_max / 1e3) / 1e9
         roofline = {"bound": "host", "achieved": host_gbs, "peak": host_peak, "unit": "GB/s",
                     "frac": host_gbs / host_peak, "peak_source": "host memory copy measured in this run (torch CPU copy)",
-                    "traffic": None, "algorithmic_bytes_per_launch": 30 * padded, "bytes_per_param": 30,
+                    "traffic": None, "algorithmic_bytes_per_launch": 36 * padded, "bytes_per_param": 36,
                     "kernel": "zero_offload_step (host Adam; reduce_out_kernel on the GPU)",
                     "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms)}
         offload = {"chunk": args.offload_chunk, "threads": args.offload_threads or os.cpu_count(),
@@ -699,7 +700,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--offload", action="store_true",
                     help="ZeRO-Offload: fp32 state in host memory, the step through zero_offload_step")
-    ap.add_argument("--offload-chunk", type=int, default=1 << 22)
+    ap.add_argument("--offload-chunk", type=int, default=1 << 23)
     ap.add_argument("--offload-threads", type=int, default=0)
     ap.add_argument("--accum", type=int, default=0,
                     help="fp32 gradient accumulation of this many bf16 micro-steps before every step (fp32 workloads)")

@@ -173,7 +173,7 @@ def gpu_flatstep(pb: Problem, guard: int = 64, device="cuda", offload: Optional[
     h = pb.hyper
     extra = {}
     if offload is not None:
-        extra = dict(offload=True, offload_chunk=offload.get("chunk", 1 << 22),
+        extra = dict(offload=True, offload_chunk=offload.get("chunk", 1 << 23),
                      offload_threads=offload.get("threads", 0))
     return FlatStep(pb.pl.numel, pb.pl.unit, stage=pb.stage, n_ranks=pb.n, grad_dtype=pb.grad_dtype,
                     lr=h.lr, beta1=h.beta1, beta2=h.beta2, eps=h.eps, weight_decay=h.weight_decay,

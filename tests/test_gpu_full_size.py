@@ -60,14 +60,15 @@ def _master_window(init_flat_host_fn, lay, pl, a, b):
 
 
 def run_full(pl, n, stage, grad_dtype, steps, seed, grad_std, outlier_fraction=0.0, gather=False,
-             register_units=True):
+             register_units=True, offload=False):
     lay = oracle.layout(pl.numel, pl.unit, n, stage)
     total = lay.total_padded
     # init params: one flat fp32 draw of all parameters, per-param views
     init_flat = si.normal_fp32(pl.total, 0.02, seed, device="cuda")
     cum = np.concatenate([[0], np.cumsum(pl.numel)])
     init = [init_flat[int(cum[p]):int(cum[p + 1])] for p in range(len(pl.numel))]
-    fs = FlatStep(pl.numel, pl.unit, stage=stage, n_ranks=n, grad_dtype=grad_dtype, init_params=init)
+    fs = FlatStep(pl.numel, pl.unit, stage=stage, n_ranks=n, grad_dtype=grad_dtype, init_params=init,
+                  offload=offload)
     try:
         assert (fs.padded, fs.n_units) == (total, len(lay.unit_numel))
         for i in range(fs.n_units):
@@ -133,6 +134,12 @@ def run_full(pl, n, stage, grad_dtype, steps, seed, grad_std, outlier_fraction=0
 def test_llama_1024_zero2_n8():
     # 73,417,728 params in one FlatParameter, N = 8, ZeRO-2, bf16 grads N(0, 1e-3), 10 steps
     assert run_full(si.llama_1024(), 8, 2, "bf16", 10, seed=2, grad_std=1e-3, register_units=False) == 10
+
+
+def test_llama_1024_zero2_n8_offload():
+    # the same workload as a ZeRO-Offload context (host fp32 state, 8 M-element chunks), 3 steps
+    assert run_full(si.llama_1024(), 8, 2, "bf16", 3, seed=12, grad_std=1e-3, register_units=False,
+                    offload=True) == 3
 
 
 def test_llama_2048_zero3_units_n8_gather():

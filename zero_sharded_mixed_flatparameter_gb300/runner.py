@@ -28,7 +28,7 @@ class FlatStep:
                  eps: float = 1e-8, weight_decay: float = 0.0, adamw: bool = False,
                  init_params: Sequence[torch.Tensor] = (), device: str | torch.device = "cuda",
                  guard: int = 0, guard_value: float = float("nan"), offload: bool = False,
-                 offload_chunk: int = 1 << 22, offload_threads: int = 0):
+                 offload_chunk: int = 1 << 23, offload_threads: int = 0):
         self.param_numel = [int(x) for x in param_numel]
         self.param_unit = [int(x) for x in param_unit]
         self.stage, self.n_ranks, self.grad_dtype = stage, n_ranks, grad_dtype
