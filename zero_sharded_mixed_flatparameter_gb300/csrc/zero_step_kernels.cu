@@ -223,7 +223,7 @@ __device__ __forceinline__ void locate_tile(const StepArgs& a, long long id, int
 template <int N, bool kFp32>
 __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_constant__ StepArgs a) {
   using L = TmaTile<N, kFp32>;
-  static_assert(kTmaTile == kStepThreads * kVec, "one 8-element vector per thread per tile");
+  static_assert(kTmaTile == kStepThreads * kVec, "8 elements per thread per tile");
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t bars[kTmaStages];
   long long n_tiles = 0;
@@ -276,43 +276,55 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
       if (threadIdx.x == 0) atomicAdd(&g_step_timeouts, 1u);
       break;
     }
+    // Which 8 elements of the tile a thread takes.  bf16 gradients: 4t..4t+3
+    // of each half of the tile, so every warp reads contiguous 256-512 B runs
+    // of shared memory (no bank conflicts; measured +0.4-2.7 % at N = 14-16).
+    // fp32 gradients: 8t..8t+7 with the loads and stores below in this
+    // order, which measured 7-10 % faster at N = 8, 9 than the split mapping
+    // and 4-7 % faster than this mapping with the two halves' stores
+    // interleaved.  The arithmetic per element is the same either way.
     const unsigned char* st = smem + static_cast<size_t>(stage) * L::kStageBytes;
-    const int t8 = threadIdx.x * kVec;
+    constexpr int kHalf = kTmaTile / 2;
+    const int e_lo = kFp32 ? threadIdx.x * kVec : threadIdx.x * 4;      // elements e_lo .. e_lo + 3
+    const int e_hi = kFp32 ? threadIdx.x * kVec + 4 : kHalf + threadIdx.x * 4;  // and e_hi .. e_hi + 3
     float g[kVec];
     if constexpr (!kFp32) {
-      const uint4 r0 = *reinterpret_cast<const uint4*>(st + t8 * 2);
-      g[0] = bf16_lo(r0.x); g[1] = bf16_hi(r0.x); g[2] = bf16_lo(r0.y); g[3] = bf16_hi(r0.y);
-      g[4] = bf16_lo(r0.z); g[5] = bf16_hi(r0.z); g[6] = bf16_lo(r0.w); g[7] = bf16_hi(r0.w);
 #pragma unroll
-      for (int r = 1; r < N; ++r) {
-        const uint4 x = *reinterpret_cast<const uint4*>(st + r * L::kGradBytes + t8 * 2);
-        g[0] = __fadd_rn(g[0], bf16_lo(x.x)); g[1] = __fadd_rn(g[1], bf16_hi(x.x));
-        g[2] = __fadd_rn(g[2], bf16_lo(x.y)); g[3] = __fadd_rn(g[3], bf16_hi(x.y));
-        g[4] = __fadd_rn(g[4], bf16_lo(x.z)); g[5] = __fadd_rn(g[5], bf16_hi(x.z));
-        g[6] = __fadd_rn(g[6], bf16_lo(x.w)); g[7] = __fadd_rn(g[7], bf16_hi(x.w));
+      for (int h = 0; h < 2; ++h) {
+        const int e0 = h ? e_hi : e_lo;
+        float* gh = g + 4 * h;
+        const uint2 r0 = *reinterpret_cast<const uint2*>(st + e0 * 2);
+        gh[0] = bf16_lo(r0.x); gh[1] = bf16_hi(r0.x); gh[2] = bf16_lo(r0.y); gh[3] = bf16_hi(r0.y);
+#pragma unroll
+        for (int r = 1; r < N; ++r) {
+          const uint2 x = *reinterpret_cast<const uint2*>(st + r * L::kGradBytes + e0 * 2);
+          gh[0] = __fadd_rn(gh[0], bf16_lo(x.x)); gh[1] = __fadd_rn(gh[1], bf16_hi(x.x));
+          gh[2] = __fadd_rn(gh[2], bf16_lo(x.y)); gh[3] = __fadd_rn(gh[3], bf16_hi(x.y));
+        }
       }
     } else {
-      const float* g0 = reinterpret_cast<const float*>(st) + t8;
+      const float* g0 = reinterpret_cast<const float*>(st) + e_lo;
 #pragma unroll
       for (int e = 0; e < kVec; ++e) g[e] = g0[e];
 #pragma unroll
       for (int r = 1; r < N; ++r) {
-        const float* gr = reinterpret_cast<const float*>(st + r * L::kGradBytes) + t8;
+        const float* gr = reinterpret_cast<const float*>(st + r * L::kGradBytes) + e_lo;
         const float4 x0 = *reinterpret_cast<const float4*>(gr), x1 = *reinterpret_cast<const float4*>(gr + 4);
         g[0] = __fadd_rn(g[0], x0.x); g[1] = __fadd_rn(g[1], x0.y); g[2] = __fadd_rn(g[2], x0.z);
         g[3] = __fadd_rn(g[3], x0.w); g[4] = __fadd_rn(g[4], x1.x); g[5] = __fadd_rn(g[5], x1.y);
         g[6] = __fadd_rn(g[6], x1.z); g[7] = __fadd_rn(g[7], x1.w);
       }
     }
-    const float* sw = reinterpret_cast<const float*>(st + N * L::kGradBytes) + t8;
-    const float* sm = reinterpret_cast<const float*>(st + N * L::kGradBytes + L::kStateBytes) + t8;
-    const float* sv = reinterpret_cast<const float*>(st + N * L::kGradBytes + 2 * L::kStateBytes) + t8;
+    const float* sw = reinterpret_cast<const float*>(st + N * L::kGradBytes);
+    const float* sm = reinterpret_cast<const float*>(st + N * L::kGradBytes + L::kStateBytes);
+    const float* sv = reinterpret_cast<const float*>(st + N * L::kGradBytes + 2 * L::kStateBytes);
     float w[kVec], m[kVec], v[kVec];
 #pragma unroll
-    for (int e = 0; e < kVec; e += 4) {
-      *reinterpret_cast<float4*>(w + e) = *reinterpret_cast<const float4*>(sw + e);
-      *reinterpret_cast<float4*>(m + e) = *reinterpret_cast<const float4*>(sm + e);
-      *reinterpret_cast<float4*>(v + e) = *reinterpret_cast<const float4*>(sv + e);
+    for (int h = 0; h < 2; ++h) {
+      const int e0 = h ? e_hi : e_lo;
+      *reinterpret_cast<float4*>(w + 4 * h) = *reinterpret_cast<const float4*>(sw + e0);
+      *reinterpret_cast<float4*>(m + 4 * h) = *reinterpret_cast<const float4*>(sm + e0);
+      *reinterpret_cast<float4*>(v + 4 * h) = *reinterpret_cast<const float4*>(sv + e0);
     }
     __syncthreads();  // every thread holds its operands: the stage can be refilled
     if (threadIdx.x == 0) {
@@ -325,19 +337,34 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
     int si;
     long long ti;
     locate_tile(a, id, &si, &ti);
-    const long long j = a.seg[si].base + ti * kTmaTile + t8;
-    st_stream_f4(a.master + j, make_float4(w[0], w[1], w[2], w[3]));
-    st_stream_f4(a.master + j + 4, make_float4(w[4], w[5], w[6], w[7]));
-    st_stream_f4(a.m + j, make_float4(m[0], m[1], m[2], m[3]));
-    st_stream_f4(a.m + j + 4, make_float4(m[4], m[5], m[6], m[7]));
-    st_stream_f4(a.v + j, make_float4(v[0], v[1], v[2], v[3]));
-    st_stream_f4(a.v + j + 4, make_float4(v[4], v[5], v[6], v[7]));
-    uint4 out;
-    out.x = pack_bf16x2(w[0], w[1]);
-    out.y = pack_bf16x2(w[2], w[3]);
-    out.z = pack_bf16x2(w[4], w[5]);
-    out.w = pack_bf16x2(w[6], w[7]);
-    st_stream(a.p16 + j, out);
+    const long long j_lo = a.seg[si].base + ti * kTmaTile + e_lo;
+    const long long j_hi = a.seg[si].base + ti * kTmaTile + e_hi;
+    if constexpr (kFp32) {
+      st_stream_f4(a.master + j_lo, make_float4(w[0], w[1], w[2], w[3]));
+      st_stream_f4(a.master + j_hi, make_float4(w[4], w[5], w[6], w[7]));
+      st_stream_f4(a.m + j_lo, make_float4(m[0], m[1], m[2], m[3]));
+      st_stream_f4(a.m + j_hi, make_float4(m[4], m[5], m[6], m[7]));
+      st_stream_f4(a.v + j_lo, make_float4(v[0], v[1], v[2], v[3]));
+      st_stream_f4(a.v + j_hi, make_float4(v[4], v[5], v[6], v[7]));
+      uint4 out;
+      out.x = pack_bf16x2(w[0], w[1]);
+      out.y = pack_bf16x2(w[2], w[3]);
+      out.z = pack_bf16x2(w[4], w[5]);
+      out.w = pack_bf16x2(w[6], w[7]);
+      st_stream(a.p16 + j_lo, out);
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const long long j = h ? j_hi : j_lo;
+        st_stream_f4(a.master + j, make_float4(w[4 * h], w[4 * h + 1], w[4 * h + 2], w[4 * h + 3]));
+        st_stream_f4(a.m + j, make_float4(m[4 * h], m[4 * h + 1], m[4 * h + 2], m[4 * h + 3]));
+        st_stream_f4(a.v + j, make_float4(v[4 * h], v[4 * h + 1], v[4 * h + 2], v[4 * h + 3]));
+        uint2 out;  // 4 contiguous bf16 per half: a warp writes 256 B runs
+        out.x = pack_bf16x2(w[4 * h], w[4 * h + 1]);
+        out.y = pack_bf16x2(w[4 * h + 2], w[4 * h + 3]);
+        __stcs(reinterpret_cast<uint2*>(a.p16 + j), out);
+      }
+    }
   }
   if (gave_up) {
     // Bounded drain of copies that may still land in this CTA's shared memory.
