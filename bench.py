@@ -606,7 +606,9 @@ def run_sweep(args):
             init = si.normal_fp32(numel, 0.02, 1, device=device)
             fs = FlatStep([numel], [0], stage=2, n_ranks=n, init_params=[init], device=device)
             del init
-            grads = si.replica_grads(n, numel, 1e-2, 2, "bf16", device=device, outlier_fraction=0.001)
+            # N replica buffers of the padded length (pads zero, as the hook pads them)
+            grads = si.replica_grads(n, fs.padded, 1e-2, 2, "bf16", device=device, outlier_fraction=0.001,
+                                     pad_from=numel)
             nbytes = bytes_per_param(n, "bf16") * fs.padded
             reps = max(5, min(50, int(2e10 // max(nbytes, 1))))
 

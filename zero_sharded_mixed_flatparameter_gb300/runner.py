@@ -126,11 +126,20 @@ class FlatStep:
         return torch.bfloat16 if self.grad_dtype == "bf16" else torch.float32
 
     # -- protocol ----------------------------------------------------------------
+    def _need(self, unit: int) -> int:
+        """Elements each replica buffer of `unit` (-1: all units) must hold:
+        the padded length the kernels read, pads included."""
+        return self.padded if unit < 0 else self.layout(unit)[1]
+
     def reduce_grads(self, unit: int, replica_grads: Sequence[torch.Tensor], stream=None) -> None:
         want = self.grad_dtype_torch()
+        need = self._need(unit)
         for g in replica_grads:
             if g.dtype != want or not g.is_contiguous() or g.device != self.device:
                 raise ValueError("replica grads must be contiguous device tensors of the configured dtype")
+            if g.numel() < need:
+                raise ValueError(f"replica grads must hold the padded {need} elements (pads included), "
+                                 f"got {g.numel()}")
         B.zero_reduce_grads(self.ctx, unit, [g.data_ptr() for g in replica_grads], self.stream_handle(stream))
         self._registered.append(list(replica_grads))  # keep alive until post_step
 
@@ -153,12 +162,17 @@ class FlatStep:
     def accumulate_grads(self, unit: int, micro_grads: Sequence[torch.Tensor], accumulators: Sequence[torch.Tensor],
                          first: bool, stream=None) -> None:
         """fp32 accumulation of one micro-step's bf16 replica gradients."""
+        need = self._need(unit)
         for g in micro_grads:
             if g.dtype != torch.bfloat16 or not g.is_contiguous() or g.device != self.device:
                 raise ValueError("micro gradients must be contiguous bf16 device tensors")
+            if g.numel() < need:
+                raise ValueError(f"micro gradients must hold the padded {need} elements, got {g.numel()}")
         for a in accumulators:
             if a.dtype != torch.float32 or not a.is_contiguous() or a.device != self.device:
                 raise ValueError("accumulators must be contiguous fp32 device tensors")
+            if a.numel() < need:
+                raise ValueError(f"accumulators must hold the padded {need} elements, got {a.numel()}")
         B.zero_accumulate_grads(self.ctx, unit, [g.data_ptr() for g in micro_grads],
                                 [a.data_ptr() for a in accumulators], first, self.stream_handle(stream))
 
