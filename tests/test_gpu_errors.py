@@ -61,6 +61,12 @@ def test_state_machine_and_no_side_effects():
         # post_step without a step
         assert _status(fs.post_step) == B.ZERO_ESTATE
         flats = upload_grads(pb, 1)
+        # the runner refuses replica buffers shorter than the padded length
+        # (the kernels read every padded element)
+        with pytest.raises(ValueError, match="padded"):
+            fs.reduce_grads(-1, [f[:fs.padded - 1] for f in flats])
+        with pytest.raises(ValueError, match="padded"):
+            fs.reduce_grads(0, [f[:fs.layout(0)[1] - 1] for f in flats])
         # partial registration is not enough
         numel, padded, shard, base = fs.layout(0)
         fs.reduce_grads(0, [f[base:base + padded] for f in flats])

@@ -159,9 +159,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
 // kTmaTile-element tile of every input stream into shared memory with one
 // cp.async.bulk per stream (4-8 KB contiguous requests), completing on an
 // mbarrier; kTmaStages tiles are in flight per CTA.  Measured on GB300 over a
-// 100 M-element buffer (GB/s, staged against register-staged): bf16 N = 14
-// 6988 / 6645, N = 15 7097 / 6632, N = 16 7146 / 6618; fp32 N = 8 7164 /
-// 6651, N = 9 7190 / 6634.  At bf16 N <= 13, fp32 N = 7 and fp32 N >= 10 the
+// 100 M-element buffer (GB/s, staged against register-staged): bf16 N = 11
+// 6770 / 6645, N = 12 6942 / 6640, N = 13 7059 / 6653, N = 14 7178 / 6645,
+// N = 16 7200 / 6618; fp32 N = 8 7164 / 6651, N = 9 7190 / 6634.  At bf16
+// N <= 10 (N = 8: 6143 / 6806), fp32 N = 7 and fp32 N >= 10 the
 // register-staged kernel is as fast or faster, so it stays the default there;
 // so it does for launches of fewer than kTmaMinElems elements, where one CTA
 // per SM works through too few tiles to hide the latency of each (N = 16
@@ -519,6 +520,9 @@ cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launche
   *launched = true;
   if (!a.grad_fp32) {
     switch (a.n_ranks) {
+      case 11: return launch_tma<11, false>(a, stream);
+      case 12: return launch_tma<12, false>(a, stream);
+      case 13: return launch_tma<13, false>(a, stream);
       case 14: return launch_tma<14, false>(a, stream);
       case 15: return launch_tma<15, false>(a, stream);
       case 16: return launch_tma<16, false>(a, stream);
