@@ -965,7 +965,6 @@ zero_status zero_clip_grad_norm_ex(zero_ctx* ctx, float max_norm, int32_t flags,
   double* partials = reinterpret_cast<double*>(ws + zfs::kClipHeaderBytes);
   float* keep_base = keep ? reinterpret_cast<float*>(ws + clip_keep_offset(ctx)) : nullptr;
   const int N = ctx->cfg.n_ranks;
-  const size_t esz = grad_bytes(ctx->cfg);
   int32_t launches = 0;
   int64_t out = 0;
   int32_t i = 0;
@@ -996,7 +995,6 @@ zero_status zero_clip_grad_norm_ex(zero_ctx* ctx, float max_norm, int32_t flags,
       chunks += c;
       out += c;
     }
-    (void)esz;
     a.nseg = n;
     if (chunks > 0) {
       const cudaError_t e = zfs::launch_grad_sq(a, chunks, s);
