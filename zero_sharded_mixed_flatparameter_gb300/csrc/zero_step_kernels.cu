@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
       if (id < n_tiles) issue(id, i);
     }
   }
-  bool gave_up = false;
+  long long gave_up_at = -1;  // the tile whose wait ran out, if any
   for (long long k = 0;; ++k) {
     const long long id = blockIdx.x + k * gridDim.x;
     if (id >= n_tiles) break;
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
     }
     // Every thread reaches this barrier; the CTA gives up together or not at all.
     if (__syncthreads_or(mine ? 1 : 0)) {
-      gave_up = true;
+      gave_up_at = k;
       if (threadIdx.x == 0) atomicAdd(&g_step_timeouts, 1u);
       break;
     }
@@ -367,11 +367,17 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
       }
     }
   }
-  if (gave_up) {
-    // Bounded drain of copies that may still land in this CTA's shared memory.
-    for (int s = 0; s < kTmaStages; ++s) {
+  if (gave_up_at >= 0) {
+    // Copies may still be landing in this CTA's shared memory: the tiles
+    // issued and not consumed are gave_up_at .. gave_up_at + kTmaStages - 1
+    // (those that exist), tile j in stage j % kTmaStages with phase parity
+    // (j / kTmaStages) & 1.  Wait for each, bounded, before leaving.
+    for (long long j = gave_up_at; j < gave_up_at + kTmaStages; ++j) {
+      if (blockIdx.x + j * gridDim.x >= n_tiles) break;
+      const int s = static_cast<int>(j % kTmaStages);
+      const uint32_t parity = static_cast<uint32_t>((j / kTmaStages) & 1);
       long long tries = 0;
-      while (!mbar_try_wait(&bars[s], 0) && !mbar_try_wait(&bars[s], 1) && ++tries < (1LL << 20)) {
+      while (!mbar_try_wait(&bars[s], parity) && ++tries < (1LL << 20)) {
       }
     }
     return;
