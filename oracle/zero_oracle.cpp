@@ -182,10 +182,20 @@ void adam_element(const Hyper& h, const StepScalars& s, float g, float* w, float
 
 // Compensated running sum (Neumaier): sum holds the rounded total and comp
 // the rounding errors lost by each addition, recovered exactly.
+// Neumaier's compensated sum of the finite terms; non-finite terms (an
+// infinite or NaN square) go to a plain sum of their own, so the result is
+// what the exact sum is under IEEE arithmetic: +inf if some term is +inf and
+// none is NaN, NaN if some term is NaN.  (Fed to the compensation, an
+// infinite term would turn into inf - inf = NaN.)
 struct CompensatedSum {
   double sum = 0.0;
   double comp = 0.0;
+  double special = 0.0;
   void add(double x) {
+    if (!std::isfinite(x)) {
+      special = special + x;
+      return;
+    }
     const double t = sum + x;
     if (std::fabs(sum) >= std::fabs(x)) {
       comp = comp + ((sum - t) + x);
@@ -194,7 +204,7 @@ struct CompensatedSum {
     }
     sum = t;
   }
-  double value() const { return sum + comp; }
+  double value() const { return special != 0.0 ? special : sum + comp; }  // NaN != 0 holds too
 };
 
 // Global L2 norm of the reduced gradient over flat elements [0, n); every

@@ -52,6 +52,27 @@ def test_norm_permutation_invariant_on_exact_sums(oracle_lib):
     assert a == b == math.sqrt(float(np.sum(vals.astype(np.float64) ** 2)))
 
 
+def test_norm_of_non_finite_gradients(oracle_lib):
+    # sqrt(sum g^2) under IEEE arithmetic: an infinite gradient makes the norm
+    # +inf, a NaN makes it NaN (NaN wins over inf); the largest finite bf16
+    # values square without overflow in fp64.
+    h = Hyper(n_ranks=1)
+    assert oracle_lib.grad_norm(h, [_bf([3.0, np.inf, 4.0])]) == math.inf
+    assert oracle_lib.grad_norm(h, [_bf([-np.inf, 1.0])]) == math.inf
+    assert math.isnan(oracle_lib.grad_norm(h, [_bf([3.0, np.nan, 4.0])]))
+    assert math.isnan(oracle_lib.grad_norm(h, [_bf([np.inf, np.nan])]))
+    top = np.array([0x7F7F], np.uint16)  # largest finite bf16, 3.3895e38
+    top_f = float((top.astype(np.uint32) << 16).view(np.float32)[0])
+    assert oracle_lib.grad_norm(h, [np.concatenate([top, top])]) == math.sqrt(2.0) * top_f
+    # replicas whose fp32 sum overflows: the reduced gradient itself is inf
+    h2 = Hyper(n_ranks=2)
+    assert oracle_lib.grad_norm(h2, [top, top]) == math.inf
+    # the coefficient: an infinite norm scales everything to 0, a NaN norm
+    # leaves the gradient unscaled (the reading taken for NaN)
+    assert oracle_lib.clip_coef(math.inf, 1.0) == 0.0
+    assert oracle_lib.clip_coef(math.nan, 1.0) == 1.0
+
+
 def test_clip_coefficient(oracle_lib):
     assert oracle_lib.clip_coef(5.0, 1.0) == f32(1.0 / (5.0 + 1e-6))
     assert oracle_lib.clip_coef(0.5, 1.0) == 1.0          # below the threshold: untouched
