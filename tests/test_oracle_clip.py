@@ -52,6 +52,16 @@ def test_norm_permutation_invariant_on_exact_sums(oracle_lib):
     assert a == b == math.sqrt(float(np.sum(vals.astype(np.float64) ** 2)))
 
 
+def test_norm_sum_is_compensated(oracle_lib):
+    # one square of 2^54 then a thousand squares of 1: a plain running fp64
+    # sum stays at 2^54 (its ulp there is 4), the exact sum 2^54 + 1000 is
+    # representable and is what the norm must be the square root of
+    h = Hyper(n_ranks=1)
+    g = _bf([2.0 ** 27] + [1.0] * 1000)
+    assert oracle_lib.grad_norm(h, [g]) == math.sqrt(float(2 ** 54 + 1000))
+    assert math.sqrt(float(2 ** 54 + 1000)) != 2.0 ** 27
+
+
 def test_norm_of_non_finite_gradients(oracle_lib):
     # sqrt(sum g^2) under IEEE arithmetic: an infinite gradient makes the norm
     # +inf, a NaN makes it NaN (NaN wins over inf); the largest finite bf16
