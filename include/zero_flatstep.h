@@ -433,6 +433,21 @@ zero_status zero_cpu_adam(const zero_config* cfg, int64_t t, const float* grad, 
  */
 zero_status zero_kernel_timeouts(const zero_ctx* ctx, uint32_t* count);
 
+/*
+ * zero_debug_inject — test hook for the bounded waits above (the pages have
+ * no counterpart).  what = ZERO_INJECT_MISSING_COPY arms it for the next
+ * zero_step: if that step's first launch uses the tile-staged kernel, the
+ * kernel announces the bytes of the launch's first tile to its mbarrier but
+ * issues no copy for it, so that one wait runs out after about a second;
+ * the CTA then counts a timeout (zero_kernel_timeouts), waits for the copies
+ * it did issue and leaves, and the elements of its tiles stay un-updated.
+ * Nothing faults: the device stays usable.  what = 0 disarms.  The hook is
+ * consumed by the next vector launch whichever kernel it uses.
+ * Errors: ZERO_EINVAL (NULL ctx, unknown value).
+ */
+#define ZERO_INJECT_MISSING_COPY 1
+zero_status zero_debug_inject(zero_ctx* ctx, int32_t what);
+
 /* Number of steps taken (t). */
 zero_status zero_step_count(const zero_ctx* ctx, int64_t* t);
 

@@ -1,15 +1,19 @@
-"""Host-side failure detection of the C ABI on a GPU machine: every bad call
-returns a status (never a fault) and leaves the context unchanged.  The
-failures are made on the host (bad pointers, wrong order of calls); no test
-here asks the GPU to fault, trap or hang."""
+"""Failure detection of the C ABI on a GPU machine: every bad call returns a
+status (never a fault) and leaves the context unchanged; the failures are
+made on the host (bad pointers, wrong order of calls).  The one device-side
+failure tested is a bounded wait that runs out because the test hook never
+issues the copy it waits for; no test here asks the GPU to fault, trap or
+hang."""
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 import synth_inputs as si
-from gpu_common import compare_state, ensure_built, make_problem, oracle_run, register, run_gpu, upload_grads
+from gpu_common import (check_guards, compare_state, ensure_built, make_problem, oracle_run, register, run_gpu,
+                        upload_grads)
 from gpu_common import gpu_flatstep
 from zero_sharded_mixed_flatparameter_gb300 import binding as B
 
@@ -112,5 +116,58 @@ def test_stage3_gather_argument_checks():
         fs.gather_weights(-1, full)
         torch.cuda.synchronize()
         assert torch.equal(full.view(torch.int16), fs.param16.view(torch.int16))
+    finally:
+        fs.close()
+
+
+def test_staged_wait_runs_out_and_the_device_stays_usable():
+    # The tile-staged step kernel bounds every wait for its bulk copies.  The
+    # test hook announces the launch's first tile to its mbarrier without
+    # issuing the copy, so CTA 0's wait runs out (after ~1 s): it counts a
+    # timeout, waits for the copies it did issue and leaves.  Exactly CTA 0's
+    # elements (its tiles and its part of the ragged tail) keep their old
+    # values; every other element is the oracle's; the next step on the same
+    # context runs normally.
+    import time
+    from gpu_common import to_np
+    n = 16
+    total = (1 << 23) + 2048 * 3 + 300          # padded to a multiple of 16 below
+    pb = make_problem(si.from_units([total]), n, 2, steps=2, seed=97)
+    padded = pb.lay.total_padded
+    fs = gpu_flatstep(pb, guard=64)
+    try:
+        before = B.zero_kernel_timeouts(fs.ctx)
+        init = tuple(to_np(x).copy() for x in (fs.master, fs.exp_avg, fs.exp_avg_sq, fs.param16))
+        flats = upload_grads(pb, 1)
+        fs.reduce_grads(-1, flats)
+        B.zero_debug_inject(fs.ctx, B.ZERO_INJECT_MISSING_COPY)
+        t0 = time.perf_counter()
+        fs.step()
+        torch.cuda.synchronize()
+        waited = time.perf_counter() - t0
+        assert B.zero_kernel_timeouts(fs.ctx) == before + 1
+        assert 0.5 < waited < 10.0, waited
+        # CTA 0's elements: tiles 0, G, 2G, ... (one CTA per SM at N = 16) and
+        # the first 256 elements after the last full tile
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        tile, full = 2048, padded // 2048
+        mine = np.zeros(padded, bool)
+        for tid in range(0, full, sms):
+            mine[tid * tile:(tid + 1) * tile] = True
+        mine[full * tile:min(full * tile + 256, padded)] = True
+        ref = oracle_run(pb, steps=1)
+        got = tuple(to_np(x) for x in (fs.master, fs.exp_avg, fs.exp_avg_sq, fs.param16))
+        for name, g, r, i0 in zip(("master", "m", "v", "param16"), got, ref, init):
+            assert np.array_equal(g[mine], i0[mine]), f"{name}: CTA 0's elements changed"
+            assert np.array_equal(g[~mine], r[~mine]), f"{name}: other elements differ from the oracle"
+        check_guards(fs, "after the injected timeout")
+        fs.post_step()
+        # the same context steps normally afterwards (no timeout, valid results
+        # for every element that the first step did update)
+        fs.reduce_grads(-1, upload_grads(pb, 2))
+        fs.step()
+        torch.cuda.synchronize()
+        assert B.zero_kernel_timeouts(fs.ctx) == before + 1
+        assert not np.isnan(to_np(fs.master)).any()
     finally:
         fs.close()

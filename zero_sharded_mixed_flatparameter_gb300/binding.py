@@ -30,8 +30,10 @@ EXPORTED = (
     "zero_grad_norm", "zero_clip_grad_norm_static", "zero_accumulate_grads", "zero_export_state",
     "zero_import_state", "zero_clip_workspace_bytes_ex", "zero_clip_grad_norm_ex", "zero_kernel_timeouts",
     "zero_make_master_offload", "zero_offload_workspace_bytes", "zero_offload_step", "zero_cpu_adam",
+    "zero_debug_inject",
 )
 ZERO_CLIP_KEEP_REDUCED = 1
+ZERO_INJECT_MISSING_COPY = 1
 
 
 class zero_config(ctypes.Structure):
@@ -99,6 +101,7 @@ def load(path: str = LIB_PATH):
             "zero_offload_workspace_bytes": [vp, i64, P(i64), P(i64)],
             "zero_offload_step": [vp, i64, vp, i64, vp, i64, i32, vp, vp],
             "zero_cpu_adam": [P(zero_config), i64, vp, vp, vp, vp, vp, i64, i32],
+            "zero_debug_inject": [vp, i32],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -267,6 +270,10 @@ def zero_kernel_timeouts(ctx: int | None = None) -> int:
     n = ctypes.c_uint32()
     _check(load().zero_kernel_timeouts(ctx, ctypes.byref(n)), ctx)
     return n.value
+
+
+def zero_debug_inject(ctx: int, what: int) -> None:
+    _check(load().zero_debug_inject(ctx, what), ctx)
 
 
 def zero_step_count(ctx: int) -> int:

@@ -54,6 +54,8 @@ struct StepArgs {
   long long total_vec;   // vectors over all segments (vector kernel)
   long long total_elems; // elements over all segments (scalar kernel)
   const float* clip;     // device clip coefficient, or nullptr (no clipping)
+  int inject_missing_copy; // test hook: the tile-staged kernel announces the
+                           // launch's first tile but issues none of its copies
   Seg seg[kMaxSegs];
 };
 

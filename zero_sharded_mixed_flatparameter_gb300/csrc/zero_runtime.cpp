@@ -69,6 +69,9 @@ struct zero_ctx {
   bool offload = false;
   zfs_host::Pool* pool = nullptr;
 
+  // Test hook armed by zero_debug_inject for the next step's first launch.
+  int32_t inject = 0;
+
   std::string error;
 
   ~zero_ctx() { zfs_host::pool_destroy(pool); }
@@ -289,6 +292,10 @@ zero_status launch_batches(zero_ctx* ctx, const std::vector<PlannedSeg>& segs, b
     a.p16 = static_cast<uint16_t*>(ctx->bufs.param16);
     a.clip = ctx->clip_ws ? reinterpret_cast<const float*>(ctx->clip_ws + 8) : nullptr;
     fill_scalars(ctx, t, &a);
+    if (ctx->inject == ZERO_INJECT_MISSING_COPY && vec) {
+      a.inject_missing_copy = 1;
+      ctx->inject = 0;
+    }
     long long vecs = 0, elems = 0;
     int n = 0;
     for (; i < segs.size() && n < zfs::kMaxSegs; ++i, ++n) {
@@ -1162,6 +1169,13 @@ zero_status zero_import_state(zero_ctx* ctx, const float* master_in, const float
     in += n;
   }
   ctx->t = t;
+  return ZERO_OK;
+}
+
+zero_status zero_debug_inject(zero_ctx* ctx, int32_t what) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  if (what != 0 && what != ZERO_INJECT_MISSING_COPY) return fail(ctx, ZERO_EINVAL, "unknown injection %d", what);
+  ctx->inject = what;
   return ZERO_OK;
 }
 

@@ -169,13 +169,26 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
 // bf16: 2363 / 3152 GB/s at 1 M elements, 5481 / 5479 at 6 M, 6179 / 5962
 // at 12 M).
 // The arithmetic and its order are those of step_vec8, so the results are
-// bit-identical.  Every wait is bounded: a CTA that gives up (which needs a
-// copy that never lands) counts it in g_step_timeouts and
-// leaves; the host can read the counter with zero_kernel_timeouts.
+// bit-identical.  Every wait is bounded in time (kTmaWaitNs): a CTA that gives
+// up (which needs a copy that never lands) counts it in g_step_timeouts,
+// waits (bounded) for the copies it issued and leaves, with the rest of its
+// tiles not updated; the host reads the counter with zero_kernel_timeouts.
+// The test hook inject_missing_copy makes exactly this happen to the launch's
+// first tile (its bytes are announced to the mbarrier, no copy is issued).
 // ---------------------------------------------------------------------------
 __device__ unsigned int g_step_timeouts = 0;
 
-constexpr long long kTmaWaitLimit = 1LL << 22;  // try_wait attempts before giving up
+// Wait limits (device global timer, ns): a tile's copies land within
+// microseconds; a second means they never will.  Draining after a give-up
+// waits at most kTmaDrainNs per outstanding tile.
+constexpr unsigned long long kTmaWaitNs = 1000000000ull;
+constexpr unsigned long long kTmaDrainNs = 50000000ull;
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -243,6 +256,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
     unsigned char* st = smem + static_cast<size_t>(stage) * L::kStageBytes;
     const long long e0 = ti * kTmaTile;
     mbar_expect_tx(&bars[stage], L::kStageBytes);
+    if (a.inject_missing_copy && id == 0) return;  // test hook: this tile's wait must run out
     for (int r = 0; r < N; ++r)
       bulk_load(st + r * L::kGradBytes, static_cast<const char*>(sg.g[r]) + e0 * (kFp32 ? 4 : 2), L::kGradBytes,
                 &bars[stage]);
@@ -263,12 +277,14 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
     if (id >= n_tiles) break;
     const int stage = static_cast<int>(k % kTmaStages);
     const uint32_t parity = static_cast<uint32_t>((k / kTmaStages) & 1);
-    long long tries = 0;
     bool mine = false;
-    while (!mbar_try_wait(&bars[stage], parity)) {
-      if (++tries > kTmaWaitLimit) {
-        mine = true;
-        break;
+    if (!mbar_try_wait(&bars[stage], parity)) {
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try_wait(&bars[stage], parity)) {
+        if (global_ns() - t0 > kTmaWaitNs) {
+          mine = true;
+          break;
+        }
       }
     }
     // Every thread reaches this barrier; the CTA gives up together or not at all.
@@ -376,8 +392,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
       if (blockIdx.x + j * gridDim.x >= n_tiles) break;
       const int s = static_cast<int>(j % kTmaStages);
       const uint32_t parity = static_cast<uint32_t>((j / kTmaStages) & 1);
-      long long tries = 0;
-      while (!mbar_try_wait(&bars[s], parity) && ++tries < (1LL << 20)) {
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try_wait(&bars[s], parity) && global_ns() - t0 < kTmaDrainNs) {
       }
     }
     return;
