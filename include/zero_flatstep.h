@@ -446,7 +446,26 @@ zero_status zero_kernel_timeouts(const zero_ctx* ctx, uint32_t* count);
  * Errors: ZERO_EINVAL (NULL ctx, unknown value).
  */
 #define ZERO_INJECT_MISSING_COPY 1
+/*
+ * what = ZERO_INJECT_SHORT_BOUNDS: the next zero_step tells its kernels that
+ * the state arrays end 8 elements before they really do (the buffers keep
+ * their full size, so no access can leave them).  In a debug build the index
+ * checks then refuse the last 8 elements (counted, not updated); in a release
+ * build the checks do not exist and the step is the normal one.
+ */
+#define ZERO_INJECT_SHORT_BOUNDS 2
 zero_status zero_debug_inject(zero_ctx* ctx, int32_t what);
+
+/*
+ * zero_debug_check_failures — in a debug build of the library (compiled with
+ * -DZFS_DEBUG_CHECKS: every kernel index is checked before the access it
+ * guards; a failed check is counted and the access skipped, never trapped),
+ * the number of failed checks on the current device since the library was
+ * loaded.  Synchronizes with the device.  The pages have no counterpart.
+ * Errors: ZERO_EINVAL (NULL); ZERO_ENOTSUP in a release build (*count = 0);
+ * ZERO_ECUDA.
+ */
+zero_status zero_debug_check_failures(uint32_t* count);
 
 /* Number of steps taken (t). */
 zero_status zero_step_count(const zero_ctx* ctx, int64_t* t);

@@ -30,10 +30,11 @@ EXPORTED = (
     "zero_grad_norm", "zero_clip_grad_norm_static", "zero_accumulate_grads", "zero_export_state",
     "zero_import_state", "zero_clip_workspace_bytes_ex", "zero_clip_grad_norm_ex", "zero_kernel_timeouts",
     "zero_make_master_offload", "zero_offload_workspace_bytes", "zero_offload_step", "zero_cpu_adam",
-    "zero_debug_inject",
+    "zero_debug_inject", "zero_debug_check_failures",
 )
 ZERO_CLIP_KEEP_REDUCED = 1
 ZERO_INJECT_MISSING_COPY = 1
+ZERO_INJECT_SHORT_BOUNDS = 2
 
 
 class zero_config(ctypes.Structure):
@@ -102,6 +103,7 @@ def load(path: str = LIB_PATH):
             "zero_offload_step": [vp, i64, vp, i64, vp, i64, i32, vp, vp],
             "zero_cpu_adam": [P(zero_config), i64, vp, vp, vp, vp, vp, i64, i32],
             "zero_debug_inject": [vp, i32],
+            "zero_debug_check_failures": [P(ctypes.c_uint32)],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -274,6 +276,13 @@ def zero_kernel_timeouts(ctx: int | None = None) -> int:
 
 def zero_debug_inject(ctx: int, what: int) -> None:
     _check(load().zero_debug_inject(ctx, what), ctx)
+
+
+def zero_debug_check_failures() -> int:
+    """Failed index checks of a debug build (raises ZERO_ENOTSUP on a release build)."""
+    n = ctypes.c_uint32()
+    _check(load().zero_debug_check_failures(ctypes.byref(n)))
+    return n.value
 
 
 def zero_step_count(ctx: int) -> int:

@@ -22,6 +22,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libzero_flatstep.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
+# The same sources with every kernel index checked (-DZFS_DEBUG_CHECKS): a
+# failed check is counted (zero_debug_check_failures) and its access skipped.
+DEBUG_LIB_PATH = os.path.join(PKG, "libzero_flatstep_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "--fmad=false", "-Xcompiler", "-fPIC,-O2",
@@ -53,25 +56,31 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug_checks: bool = False) -> str:
+    """Build the library (or, with debug_checks, its index-checking variant)."""
+    out_path = DEBUG_LIB_PATH if debug_checks else LIB_PATH
+    build_dir = os.path.join(BUILD, "debug") if debug_checks else BUILD
+    if debug_checks:
+        extra_flags = (*extra_flags, "-DZFS_DEBUG_CHECKS")
+    if not force and up_to_date(out_path):
+        return out_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
 
     cxx = _cxx()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         if src in HOST_SOURCES:
-            cmd = [cxx, *HOST_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+            cmd = [cxx, *HOST_FLAGS, *[f for f in extra_flags if f.startswith("-D")], "-c",
+                   os.path.join(CSRC, src), "-o", obj]
         else:
             cmd = [nvcc, *ARCH, *COMMON, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
@@ -85,13 +94,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES) + len(HOST_SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES + HOST_SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = out_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, out_path)
+    return out_path
 
 
 if __name__ == "__main__":

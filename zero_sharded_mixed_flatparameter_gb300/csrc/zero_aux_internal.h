@@ -83,6 +83,7 @@ struct ReduceSeg {
 
 struct ReduceArgs {
   float* out;
+  long long out_len;  // elements of out (debug bounds checks)
   const float* clip;  // device clip coefficient, or nullptr
   float inv_n;
   int n_ranks;
@@ -92,6 +93,10 @@ struct ReduceArgs {
   ReduceSeg seg[kMaxSegs];
 };
 cudaError_t launch_reduce_out(const ReduceArgs& a, cudaStream_t stream);
+
+// Failed index checks of a debug build in zero_aux_kernels.cu (0xFFFFFFFF if
+// the counter cannot be read; always 0 in a release build).
+unsigned int aux_debug_failures();
 
 // ZeRO-3 unit gather: copy n bf16 elements; *launches counts the kernels enqueued.
 cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaStream_t stream, int* launches);

@@ -173,7 +173,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) grad_sq_kernel(const __grid_c
   const long long k = b - s.chunk_start;
   const long long c0 = k * kClipChunk;
   const long long c1 = (k == s.n_chunks - 1) ? s.len : c0 + kClipChunk;
-  const long long len = c1 - c0;
+  // (CTA-uniform: a failed check empties the chunk, the block sum still runs)
+  const long long len = ZFS_CHECK(k >= 0 && k < s.n_chunks && c1 <= s.len) ? c1 - c0 : 0;
   SqAcc acc;
   long long grp = threadIdx.x;
   for (; s.vec_ok && (grp + kStepThreads) * kVec + kVec <= len; grp += 2 * kStepThreads) {
@@ -387,6 +388,9 @@ __global__ void __launch_bounds__(kStepThreads) reduce_out_kernel(const __grid_c
     const ReduceSeg& sg = a.seg[s];
     const long long k = (q - sg.group_start) * kVec;
     float* out = a.out + sg.out_off + k;
+    if (!ZFS_CHECK(k >= 0 && k < sg.len && sg.out_off + (k + kVec < sg.len ? k + kVec : sg.len) <= a.out_len)) {
+      continue;
+    }
     if (sg.vec_ok && k + kVec <= sg.len) {
       float acc[kVec];
       for (int r = 0; r < a.n_ranks; ++r) {
@@ -416,6 +420,16 @@ __global__ void __launch_bounds__(kStepThreads) reduce_out_kernel(const __grid_c
 }
 
 }  // namespace
+
+unsigned int aux_debug_failures() {
+#ifdef ZFS_DEBUG_CHECKS
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_debug_failures, sizeof v) != cudaSuccess) return 0xFFFFFFFFu;
+  return v;
+#else
+  return 0;
+#endif
+}
 
 cudaError_t launch_reduce_out(const ReduceArgs& a, cudaStream_t stream) {
   if (a.total_groups <= 0 || a.nseg <= 0) return cudaSuccess;

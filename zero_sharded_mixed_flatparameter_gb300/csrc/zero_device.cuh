@@ -10,6 +10,21 @@
 
 namespace zfs {
 
+// Debug builds (-DZFS_DEBUG_CHECKS) check every index before the access it
+// guards: a failed check counts in this file's counter and the access is
+// skipped (no trap, no out-of-range access).  Release builds compile the
+// checks away.
+#ifdef ZFS_DEBUG_CHECKS
+static __device__ unsigned int g_debug_failures = 0;
+__device__ __forceinline__ bool debug_check(bool ok) {
+  if (!ok) atomicAdd(&g_debug_failures, 1u);
+  return ok;
+}
+#define ZFS_CHECK(cond) (::zfs::debug_check(static_cast<bool>(cond)))
+#else
+#define ZFS_CHECK(cond) true
+#endif
+
 __device__ __forceinline__ float bf16_lo(uint32_t word) { return __uint_as_float(word << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t word) { return __uint_as_float(word & 0xFFFF0000u); }
 

@@ -54,6 +54,7 @@ struct StepArgs {
   long long total_vec;   // vectors over all segments (vector kernel)
   long long total_elems; // elements over all segments (scalar kernel)
   const float* clip;     // device clip coefficient, or nullptr (no clipping)
+  long long total_padded;  // elements of master / m / v / p16 (debug bounds checks)
   int inject_missing_copy; // test hook: the tile-staged kernel announces the
                            // launch's first tile but issues none of its copies
   Seg seg[kMaxSegs];
@@ -72,6 +73,9 @@ int sm_count();
 // Bounded waits of the tile-staged step kernel that gave up on the current
 // device since the library was loaded (0xFFFFFFFF if it cannot be read).
 unsigned int step_timeouts();
+// Failed index checks of a debug build in zero_step_kernels.cu (0xFFFFFFFF
+// if the counter cannot be read; always 0 in a release build).
+unsigned int step_debug_failures();
 
 // CTAs for a grid-stride launch of kStepThreads-thread CTAs over work_items
 // items: enough to cover them, at most blocks_per_sm per SM.

@@ -292,10 +292,12 @@ zero_status launch_batches(zero_ctx* ctx, const std::vector<PlannedSeg>& segs, b
     a.p16 = static_cast<uint16_t*>(ctx->bufs.param16);
     a.clip = ctx->clip_ws ? reinterpret_cast<const float*>(ctx->clip_ws + 8) : nullptr;
     fill_scalars(ctx, t, &a);
+    a.total_padded = ctx->padded_total;
     if (ctx->inject == ZERO_INJECT_MISSING_COPY && vec) {
       a.inject_missing_copy = 1;
       ctx->inject = 0;
     }
+    if (ctx->inject == ZERO_INJECT_SHORT_BOUNDS) a.total_padded = ctx->padded_total - zfs::kVec;
     long long vecs = 0, elems = 0;
     int n = 0;
     for (; i < segs.size() && n < zfs::kMaxSegs; ++i, ++n) {
@@ -652,6 +654,7 @@ zero_status zero_step(zero_ctx* ctx, void* stream) {
       a.p16 = static_cast<uint16_t*>(ctx->bufs.param16);
       a.clip = reinterpret_cast<const float*>(ctx->clip_ws + 8);
       fill_scalars(ctx, t, &a);
+      a.total_padded = ctx->padded_total - (ctx->inject == ZERO_INJECT_SHORT_BOUNDS ? zfs::kVec : 0);
       a.inv_n = 1.0f;
       a.n_ranks = 1;
       a.grad_fp32 = 1;
@@ -680,6 +683,7 @@ zero_status zero_step(zero_ctx* ctx, void* stream) {
     st = launch_batches(ctx, scalar_segs, false, t, s, &launches);
     if (st != ZERO_OK) return st;
   }
+  if (ctx->inject == ZERO_INJECT_SHORT_BOUNDS) ctx->inject = 0;
   ctx->last_launches = launches;
   ctx->t = t;
   ctx->phase = Phase::kStepped;
@@ -737,6 +741,7 @@ cudaError_t enqueue_chunk_reduce(const zero_ctx* ctx, const std::vector<PlannedS
   zfs::ReduceArgs a;
   std::memset(&a, 0, sizeof a);
   a.out = out;
+  a.out_len = c1 - c0;
   a.clip = clip;
   a.inv_n = 1.0f / static_cast<float>(N);
   a.n_ranks = N;
@@ -1172,9 +1177,23 @@ zero_status zero_import_state(zero_ctx* ctx, const float* master_in, const float
   return ZERO_OK;
 }
 
+zero_status zero_debug_check_failures(uint32_t* count) {
+  if (!count) return fail(nullptr, ZERO_EINVAL, "count is NULL");
+#ifdef ZFS_DEBUG_CHECKS
+  const unsigned int a = zfs::step_debug_failures(), b = zfs::aux_debug_failures();
+  if (a == 0xFFFFFFFFu || b == 0xFFFFFFFFu) return fail(nullptr, ZERO_ECUDA, "cannot read the check counters");
+  *count = a + b;
+  return ZERO_OK;
+#else
+  *count = 0;
+  return fail(nullptr, ZERO_ENOTSUP, "library built without ZFS_DEBUG_CHECKS");
+#endif
+}
+
 zero_status zero_debug_inject(zero_ctx* ctx, int32_t what) {
   if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
-  if (what != 0 && what != ZERO_INJECT_MISSING_COPY) return fail(ctx, ZERO_EINVAL, "unknown injection %d", what);
+  if (what != 0 && what != ZERO_INJECT_MISSING_COPY && what != ZERO_INJECT_SHORT_BOUNDS)
+    return fail(ctx, ZERO_EINVAL, "unknown injection %d", what);
   ctx->inject = what;
   return ZERO_OK;
 }

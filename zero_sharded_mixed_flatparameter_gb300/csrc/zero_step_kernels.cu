@@ -53,6 +53,7 @@ __device__ __forceinline__ float reduce_scalar(const StepArgs& a, const Seg& s, 
 
 __device__ __forceinline__ void step_scalar_element(const StepArgs& a, const Seg& s, long long k, float clip) {
   const long long j = s.base + k;
+  if (!ZFS_CHECK(k >= 0 && k < s.len && j < a.total_padded)) return;
   const float g = __fmul_rn(reduce_scalar(a, s, k), clip);
   float w = a.master[j], m = a.m[j], v = a.v[j];
   adam(a, g, w, m, v);
@@ -68,6 +69,7 @@ __device__ __forceinline__ void step_scalar_element(const StepArgs& a, const Seg
 template <int N, bool kFp32>
 __device__ __forceinline__ void step_vec8(const StepArgs& a, const Seg& s, long long vi, float clip) {
   const long long j = s.base + vi * kVec;
+  if (!ZFS_CHECK(vi >= 0 && (vi + 1) * kVec <= s.len && j + kVec <= a.total_padded)) return;
   float g[kVec];
   if constexpr (!kFp32) {
     uint4 raw[N];
@@ -255,6 +257,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
     const Seg& sg = a.seg[si];
     unsigned char* st = smem + static_cast<size_t>(stage) * L::kStageBytes;
     const long long e0 = ti * kTmaTile;
+    if (!ZFS_CHECK(ti >= 0 && e0 + kTmaTile <= sg.len && sg.base + e0 + kTmaTile <= a.total_padded)) {
+      // complete the stage's phase without bytes: its stores are skipped below
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[stage])) : "memory");
+      return;
+    }
     mbar_expect_tx(&bars[stage], L::kStageBytes);
     if (a.inject_missing_copy && id == 0) return;  // test hook: this tile's wait must run out
     for (int r = 0; r < N; ++r)
@@ -356,6 +363,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
     locate_tile(a, id, &si, &ti);
     const long long j_lo = a.seg[si].base + ti * kTmaTile + e_lo;
     const long long j_hi = a.seg[si].base + ti * kTmaTile + e_hi;
+    if (!ZFS_CHECK((ti + 1) * kTmaTile <= a.seg[si].len && a.seg[si].base + (ti + 1) * kTmaTile <= a.total_padded)) {
+      continue;
+    }
     if constexpr (kFp32) {
       st_stream_f4(a.master + j_lo, make_float4(w[0], w[1], w[2], w[3]));
       st_stream_f4(a.master + j_hi, make_float4(w[4], w[5], w[6], w[7]));
@@ -508,6 +518,16 @@ long long grid_for(long long work_items, int sms, int blocks_per_sm) {
 
 
 int sm_count() { return cached_sms(current_device()); }
+
+unsigned int step_debug_failures() {
+#ifdef ZFS_DEBUG_CHECKS
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_debug_failures, sizeof v) != cudaSuccess) return 0xFFFFFFFFu;
+  return v;
+#else
+  return 0;
+#endif
+}
 
 unsigned int step_timeouts() {
   unsigned int v = 0;
