@@ -185,6 +185,7 @@ __device__ unsigned int g_step_timeouts = 0;
 // waits at most kTmaDrainNs per outstanding tile.
 constexpr unsigned long long kTmaWaitNs = 1000000000ull;
 constexpr unsigned long long kTmaDrainNs = 50000000ull;
+constexpr int kTmaFastSpins = 64;  // try_wait attempts before the timed wait starts
 
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
@@ -210,6 +211,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// The rest of a tile's wait after a first try_wait failed: a short spin
+// (tiles usually land within a few tries), then tries until kTmaWaitNs have
+// passed.  False: the copies never landed.  Out of line so that the rarely
+// long wait does not weigh on the register allocation of the tile loop.
+__device__ __noinline__ bool wait_tile(uint64_t* bar, uint32_t parity) {
+  for (int i = 0; i < kTmaFastSpins; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kTmaWaitNs) return false;
+  }
+  return true;
+}
+
 // Global -> this CTA's shared memory; completes `bytes` on the mbarrier.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -284,16 +300,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
     if (id >= n_tiles) break;
     const int stage = static_cast<int>(k % kTmaStages);
     const uint32_t parity = static_cast<uint32_t>((k / kTmaStages) & 1);
-    bool mine = false;
-    if (!mbar_try_wait(&bars[stage], parity)) {
-      const unsigned long long t0 = global_ns();
-      while (!mbar_try_wait(&bars[stage], parity)) {
-        if (global_ns() - t0 > kTmaWaitNs) {
-          mine = true;
-          break;
-        }
-      }
-    }
+    const bool mine = !mbar_try_wait(&bars[stage], parity) && !wait_tile(&bars[stage], parity);
     // Every thread reaches this barrier; the CTA gives up together or not at all.
     if (__syncthreads_or(mine ? 1 : 0)) {
       gave_up_at = k;
