@@ -407,6 +407,20 @@ def run_ours(args):
             torch.cuda.synchronize(device)
     torch.cuda.synchronize(device)
 
+    # --graph: the step (registration, clip, step, gathers, post_step) is
+    # captured once into a CUDA graph in the library's capturable mode and
+    # the timed region replays it; one eager capturable step first caches
+    # the launch shapes.
+    graph, graph_launches = None, 0
+    if args.graph:
+        fs.enable_capturable(max_steps=warm_done + args.steps + 2)
+        graph_launches = one_step()
+        torch.cuda.synchronize(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one_step()
+        torch.cuda.synchronize(device)
+
     # ---- device-resident timed region ----
     pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clip_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -423,7 +437,13 @@ def run_ours(args):
         t_region0 = time.time()
         start.record(stream)
         for k in range(args.steps):
-            launches += one_step(pairs[k], clip_pairs[k], accum_pairs[k], gather_pairs[k])
+            if graph is not None:
+                pairs[k][0].record(stream)
+                graph.replay()
+                pairs[k][1].record(stream)
+                launches += graph_launches
+            else:
+                launches += one_step(pairs[k], clip_pairs[k], accum_pairs[k], gather_pairs[k])
         end.record(stream)
         torch.cuda.synchronize(device)
         t_region1 = time.time()
@@ -431,9 +451,12 @@ def run_ours(args):
         clocks.mark(t_region0, t_region1)
     total_ms = start.elapsed_time(end)
     step_kernel_ms = [a.elapsed_time(b) for a, b in pairs]
-    clip_ms = [a.elapsed_time(b) for a, b in clip_pairs] if args.clip > 0 else None
-    accum_ms = [a.elapsed_time(b) for a, b in accum_pairs] if args.accum > 0 else None
-    gather_ms = [a.elapsed_time(b) for a, b in gather_pairs] if gather_bufs else None
+    clip_ms = [a.elapsed_time(b) for a, b in clip_pairs] if args.clip > 0 and graph is None else None
+    accum_ms = [a.elapsed_time(b) for a, b in accum_pairs] if args.accum > 0 and graph is None else None
+    gather_ms = [a.elapsed_time(b) for a, b in gather_pairs] if gather_bufs and graph is None else None
+    if graph is not None:
+        fs.disable_capturable()  # the end-to-end leg below runs eagerly
+        del graph
     clock = clocks.summary()
 
     total_ms_max, kern_ms_max = aggregate([total_ms, statistics.mean(step_kernel_ms)], "max", world, device)
@@ -520,7 +543,8 @@ def run_ours(args):
                 "frac": achieved_gbs / peak, "peak_source": f"hbm_gbs {peak_kind}",
                 "traffic": traffic, "algorithmic_bytes_per_launch": bytes_per_launch,
                 "bytes_per_param": bpp, "kernel": step_kernel_name(n, wl["grad_dtype"], args.clip_keep, padded),
-                "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms)}
+                "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms),
+                "timed": "whole replayed step (CUDA graph)" if args.graph else "step kernel launch"}
     offload = None
     if args.offload:
         # The offloaded step is bound by host memory: the host Adam moves
@@ -550,7 +574,8 @@ def run_ours(args):
                        "units": fs.n_units, "n_ranks_simulated": n, "zero_stage": wl["stage"],
                        "grad_dtype": wl["grad_dtype"], "optimizer": "Adam fp32 (lr 1e-3, betas 0.9/0.999, eps 1e-8)",
                        "parallelism": f"{world} GPU replica(s); N={n} DP ranks simulated per GPU",
-                       "l2": f"inputs larger than L2: {bytes_per_launch / 1e9:.2f} GB moved per step (L2 129 MB)"},
+                       "l2": f"inputs larger than L2: {bytes_per_launch / 1e9:.2f} GB moved per step (L2 129 MB)",
+                       "cuda_graph": bool(args.graph)},
             "hbm_gbs": None if args.offload else achieved_gbs,
             "hbm_frac_of_peak": None if args.offload else achieved_gbs / peak,
             "roofline": roofline,
@@ -700,6 +725,8 @@ def main():
     ap.add_argument("--workload", default="llama1024_zero2_n8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step into a CUDA graph (capturable mode) and time its replays")
     ap.add_argument("--offload", action="store_true",
                     help="ZeRO-Offload: fp32 state in host memory, the step through zero_offload_step")
     ap.add_argument("--offload-chunk", type=int, default=1 << 23)
@@ -717,6 +744,8 @@ def main():
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 50 if args.offload else 2000
+    if args.graph and args.offload:
+        ap.error("--graph and --offload exclude each other (the offload step runs on host threads)")
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
     if args.sweep:

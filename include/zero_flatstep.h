@@ -345,6 +345,45 @@ zero_status zero_export_state(zero_ctx* ctx, float* master_out, float* exp_avg_o
 zero_status zero_import_state(zero_ctx* ctx, const float* master_in, const float* exp_avg_in,
                               const float* exp_avg_sq_in, int64_t t, void* stream);
 
+/* ---- Capturable steps (CUDA graphs) --------------------------------------
+ * The pages have no counterpart: this is the library's way of letting a
+ * whole step (registration, clip, step, post_step, gathers) be captured once
+ * into a CUDA graph and replayed every iteration without host work.  A
+ * replayed launch repeats its arguments, so what changes from step to step
+ * (the bias corrections 1 - beta^t) must come from device memory: in
+ * capturable mode the step count lives on the device and the kernels look up
+ * bc1, bc2 of step t in a table the host computed once (the same fp32 values
+ * zero_step would pass, so results are bit-identical).  Each zero_step (and
+ * each replay of a captured one) reads the count, updates, and then advances
+ * the count with one extra one-thread launch.  Replays also repeat the
+ * gradient pointers, the clip workspace and the learning rate captured.
+ */
+
+/* Bytes of the capturable workspace for up to max_steps steps in total
+ * (16 + 8 * max_steps).  Errors: ZERO_EINVAL. */
+zero_status zero_capturable_workspace_bytes(const zero_ctx* ctx, int64_t max_steps, int64_t* bytes);
+
+/*
+ * zero_enable_capturable — turn the mode on: workspace = device memory of the
+ * context's device (16-byte aligned, caller-owned, kept until
+ * zero_disable_capturable), holding the step count (set to the steps taken
+ * so far) and the bias corrections of steps 1..max_steps.  Synchronizes
+ * `stream`.  A step whose count would pass max_steps is skipped by the
+ * kernels (nothing changes; zero_step_count then reports ZERO_ESTATE).
+ * Errors: ZERO_EINVAL (workspace, max_steps <= steps taken); ZERO_ESTATE (a
+ * step awaits post_step); ZERO_ENOTSUP (offload context); ZERO_ENOMEM;
+ * ZERO_ECUDA.  Export and import are refused while the mode is on.
+ */
+zero_status zero_enable_capturable(zero_ctx* ctx, void* workspace, int64_t workspace_bytes, int64_t max_steps,
+                                   void* stream);
+
+/*
+ * zero_disable_capturable — turn the mode off: the context's step count
+ * becomes the device count (capped at max_steps: later steps were skipped).
+ * Synchronizes `stream`.  Errors: ZERO_ESTATE (mode not on); ZERO_ECUDA.
+ */
+zero_status zero_disable_capturable(zero_ctx* ctx, void* stream);
+
 /* ---- ZeRO-Offload -------------------------------------------------------
  * CMU 15-779 Lecture 13 notes §7.1-7.2 (ZeRO-Offload's partition and its
  * timeline): only the 16-bit parameters stay on the GPU; the fp32 master,
@@ -467,7 +506,8 @@ zero_status zero_debug_inject(zero_ctx* ctx, int32_t what);
  */
 zero_status zero_debug_check_failures(uint32_t* count);
 
-/* Number of steps taken (t). */
+/* Number of steps taken (t).  In capturable mode it is read from the device
+ * (synchronizing), and ZERO_ESTATE reports steps skipped past max_steps. */
 zero_status zero_step_count(const zero_ctx* ctx, int64_t* t);
 
 /*

@@ -30,7 +30,8 @@ EXPORTED = (
     "zero_grad_norm", "zero_clip_grad_norm_static", "zero_accumulate_grads", "zero_export_state",
     "zero_import_state", "zero_clip_workspace_bytes_ex", "zero_clip_grad_norm_ex", "zero_kernel_timeouts",
     "zero_make_master_offload", "zero_offload_workspace_bytes", "zero_offload_step", "zero_cpu_adam",
-    "zero_debug_inject", "zero_debug_check_failures",
+    "zero_debug_inject", "zero_debug_check_failures", "zero_capturable_workspace_bytes", "zero_enable_capturable",
+    "zero_disable_capturable",
 )
 ZERO_CLIP_KEEP_REDUCED = 1
 ZERO_INJECT_MISSING_COPY = 1
@@ -104,6 +105,9 @@ def load(path: str = LIB_PATH):
             "zero_cpu_adam": [P(zero_config), i64, vp, vp, vp, vp, vp, i64, i32],
             "zero_debug_inject": [vp, i32],
             "zero_debug_check_failures": [P(ctypes.c_uint32)],
+            "zero_capturable_workspace_bytes": [vp, i64, P(i64)],
+            "zero_enable_capturable": [vp, vp, i64, i64, vp],
+            "zero_disable_capturable": [vp, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -283,6 +287,20 @@ def zero_debug_check_failures() -> int:
     n = ctypes.c_uint32()
     _check(load().zero_debug_check_failures(ctypes.byref(n)))
     return n.value
+
+
+def zero_capturable_workspace_bytes(ctx: int, max_steps: int) -> int:
+    n = ctypes.c_int64()
+    _check(load().zero_capturable_workspace_bytes(ctx, max_steps, ctypes.byref(n)), ctx)
+    return n.value
+
+
+def zero_enable_capturable(ctx: int, workspace: int, workspace_bytes: int, max_steps: int, stream: int = 0) -> None:
+    _check(load().zero_enable_capturable(ctx, workspace, workspace_bytes, max_steps, stream or None), ctx)
+
+
+def zero_disable_capturable(ctx: int, stream: int = 0) -> None:
+    _check(load().zero_disable_capturable(ctx, stream or None), ctx)
 
 
 def zero_step_count(ctx: int) -> int:

@@ -55,6 +55,12 @@ struct StepArgs {
   long long total_elems; // elements over all segments (scalar kernel)
   const float* clip;     // device clip coefficient, or nullptr (no clipping)
   long long total_padded;  // elements of master / m / v / p16 (debug bounds checks)
+  // Capturable steps (dev_t != nullptr): the step count before this step is
+  // *dev_t, and bc1 / bc2 of step t are dev_bias[2(t-1)], dev_bias[2(t-1)+1]
+  // for t <= dev_steps (instead of the bc1 / bc2 above).
+  const long long* dev_t;
+  const float* dev_bias;
+  long long dev_steps;
   int inject_missing_copy; // test hook: the tile-staged kernel announces the
                            // launch's first tile but issues none of its copies
   Seg seg[kMaxSegs];
@@ -73,6 +79,8 @@ int sm_count();
 // Bounded waits of the tile-staged step kernel that gave up on the current
 // device since the library was loaded (0xFFFFFFFF if it cannot be read).
 unsigned int step_timeouts();
+// Capturable steps: *t += 1 on the stream (one thread).
+cudaError_t launch_count_step(long long* t, cudaStream_t stream);
 // Failed index checks of a debug build in zero_step_kernels.cu (0xFFFFFFFF
 // if the counter cannot be read; always 0 in a release build).
 unsigned int step_debug_failures();

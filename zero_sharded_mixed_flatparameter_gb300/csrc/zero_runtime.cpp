@@ -72,6 +72,12 @@ struct zero_ctx {
   // Test hook armed by zero_debug_inject for the next step's first launch.
   int32_t inject = 0;
 
+  // Capturable mode: the device step count and the table of bias
+  // corrections in the caller's workspace (nullptr when off).
+  long long* cap_t = nullptr;
+  float* cap_bias = nullptr;
+  int64_t cap_steps = 0;
+
   std::string error;
 
   ~zero_ctx() { zfs_host::pool_destroy(pool); }
@@ -293,6 +299,9 @@ zero_status launch_batches(zero_ctx* ctx, const std::vector<PlannedSeg>& segs, b
     a.clip = ctx->clip_ws ? reinterpret_cast<const float*>(ctx->clip_ws + 8) : nullptr;
     fill_scalars(ctx, t, &a);
     a.total_padded = ctx->padded_total;
+    a.dev_t = ctx->cap_t;
+    a.dev_bias = ctx->cap_bias;
+    a.dev_steps = ctx->cap_steps;
     if (ctx->inject == ZERO_INJECT_MISSING_COPY && vec) {
       a.inject_missing_copy = 1;
       ctx->inject = 0;
@@ -655,6 +664,9 @@ zero_status zero_step(zero_ctx* ctx, void* stream) {
       a.clip = reinterpret_cast<const float*>(ctx->clip_ws + 8);
       fill_scalars(ctx, t, &a);
       a.total_padded = ctx->padded_total - (ctx->inject == ZERO_INJECT_SHORT_BOUNDS ? zfs::kVec : 0);
+      a.dev_t = ctx->cap_t;
+      a.dev_bias = ctx->cap_bias;
+      a.dev_steps = ctx->cap_steps;
       a.inv_n = 1.0f;
       a.n_ranks = 1;
       a.grad_fp32 = 1;
@@ -684,6 +696,11 @@ zero_status zero_step(zero_ctx* ctx, void* stream) {
     if (st != ZERO_OK) return st;
   }
   if (ctx->inject == ZERO_INJECT_SHORT_BOUNDS) ctx->inject = 0;
+  if (ctx->cap_t) {
+    const cudaError_t e = zfs::launch_count_step(ctx->cap_t, s);
+    if (e != cudaSuccess) return fail_cuda(ctx, "step count launch", e);
+    ++launches;
+  }
   ctx->last_launches = launches;
   ctx->t = t;
   ctx->phase = Phase::kStepped;
@@ -1120,6 +1137,7 @@ zero_status zero_export_state(zero_ctx* ctx, float* master_out, float* exp_avg_o
   if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
   zero_status st = require_bound(ctx);
   if (st != ZERO_OK) return st;
+  if (ctx->cap_t) return fail(ctx, ZERO_ESTATE, "capturable mode: call zero_disable_capturable first");
   const void* ptrs[3] = {master_out, exp_avg_out, exp_avg_sq_out};
   const char* names[3] = {"master_out", "exp_avg_out", "exp_avg_sq_out"};
   st = check_state_buffers(ctx, ptrs, names);
@@ -1153,6 +1171,7 @@ zero_status zero_import_state(zero_ctx* ctx, const float* master_in, const float
   zero_status st = require_bound(ctx);
   if (st != ZERO_OK) return st;
   if (ctx->phase == Phase::kStepped) return fail(ctx, ZERO_ESTATE, "import while a step awaits post_step");
+  if (ctx->cap_t) return fail(ctx, ZERO_ESTATE, "capturable mode: call zero_disable_capturable first");
   if (t < 0) return fail(ctx, ZERO_EINVAL, "t is negative");
   const void* ptrs[3] = {master_in, exp_avg_in, exp_avg_sq_in};
   const char* names[3] = {"master_in", "exp_avg_in", "exp_avg_sq_in"};
@@ -1206,8 +1225,96 @@ zero_status zero_kernel_timeouts(const zero_ctx* ctx, uint32_t* count) {
   return ZERO_OK;
 }
 
+zero_status zero_capturable_workspace_bytes(const zero_ctx* ctx, int64_t max_steps, int64_t* bytes) {
+  if (!ctx || !bytes) return fail(nullptr, ZERO_EINVAL, "NULL argument");
+  if (max_steps < 1) return fail(const_cast<zero_ctx*>(ctx), ZERO_EINVAL, "max_steps must be >= 1");
+  *bytes = 16 + 8 * max_steps;  // the step count, then bc1, bc2 per step
+  return ZERO_OK;
+}
+
+zero_status zero_enable_capturable(zero_ctx* ctx, void* workspace, int64_t workspace_bytes, int64_t max_steps,
+                                   void* stream) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  zero_status st = require_bound(ctx);
+  if (st != ZERO_OK) return st;
+  if (ctx->offload) return fail(ctx, ZERO_ENOTSUP, "the offload step is not capturable (it runs on host threads)");
+  if (ctx->phase == Phase::kStepped) return fail(ctx, ZERO_ESTATE, "a step awaits post_step");
+  if (max_steps < 1) return fail(ctx, ZERO_EINVAL, "max_steps must be >= 1");
+  if (max_steps <= ctx->t) return fail(ctx, ZERO_EINVAL, "max_steps %lld does not exceed the steps taken (%lld)",
+                                       static_cast<long long>(max_steps), static_cast<long long>(ctx->t));
+  if (!workspace || !aligned(workspace, 16)) return fail(ctx, ZERO_EINVAL, "workspace NULL or not 16-byte aligned");
+  if (workspace_bytes < 16 + 8 * max_steps) return fail(ctx, ZERO_EINVAL, "workspace too small");
+  int wdev = -1;
+  if (!is_device_pointer(workspace, &wdev) || wdev != ctx->device)
+    return fail(ctx, ZERO_EINVAL, "workspace is not memory of the context's device");
+  std::vector<float> table;
+  try {
+    table.resize(static_cast<size_t>(2 * max_steps));
+  } catch (const std::bad_alloc&) {
+    return fail(ctx, ZERO_ENOMEM, "cannot allocate the host table");
+  }
+  for (int64_t t = 1; t <= max_steps; ++t) {  // the same scalars zero_step would pass
+    const zfs_host::AdamScalars sc = adam_scalars(ctx->cfg, t);
+    table[2 * (t - 1)] = sc.bc1;
+    table[2 * (t - 1) + 1] = sc.bc2;
+  }
+  long long* cap_t = static_cast<long long*>(workspace);
+  float* cap_bias = reinterpret_cast<float*>(static_cast<char*>(workspace) + 16);
+  const long long t_now = ctx->t;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(cap_t, &t_now, sizeof t_now, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(cap_bias, table.data(), table.size() * sizeof(float), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // the host sources leave scope here
+  if (e != cudaSuccess) return fail_cuda(ctx, "capturable upload", e);
+  ctx->cap_t = cap_t;
+  ctx->cap_bias = cap_bias;
+  ctx->cap_steps = max_steps;
+  return ZERO_OK;
+}
+
+namespace {
+
+// The device step count of a capturable context (synchronizes the stream).
+zero_status read_device_count(zero_ctx* ctx, void* stream, long long* t) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(t, ctx->cap_t, sizeof *t, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(ctx, "reading the step count", e);
+  return ZERO_OK;
+}
+
+}  // namespace
+
+zero_status zero_disable_capturable(zero_ctx* ctx, void* stream) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  if (!ctx->cap_t) return fail(ctx, ZERO_ESTATE, "capturable mode is not on");
+  long long t = 0;
+  zero_status st = read_device_count(ctx, stream, &t);
+  if (st != ZERO_OK) return st;
+  // Steps past the table were skipped: they changed nothing.
+  ctx->t = t < ctx->cap_steps ? t : ctx->cap_steps;
+  ctx->cap_t = nullptr;
+  ctx->cap_bias = nullptr;
+  ctx->cap_steps = 0;
+  return ZERO_OK;
+}
+
 zero_status zero_step_count(const zero_ctx* ctx, int64_t* t) {
   if (!ctx || !t) return fail(nullptr, ZERO_EINVAL, "NULL argument");
+  if (ctx->cap_t) {
+    zero_ctx* c = const_cast<zero_ctx*>(ctx);
+    long long d = 0;
+    zero_status st = read_device_count(c, nullptr, &d);
+    if (st != ZERO_OK) return st;
+    if (d > ctx->cap_steps) {
+      *t = ctx->cap_steps;
+      return fail(c, ZERO_ESTATE, "capturable table of %lld steps exhausted: %lld later step(s) were skipped",
+                  static_cast<long long>(ctx->cap_steps), d - static_cast<long long>(ctx->cap_steps));
+    }
+    *t = d;
+    return ZERO_OK;
+  }
   *t = ctx->t;
   return ZERO_OK;
 }

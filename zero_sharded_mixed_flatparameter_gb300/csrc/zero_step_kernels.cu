@@ -25,14 +25,33 @@ namespace zfs {
 namespace {
 
 // Adam / AdamW on one element (decay == 1 exactly for plain Adam).
-__device__ __forceinline__ void adam(const StepArgs& a, float g, float& w, float& m, float& v) {
+__device__ __forceinline__ void adam(const StepArgs& a, float bc1, float bc2, float g, float& w, float& m,
+                                     float& v) {
   w = __fmul_rn(w, a.decay);
   m = __fadd_rn(__fmul_rn(a.beta1, m), __fmul_rn(a.omb1, g));
   v = __fadd_rn(__fmul_rn(a.beta2, v), __fmul_rn(a.omb2, __fmul_rn(g, g)));
-  const float m_hat = __fdiv_rn(m, a.bc1);
-  const float v_hat = __fdiv_rn(v, a.bc2);
+  const float m_hat = __fdiv_rn(m, bc1);
+  const float v_hat = __fdiv_rn(v, bc2);
   const float denom = __fadd_rn(__fsqrt_rn(v_hat), a.eps);
   w = __fsub_rn(w, __fmul_rn(a.lr, __fdiv_rn(m_hat, denom)));
+}
+
+// The bias corrections of this step.  kDevBias (capturable steps): the step
+// count lives on the device and the host's table holds bc1, bc2 for every t
+// up to dev_steps; a count past the table gives false (the step is skipped,
+// the table is never read out of range).  Otherwise the launch carries them.
+template <bool kDevBias>
+__device__ __forceinline__ bool step_bias(const StepArgs& a, float* bc1, float* bc2) {
+  if constexpr (kDevBias) {
+    const long long t = *a.dev_t + 1;
+    if (t < 1 || t > a.dev_steps) return false;
+    *bc1 = a.dev_bias[2 * (t - 1)];
+    *bc2 = a.dev_bias[2 * (t - 1) + 1];
+  } else {
+    *bc1 = a.bc1;
+    *bc2 = a.bc2;
+  }
+  return true;
 }
 
 // Reduced gradient of one element k of segment s, any N, any alignment.
@@ -51,12 +70,13 @@ __device__ __forceinline__ float reduce_scalar(const StepArgs& a, const Seg& s, 
   return __fmul_rn(acc, a.inv_n);
 }
 
-__device__ __forceinline__ void step_scalar_element(const StepArgs& a, const Seg& s, long long k, float clip) {
+__device__ __forceinline__ void step_scalar_element(const StepArgs& a, const Seg& s, long long k, float clip,
+                                                    float bc1, float bc2) {
   const long long j = s.base + k;
   if (!ZFS_CHECK(k >= 0 && k < s.len && j < a.total_padded)) return;
   const float g = __fmul_rn(reduce_scalar(a, s, k), clip);
   float w = a.master[j], m = a.m[j], v = a.v[j];
-  adam(a, g, w, m, v);
+  adam(a, bc1, bc2, g, w, m, v);
   a.master[j] = w;
   a.m[j] = m;
   a.v[j] = v;
@@ -67,7 +87,8 @@ __device__ __forceinline__ void step_scalar_element(const StepArgs& a, const Seg
 // Vector kernel: 8 elements per thread-iteration.
 // ---------------------------------------------------------------------------
 template <int N, bool kFp32>
-__device__ __forceinline__ void step_vec8(const StepArgs& a, const Seg& s, long long vi, float clip) {
+__device__ __forceinline__ void step_vec8(const StepArgs& a, const Seg& s, long long vi, float clip, float bc1,
+                                          float bc2) {
   const long long j = s.base + vi * kVec;
   if (!ZFS_CHECK(vi >= 0 && (vi + 1) * kVec <= s.len && j + kVec <= a.total_padded)) return;
   float g[kVec];
@@ -111,7 +132,7 @@ __device__ __forceinline__ void step_vec8(const StepArgs& a, const Seg& s, long 
   float m[kVec] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
   float v[kVec] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-  for (int e = 0; e < kVec; ++e) adam(a, __fmul_rn(__fmul_rn(g[e], a.inv_n), clip), w[e], m[e], v[e]);
+  for (int e = 0; e < kVec; ++e) adam(a, bc1, bc2, __fmul_rn(__fmul_rn(g[e], a.inv_n), clip), w[e], m[e], v[e]);
   st_stream_f4(a.master + j, make_float4(w[0], w[1], w[2], w[3]));
   st_stream_f4(a.master + j + 4, make_float4(w[4], w[5], w[6], w[7]));
   st_stream_f4(a.m + j, make_float4(m[0], m[1], m[2], m[3]));
@@ -129,17 +150,19 @@ __device__ __forceinline__ void step_vec8(const StepArgs& a, const Seg& s, long 
 // Minimum of one resident CTA in the bounds lets each thread keep all of its
 // 16-byte loads in flight before the first use (about 94 registers at N = 8);
 // the grid then caps residency at kStepCtasPerSm CTAs per SM (see launch_step_vec).
-template <int N, bool kFp32>
+template <int N, bool kFp32, bool kDevBias>
 __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_constant__ StepArgs a) {
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  float bc1, bc2;
+  if (!step_bias<kDevBias>(a, &bc1, &bc2)) return;
   // Clip coefficient of the global norm (x 1 is exact when not clipping).
   const float clip = a.clip ? *a.clip : 1.0f;
   for (int s = 0; s < a.nseg; ++s) {
     const Seg& seg = a.seg[s];
     const long long nvec = seg.len / kVec;
     for (long long vi = first_index(tid, seg.vec_start, stride); vi < nvec; vi += stride) {
-      step_vec8<N, kFp32>(a, seg, vi, clip);
+      step_vec8<N, kFp32>(a, seg, vi, clip, bc1, bc2);
     }
   }
   // Ragged ends (fewer than 8 elements per segment), element by element.
@@ -148,7 +171,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
     const long long done = (seg.len / kVec) * kVec;
     const long long k = done + tid - static_cast<long long>(s) * kVec;
     if (tid >= static_cast<long long>(s) * kVec && k < seg.len && k < done + kVec) {
-      step_scalar_element(a, seg, k, clip);
+      step_scalar_element(a, seg, k, clip, bc1, bc2);
     }
   }
 }
@@ -252,8 +275,10 @@ __device__ __forceinline__ void locate_tile(const StepArgs& a, long long id, int
   *ti = id;
 }
 
-template <int N, bool kFp32>
+template <int N, bool kFp32, bool kDevBias>
 __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_constant__ StepArgs a) {
+  float bc1, bc2;
+  if (!step_bias<kDevBias>(a, &bc1, &bc2)) return;  // before any barrier or copy
   using L = TmaTile<N, kFp32>;
   static_assert(kTmaTile == kStepThreads * kVec, "8 elements per thread per tile");
   extern __shared__ __align__(128) unsigned char smem[];
@@ -364,7 +389,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
       if (next < n_tiles) issue(next, stage);
     }
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) adam(a, __fmul_rn(__fmul_rn(g[e], a.inv_n), clip), w[e], m[e], v[e]);
+    for (int e = 0; e < kVec; ++e) adam(a, bc1, bc2, __fmul_rn(__fmul_rn(g[e], a.inv_n), clip), w[e], m[e], v[e]);
     int si;
     long long ti;
     locate_tile(a, id, &si, &ti);
@@ -422,7 +447,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
   for (int s = 0; s < a.nseg; ++s) {
     const Seg& sg = a.seg[s];
     for (long long k = (sg.len / kTmaTile) * kTmaTile + tid; k < sg.len; k += stride) {
-      step_scalar_element(a, sg, k, clip);
+      step_scalar_element(a, sg, k, clip, bc1, bc2);
     }
   }
 }
@@ -430,44 +455,50 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
 // ---------------------------------------------------------------------------
 // Scalar kernel: one element per thread-iteration, any alignment, any N.
 // ---------------------------------------------------------------------------
+template <bool kDevBias>
 __global__ void __launch_bounds__(kStepThreads) step_scalar_kernel(const __grid_constant__ StepArgs a) {
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  float bc1, bc2;
+  if (!step_bias<kDevBias>(a, &bc1, &bc2)) return;
   const float clip = a.clip ? *a.clip : 1.0f;
   long long start = 0;
   for (int s = 0; s < a.nseg; ++s) {
     const Seg& seg = a.seg[s];
     for (long long k = first_index(tid, start, stride); k < seg.len; k += stride) {
-      step_scalar_element(a, seg, k, clip);
+      step_scalar_element(a, seg, k, clip, bc1, bc2);
     }
     start += seg.len;
   }
 }
+
+// Capturable steps: the device step count advances after the step's launches.
+__global__ void count_step_kernel(long long* t) { *t += 1; }
 
 // ---------------------------------------------------------------------------
 // Launch configuration.
 // ---------------------------------------------------------------------------
 using StepKernel = void (*)(StepArgs);
 
-template <bool kFp32>
+template <bool kFp32, bool kDevBias>
 StepKernel vec_kernel_for(int n) {
   switch (n) {
-    case 1: return step_vec_kernel<1, kFp32>;
-    case 2: return step_vec_kernel<2, kFp32>;
-    case 3: return step_vec_kernel<3, kFp32>;
-    case 4: return step_vec_kernel<4, kFp32>;
-    case 5: return step_vec_kernel<5, kFp32>;
-    case 6: return step_vec_kernel<6, kFp32>;
-    case 7: return step_vec_kernel<7, kFp32>;
-    case 8: return step_vec_kernel<8, kFp32>;
-    case 9: return step_vec_kernel<9, kFp32>;
-    case 10: return step_vec_kernel<10, kFp32>;
-    case 11: return step_vec_kernel<11, kFp32>;
-    case 12: return step_vec_kernel<12, kFp32>;
-    case 13: return step_vec_kernel<13, kFp32>;
-    case 14: return step_vec_kernel<14, kFp32>;
-    case 15: return step_vec_kernel<15, kFp32>;
-    case 16: return step_vec_kernel<16, kFp32>;
+    case 1: return step_vec_kernel<1, kFp32, kDevBias>;
+    case 2: return step_vec_kernel<2, kFp32, kDevBias>;
+    case 3: return step_vec_kernel<3, kFp32, kDevBias>;
+    case 4: return step_vec_kernel<4, kFp32, kDevBias>;
+    case 5: return step_vec_kernel<5, kFp32, kDevBias>;
+    case 6: return step_vec_kernel<6, kFp32, kDevBias>;
+    case 7: return step_vec_kernel<7, kFp32, kDevBias>;
+    case 8: return step_vec_kernel<8, kFp32, kDevBias>;
+    case 9: return step_vec_kernel<9, kFp32, kDevBias>;
+    case 10: return step_vec_kernel<10, kFp32, kDevBias>;
+    case 11: return step_vec_kernel<11, kFp32, kDevBias>;
+    case 12: return step_vec_kernel<12, kFp32, kDevBias>;
+    case 13: return step_vec_kernel<13, kFp32, kDevBias>;
+    case 14: return step_vec_kernel<14, kFp32, kDevBias>;
+    case 15: return step_vec_kernel<15, kFp32, kDevBias>;
+    case 16: return step_vec_kernel<16, kFp32, kDevBias>;
     default: return nullptr;
   }
 }
@@ -476,9 +507,10 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
   int sms = 0;
-  int vec_blocks_per_sm[2][kMaxRanks + 1] = {};
-  int scalar_blocks_per_sm = 0;
-  int tma_smem_set[2][kMaxRanks + 1] = {};
+  // [device-side bias][fp32 gradients][N]
+  int vec_blocks_per_sm[2][2][kMaxRanks + 1] = {};
+  int scalar_blocks_per_sm[2] = {};
+  int tma_smem_set[2][2][kMaxRanks + 1] = {};
 };
 
 // Shared memory of one SM usable by CTAs, and what each CTA reserves.
@@ -542,17 +574,17 @@ unsigned int step_timeouts() {
   return v;
 }
 
-template <int N, bool kFp32>
+template <int N, bool kFp32, bool kDevBias>
 cudaError_t launch_tma(const StepArgs& a, cudaStream_t stream) {
   constexpr uint32_t kSmem = TmaTile<N, kFp32>::kSmemBytes;
   static_assert(kSmem + 128 <= 227 * 1024, "staged tiles must fit one CTA's shared memory (227 KB)");
   const int dev = current_device();
   {
     std::lock_guard<std::mutex> lock(g_info_mutex);
-    int& done = g_info[dev].tma_smem_set[kFp32 ? 1 : 0][N];
+    int& done = g_info[dev].tma_smem_set[kDevBias ? 1 : 0][kFp32 ? 1 : 0][N];
     if (!done) {
-      const cudaError_t e =
-          cudaFuncSetAttribute(step_tma_kernel<N, kFp32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      const cudaError_t e = cudaFuncSetAttribute(step_tma_kernel<N, kFp32, kDevBias>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
       if (e != cudaSuccess) return e;
       done = 1;
     }
@@ -560,27 +592,29 @@ cudaError_t launch_tma(const StepArgs& a, cudaStream_t stream) {
   int per_sm = static_cast<int>(kMaxSmemPerSm / (kSmem + kSmemReservedPerCta));
   if (per_sm < 1) per_sm = 1;
   if (per_sm > kStepCtasPerSm) per_sm = kStepCtasPerSm;
-  step_tma_kernel<N, kFp32><<<static_cast<unsigned>(cached_sms(dev) * per_sm), kStepThreads, kSmem, stream>>>(a);
+  step_tma_kernel<N, kFp32, kDevBias>
+      <<<static_cast<unsigned>(cached_sms(dev) * per_sm), kStepThreads, kSmem, stream>>>(a);
   return cudaGetLastError();
 }
 
 // The staged kernel where it measured faster and its tiles fit in shared memory.
+template <bool kDevBias>
 cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launched) {
   *launched = true;
   if (!a.grad_fp32) {
     switch (a.n_ranks) {
-      case 11: return launch_tma<11, false>(a, stream);
-      case 12: return launch_tma<12, false>(a, stream);
-      case 13: return launch_tma<13, false>(a, stream);
-      case 14: return launch_tma<14, false>(a, stream);
-      case 15: return launch_tma<15, false>(a, stream);
-      case 16: return launch_tma<16, false>(a, stream);
+      case 11: return launch_tma<11, false, kDevBias>(a, stream);
+      case 12: return launch_tma<12, false, kDevBias>(a, stream);
+      case 13: return launch_tma<13, false, kDevBias>(a, stream);
+      case 14: return launch_tma<14, false, kDevBias>(a, stream);
+      case 15: return launch_tma<15, false, kDevBias>(a, stream);
+      case 16: return launch_tma<16, false, kDevBias>(a, stream);
       default: break;
     }
   } else {
     switch (a.n_ranks) {
-      case 8: return launch_tma<8, true>(a, stream);
-      case 9: return launch_tma<9, true>(a, stream);
+      case 8: return launch_tma<8, true, kDevBias>(a, stream);
+      case 9: return launch_tma<9, true, kDevBias>(a, stream);
       default: break;
     }
   }
@@ -588,17 +622,18 @@ cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launche
   return cudaSuccess;
 }
 
-cudaError_t launch_step_vec(const StepArgs& a, cudaStream_t stream) {
+template <bool kDevBias>
+cudaError_t launch_step_vec_t(const StepArgs& a, cudaStream_t stream) {
   if (a.total_elems >= kTmaMinElems && a.n_ranks >= (a.grad_fp32 ? kTmaMinRanksFp32 : kTmaMinRanks)) {
     bool launched = false;
-    const cudaError_t e = try_launch_tma(a, stream, &launched);
+    const cudaError_t e = try_launch_tma<kDevBias>(a, stream, &launched);
     if (launched) return e;
   }
-  StepKernel k = a.grad_fp32 ? vec_kernel_for<true>(a.n_ranks) : vec_kernel_for<false>(a.n_ranks);
+  StepKernel k = a.grad_fp32 ? vec_kernel_for<true, kDevBias>(a.n_ranks) : vec_kernel_for<false, kDevBias>(a.n_ranks);
   if (!k) return cudaErrorInvalidValue;
   const int dev = current_device();
   const int sms = cached_sms(dev);
-  int bps = resident_blocks(&g_info[dev].vec_blocks_per_sm[a.grad_fp32 ? 1 : 0][a.n_ranks],
+  int bps = resident_blocks(&g_info[dev].vec_blocks_per_sm[kDevBias ? 1 : 0][a.grad_fp32 ? 1 : 0][a.n_ranks],
                             reinterpret_cast<const void*>(k));
   // 512 resident threads per SM: measured on GB300 to give the best DRAM
   // efficiency across N = 1..16 (more threads widen the address window the
@@ -612,13 +647,27 @@ cudaError_t launch_step_vec(const StepArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_step_scalar(const StepArgs& a, cudaStream_t stream) {
+template <bool kDevBias>
+cudaError_t launch_step_scalar_t(const StepArgs& a, cudaStream_t stream) {
   const int dev = current_device();
   const int sms = cached_sms(dev);
-  const int bps = resident_blocks(&g_info[dev].scalar_blocks_per_sm,
-                                  reinterpret_cast<const void*>(step_scalar_kernel));
+  const int bps = resident_blocks(&g_info[dev].scalar_blocks_per_sm[kDevBias ? 1 : 0],
+                                  reinterpret_cast<const void*>(step_scalar_kernel<kDevBias>));
   const long long grid = grid_for(a.total_elems, sms, bps);
-  step_scalar_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(a);
+  step_scalar_kernel<kDevBias><<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_step_vec(const StepArgs& a, cudaStream_t stream) {
+  return a.dev_t ? launch_step_vec_t<true>(a, stream) : launch_step_vec_t<false>(a, stream);
+}
+
+cudaError_t launch_step_scalar(const StepArgs& a, cudaStream_t stream) {
+  return a.dev_t ? launch_step_scalar_t<true>(a, stream) : launch_step_scalar_t<false>(a, stream);
+}
+
+cudaError_t launch_count_step(long long* t, cudaStream_t stream) {
+  count_step_kernel<<<1, 1, 0, stream>>>(t);
   return cudaGetLastError();
 }
 

@@ -206,6 +206,18 @@ class FlatStep:
                             self.stream_handle(stream))
         torch.cuda.current_stream(self.device).synchronize()
 
+    def enable_capturable(self, max_steps: int, stream=None) -> None:
+        """Capturable mode (CUDA graphs): the step count and the bias
+        corrections of steps 1..max_steps live in a device workspace, so a
+        captured step can be replayed.  The workspace is allocated by torch."""
+        need = B.zero_capturable_workspace_bytes(self.ctx, max_steps)
+        self._cap_ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        B.zero_enable_capturable(self.ctx, self._cap_ws.data_ptr(), need, max_steps, self.stream_handle(stream))
+
+    def disable_capturable(self, stream=None) -> None:
+        B.zero_disable_capturable(self.ctx, self.stream_handle(stream))
+        self._cap_ws = None
+
     def step_count(self) -> int:
         return B.zero_step_count(self.ctx)
 
