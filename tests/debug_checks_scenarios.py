@@ -43,6 +43,22 @@ def main():
              clip_keep=True)
     scenario("offload, 1,000-element chunks", make_problem(odd, 4, 2, steps=2, seed=216),
              offload=dict(chunk=1000, threads=3))
+    # capturable mode: the kernels read the step count and bias corrections from the device
+    import torch
+    from gpu_common import gpu_flatstep, upload_grads
+    pb = make_problem(odd, 8, 3, steps=3, seed=217, max_norm=0.05)
+    ref = oracle_run(pb)
+    fs = gpu_flatstep(pb)
+    fs.enable_capturable(max_steps=8)
+    for t in range(1, 4):
+        fs.reduce_grads(-1, upload_grads(pb, t))
+        fs.clip_grad_norm(pb.max_norm)
+        fs.step()
+        fs.post_step()
+    torch.cuda.synchronize()
+    compare_state(fs, ref, "capturable mode")
+    fs.close()
+    print("ok capturable mode", flush=True)
     failures = B.zero_debug_check_failures()
     print("debug check failures:", failures, flush=True)
     if failures != 0:
