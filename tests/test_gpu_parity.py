@@ -180,3 +180,21 @@ def test_tile_staged_threshold_neighbours():
         fs = run_gpu(pb, mode="all")
         compare_state(fs, ref, f"{total} elements")
         fs.close()
+
+
+@pytest.mark.parametrize("fresh", [False, True])
+def test_long_run(fresh):
+    # many steps, bit for bit: an error that grows step by step (the pages
+    # found a silent bug only by running identical data every step and
+    # watching the error grow) shows here.  N = 3 makes 1/N inexact; AdamW.
+    steps = 100 if fresh else 200
+    pl = si.from_units([1552, 7, 3000, 33])
+    pb = make_problem(pl, 3, 3, steps=1 if not fresh else steps, seed=500 + fresh, adamw=True, weight_decay=0.1,
+                      max_norm=0.05 if fresh else 0.0)
+    if not fresh:
+        pb.grads = pb.grads * steps              # the same gradients every step
+    ref = oracle_run(pb)
+    fs = run_gpu(pb, mode="units")
+    compare_state(fs, ref, f"after {steps} steps")
+    assert fs.step_count() == steps
+    fs.close()
