@@ -1,12 +1,19 @@
 // Host runtime of the ZeRO flat-parameter library: the C ABI declared in
 // include/zero_flatstep.h.  It owns only host metadata — the FlatParameter
-// layout, the registered gradient pointers, the step count and error text —
-// and enqueues the sm_103a kernels (zero_step_kernels.cu, zero_aux_kernels.cu) on the caller's stream.
+// layout, the registered gradient pointers, the step count and error text,
+// and an offload context's worker threads — and enqueues the sm_103a kernels
+// (zero_step_kernels.cu, zero_aux_kernels.cu) on the caller's stream.
 //
 // Protocol: Femtotron dev log #6 (ShardingStrategy: make_master /
 // reduce_grads / gather_weights / post_step).  Layout: CMU 15-779 Lecture 13
 // notes §0.4 and §5.2 (flatten, concatenate, right-pad to a multiple of F,
 // split evenly).  Ledger: same notes §2.3, §3.5, §9 item 2, §11 Exercise 5.
+// ZeRO-Offload (host-resident fp32 state, CPU Adam): same notes §7.1-7.2.
+//
+// Sections, in order: context and helpers; planning and make_master (also
+// the offload variant); registration; the step; the offload step and the
+// stateless CPU Adam; clipping; gather / post_step; checkpoints; queries,
+// test hooks and capturable mode.
 
 #include <algorithm>
 #include <cmath>
