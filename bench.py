@@ -570,7 +570,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": warm_done, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; bf16/fp32 grads, fp32 state)",
-            "config": {"workload": args.workload, "model": pl.name, "params": pl.total, "padded_params": padded,
+            "config": {"workload": args.workload, "layout": pl.name, "params": pl.total, "padded_params": padded,
                        "units": fs.n_units, "n_ranks_simulated": n, "zero_stage": wl["stage"],
                        "grad_dtype": wl["grad_dtype"], "optimizer": "Adam fp32 (lr 1e-3, betas 0.9/0.999, eps 1e-8)",
                        "parallelism": f"{world} GPU replica(s); N={n} DP ranks simulated per GPU",
@@ -706,7 +706,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "model": wl["pl"].name, "params": wl["pl"].total,
+        "config": {"workload": args.workload, "layout": wl["pl"].name, "params": wl["pl"].total,
                    "n_ranks_simulated": wl["n"], "zero_stage": wl["stage"], "grad_dtype": wl["grad_dtype"]},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"each step: one literal per-rank oracle step on a contiguous {sample_params:,}-param "
