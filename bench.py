@@ -677,6 +677,39 @@ def run_sweep(args):
 
 
 # ---------------------------------------------------------------------------
+# DRAM ceilings by read:write mix: torch's own elementwise kernels over
+# 256 M-element fp32 tensors (1 GiB each), GB/s of bytes moved.  Context for
+# the roofline: the copy (1 : 1) is the most write-heavy mix; the step at
+# N = 8 bf16 is 2 : 1 and at N = 16 about 3 : 1.
+# ---------------------------------------------------------------------------
+def run_mix_ceilings(args):
+    import torch
+    n = 256 * 1024 * 1024
+    t = [torch.randn(n, device="cuda") for _ in range(4)]
+
+    def gbs(fn, nbytes, reps=30):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        return nbytes / statistics.median(times) / 1e6
+    print(json.dumps({
+        "mix_ceilings_gbs": {
+            "copy 1:1": gbs(lambda: t[1].copy_(t[0]), 8 * n),
+            "add 2:1": gbs(lambda: torch.add(t[0], t[1], out=t[2]), 12 * n),
+            "addcmul 3:1": gbs(lambda: torch.addcmul(t[0], t[1], t[2], out=t[3]), 16 * n),
+            "fill 0:1": gbs(lambda: t[3].fill_(1.0), 4 * n)},
+        "tensors": "4 x 256 M fp32 (1 GiB each)", "peak_measured_gbs": measured_peaks()[0]}), flush=True)
+
+
+# ---------------------------------------------------------------------------
 # Reference arm: the CPU oracle on the host cores.
 # ---------------------------------------------------------------------------
 def run_reference(args):
@@ -735,6 +768,8 @@ def main():
                     help="fp32 gradient accumulation of this many bf16 micro-steps before every step (fp32 workloads)")
     ap.add_argument("--clip-keep", action="store_true",
                     help="with --clip: keep the reduced gradient for the step (fewer bytes for N > 4)")
+    ap.add_argument("--mix-ceilings", action="store_true",
+                    help="DRAM GB/s of torch copy / add / addcmul / fill (read:write mixes 1:1 .. 0:1)")
     ap.add_argument("--sweep", action="store_true",
                     help="roofline sweep of flat buffers (one JSON line per point instead of the bench line)")
     ap.add_argument("--sweep-sizes", default="1e6,16e6,128e6,512e6,1e9")
@@ -748,7 +783,9 @@ def main():
         ap.error("--graph and --offload exclude each other (the offload step runs on host threads)")
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.sweep:
+    if args.mix_ceilings:
+        run_mix_ceilings(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
