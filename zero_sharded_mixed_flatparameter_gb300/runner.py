@@ -73,6 +73,8 @@ class FlatStep:
             self._host_ws = torch.empty(hb, dtype=torch.uint8, pin_memory=True)
             self._dev_ws = torch.empty(db, dtype=torch.uint8, device=self.device)
             self._copy_stream = torch.cuda.Stream(self.device)
+        # padded length of every unit, for the registration length checks
+        self._unit_padded = [B.zero_layout(self.ctx, i)[1] for i in range(self.n_units)]
         # make_master reads the init params on the stream; once it has run they
         # may be released.
         torch.cuda.current_stream(self.device).synchronize()
@@ -129,7 +131,11 @@ class FlatStep:
     def _need(self, unit: int) -> int:
         """Elements each replica buffer of `unit` (-1: all units) must hold:
         the padded length the kernels read, pads included."""
-        return self.padded if unit < 0 else self.layout(unit)[1]
+        if unit < 0:
+            return self.padded
+        if unit >= self.n_units:
+            return 0  # the library reports the bad unit
+        return self._unit_padded[unit]
 
     def reduce_grads(self, unit: int, replica_grads: Sequence[torch.Tensor], stream=None) -> None:
         want = self.grad_dtype_torch()
