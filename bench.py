@@ -52,6 +52,14 @@ def workload(name: str):
                     per_unit=False, outliers=0.0)
     if name == "toy_mlp_n4":
         return dict(pl=si.toy_mlp(), n=4, stage=2, grad_dtype="bf16", grad_std=1e-2, per_unit=True, outliers=0.0)
+    if name.startswith("flat32:"):  # one flat buffer, fp32 replica gradients, ZeRO-1 (the stage-buffer case, any size)
+        _, numel, n = name.split(":")
+        return dict(pl=si.single_buffer(int(float(numel))), n=int(n), stage=1, grad_dtype="fp32", grad_std=1e-3,
+                    per_unit=False, outliers=0.0)
+    if name.startswith("units3:"):  # ZeRO-3 over equal units with per-unit gathers
+        _, units, numel, n = name.split(":")
+        return dict(pl=si.from_units([int(float(numel))] * int(units)), n=int(n), stage=3, grad_dtype="bf16",
+                    grad_std=1e-3, per_unit=True, outliers=0.0)
     if name.startswith("flat:"):
         _, numel, n = name.split(":")
         return dict(pl=si.single_buffer(int(float(numel))), n=int(n), stage=2, grad_dtype="bf16", grad_std=1e-2,
