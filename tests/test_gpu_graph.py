@@ -146,3 +146,48 @@ def test_capturable_refusals():
     finally:
         fs.close()
         off.close()
+
+
+def test_capturable_step_over_several_launches():
+    # 100 units registered separately: the step spans three launches (48
+    # segments each), which must all read the same device step count, and
+    # the count advances once per step; replayed as a graph too
+    pl = si.from_units([211 + 17 * (i % 5) for i in range(100)])
+    steps = 4
+    pb = make_problem(pl, 3, 2, steps=steps, seed=480)
+    refs = _refs(pb)
+    fs = gpu_flatstep(pb)
+    try:
+        fs.enable_capturable(max_steps=steps)
+        # one separately allocated buffer per unit and replica: the units do
+        # not merge into one segment, so the step takes several launches
+        spans = [fs.layout(i) for i in range(fs.n_units)]
+        views = [[torch.empty(padded, dtype=torch.bfloat16, device="cuda") for _ in range(pb.n)]
+                 for (numel, padded, shard, base) in spans]
+
+        def load(t):
+            for f_r, r in zip(upload_grads(pb, t), range(pb.n)):
+                for (numel, padded, shard, base), v in zip(spans, views):
+                    v[r].copy_(f_r[base:base + padded])
+        load(1)
+
+        def one_step():
+            for i, v in enumerate(views):
+                fs.reduce_grads(i, v)
+            fs.step()
+            fs.post_step()
+        one_step()
+        torch.cuda.synchronize()
+        assert fs.last_launches() == 4  # 100 segments in three step launches, then the count
+        compare_state(fs, refs[1], "eager step over several launches")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one_step()
+        for t in range(2, steps + 1):
+            load(t)
+            graph.replay()
+            torch.cuda.synchronize()
+            compare_state(fs, refs[t], f"replay {t} over several launches")
+        assert fs.step_count() == steps
+    finally:
+        fs.close()

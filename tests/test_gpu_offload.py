@@ -210,3 +210,11 @@ def test_make_master_offload_rejects_device_state():
         B.zero_make_master_offload(cfg, pl.numel, pl.unit, [init.data_ptr()], *(h.data_ptr() for h in host),
                                    torch.zeros(64, dtype=torch.bfloat16).data_ptr())
     assert e.value.status == B.ZERO_EINVAL
+
+
+def test_many_units_span_several_reduce_launches():
+    # 100 units (more than the 48 segments one reduce launch takes) with
+    # chunks that span dozens of units each, ZeRO-3, clipped
+    pl = si.from_units([97 + 13 * (i % 7) for i in range(100)])
+    pb = make_problem(pl, 4, 3, steps=3, seed=470, max_norm=0.05)
+    _per_step(pb, "separate", dict(chunk=5000, threads=3))
