@@ -13,7 +13,10 @@
  * Conventions for every call:
  *  - Plain pointers and sizes only.  "dev" pointers are CUDA device memory
  *    owned by the caller; the library never allocates, frees or retains
- *    device memory, and holds only host-side metadata in a zero_ctx.
+ *    device memory, and holds only host-side metadata in a zero_ctx.  Two
+ *    stated exceptions: zero_clip_grad_norm_static's fixed scratch array in
+ *    the library's own device memory, and an offload context's host worker
+ *    threads (see the ZeRO-Offload calls).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Device work is enqueued on it asynchronously; the caller keeps
  *    every buffer alive until that work has completed on the stream.
@@ -207,8 +210,12 @@ zero_status zero_accumulate_grads(zero_ctx* ctx, int32_t unit, const void* const
  * contraction, IEEE division and square root).  After zero_clip_grad_norm,
  * g is multiplied by the clip coefficient before Adam.  Requires every unit's
  * gradients registered since the last post_step.
+ * In capturable mode (zero_enable_capturable) the bias corrections come
+ * from the device table and one more one-thread launch advances the device
+ * step count.
  * Errors: ZERO_ESTATE (no buffers, missing gradients, step already taken
- * without post_step); ZERO_ECUDA (a launch failed; t is left unchanged, but
+ * without post_step, an offload context — its step is zero_offload_step);
+ * ZERO_ECUDA (a launch failed; t is left unchanged, but
  * when a step needs more than one launch — more than 48 gradient segments, or
  * both aligned and unaligned ones — launches enqueued before the failing one
  * have updated their elements).
@@ -311,8 +318,9 @@ zero_status zero_gather_weights(zero_ctx* ctx, int32_t unit, void* unit_buf, voi
 
 /*
  * zero_post_step — the protocol's post_step: forget the registered gradients
- * (and the pending clip coefficient) so the next step needs fresh ones.  ZERO_ESTATE unless a step was taken
- * since the last post_step.  No device work.
+ * (and the pending clip coefficient) so the next step needs fresh ones.
+ * ZERO_ESTATE unless a step was taken since the last post_step.  No device
+ * work.
  */
 zero_status zero_post_step(zero_ctx* ctx, void* stream);
 
