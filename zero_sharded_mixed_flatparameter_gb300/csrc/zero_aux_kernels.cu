@@ -353,10 +353,13 @@ __global__ void copy_f32_kernel(const float* __restrict__ src, float* __restrict
   for (long long k = tid; k < n; k += stride) dst[k] = src[k];
 }
 
+// One 16-byte vector per thread over a grid covering the unit (no grid-
+// stride loop) with plain loads and stores: measured as the fastest of the
+// copy variants tried — on 800 MB 6566 GB/s against 6353-6404 for a
+// persistent 8-CTA-per-SM grid with streaming hints (cudaMemcpyAsync: 6621).
 __global__ void gather_vec_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n16) {
-  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = tid; i < n16; i += stride) __stcs(dst + i, __ldcs(src + i));
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n16) dst[i] = src[i];
 }
 
 __global__ void gather_scalar_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
@@ -531,7 +534,8 @@ cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaS
   if (aligned) {
     const long long n16 = n / 8;
     if (n16 > 0) {
-      const long long grid = grid_for(n16, sm_count(), 8);
+      // one thread per vector: under 2^31 blocks for any unit a device can hold
+      const long long grid = (n16 + kStepThreads - 1) / kStepThreads;
       gather_vec_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(
           reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), n16);
       const cudaError_t e = cudaGetLastError();
