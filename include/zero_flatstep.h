@@ -483,7 +483,7 @@ zero_status zero_kernel_timeouts(const zero_ctx* ctx, uint32_t* count);
 /*
  * zero_debug_inject — test hook for the bounded waits above (the pages have
  * no counterpart).  what = ZERO_INJECT_MISSING_COPY arms it for the next
- * zero_step: if that step's first launch uses the tile-staged kernel, the
+ * zero_step: if that step's first launch uses a tile-staged kernel, the
  * kernel announces the bytes of the launch's first tile to its mbarrier but
  * issues no copy for it, so that one wait runs out after about a second;
  * the CTA then counts a timeout (zero_kernel_timeouts), waits for the copies

@@ -120,7 +120,8 @@ def test_stage3_gather_argument_checks():
         fs.close()
 
 
-def test_staged_wait_runs_out_and_the_device_stays_usable():
+@pytest.mark.parametrize("n,gd,tile", [(16, "bf16", 2048), (12, "fp32", 1024)])
+def test_staged_wait_runs_out_and_the_device_stays_usable(n, gd, tile):
     # The tile-staged step kernel bounds every wait for its bulk copies.  The
     # test hook announces the launch's first tile to its mbarrier without
     # issuing the copy, so CTA 0's wait runs out (after ~1 s): it counts a
@@ -130,9 +131,8 @@ def test_staged_wait_runs_out_and_the_device_stays_usable():
     # context runs normally.
     import time
     from gpu_common import to_np
-    n = 16
-    total = (1 << 23) + 2048 * 3 + 300          # padded to a multiple of 16 below
-    pb = make_problem(si.from_units([total]), n, 2, steps=2, seed=97)
+    total = (1 << 23) + 2048 * 3 + 300          # padded to a multiple of N below
+    pb = make_problem(si.from_units([total]), n, 2, grad_dtype=gd, steps=2, seed=97)
     padded = pb.lay.total_padded
     fs = gpu_flatstep(pb, guard=64)
     try:
@@ -147,10 +147,10 @@ def test_staged_wait_runs_out_and_the_device_stays_usable():
         waited = time.perf_counter() - t0
         assert B.zero_kernel_timeouts(fs.ctx) == before + 1
         assert 0.5 < waited < 10.0, waited
-        # CTA 0's elements: tiles 0, G, 2G, ... (one CTA per SM at N = 16) and
-        # the first 256 elements after the last full tile
+        # CTA 0's elements: tiles 0, G, 2G, ... (one CTA per SM for both
+        # kernels at these N) and the first 256 elements after the last full tile
         sms = torch.cuda.get_device_properties(0).multi_processor_count
-        tile, full = 2048, padded // 2048
+        full = padded // tile
         mine = np.zeros(padded, bool)
         for tid in range(0, full, sms):
             mine[tid * tile:(tid + 1) * tile] = True

@@ -16,7 +16,7 @@ constexpr int kStepThreads = 256; // threads per CTA of the step kernels
 constexpr int kStepCtasPerSm = 2; // resident CTAs per SM of the vector step kernel
 // Tile-staged (TMA bulk copy) step kernel: used from this many replicas on.
 constexpr int kTmaMinRanks = 11;     // bf16 replicas
-constexpr int kTmaMinRanksFp32 = 8;  // fp32 replicas (8 and 9 only)
+constexpr int kTmaMinRanksFp32 = 8;  // fp32 replicas (2,048-element tiles for 8, 9; 1,024 from 10)
 constexpr long long kTmaMinElems = 1LL << 23;  // and from this many elements per launch
 constexpr long long kTmaTile = 2048; // elements per tile (one 8-element vector per thread)
 constexpr int kTmaStages = 2;        // tiles in flight per CTA

@@ -453,6 +453,154 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
 }
 
 // ---------------------------------------------------------------------------
+// Tile-staged kernel for many fp32 replicas (N = 10..16): tiles of 1,024
+// elements, 4 per thread, so that two stages of N + 3 tiles of 4 KB fit one
+// CTA's shared memory (2,048-element tiles do not from N = 10 on).  Thread t
+// takes elements 4t..4t+3 of a tile: every warp reads contiguous 512-byte
+// runs of shared memory.  Waits, give-up, test hook and index checks as in
+// step_tma_kernel; the arithmetic per element is step_vec8's.
+//
+// Measured on GB300 over 400 M elements (step bytes / event time): one CTA
+// per SM with three stages at N = 10, 11 (7,135 and 7,151 GB/s; two stages
+// 7,076 / 7,123; two CTAs per SM 6,887 / 6,902) and two stages from N = 12
+// on (7,133-7,179 GB/s; three stages 6,651-6,949), against 6,800-6,889 GB/s
+// for the register-staged kernel at N = 10..16.
+// ---------------------------------------------------------------------------
+constexpr long long kTma4Tile = kStepThreads * 4;
+constexpr int kTma4CtasPerSm = 1;
+
+template <int N>
+struct Tma4Tile {
+  static constexpr uint32_t kBytes = kTma4Tile * 4;  // every stream is fp32
+  static constexpr uint32_t kStageBytes = (N + 3) * kBytes;
+  static constexpr int kStages = N <= 11 ? 3 : 2;
+  static constexpr uint32_t kSmemBytes = kStageBytes * kStages;
+};
+
+// Full kTma4Tile-element tiles of a launch, segment after segment.
+__device__ __forceinline__ void locate_tile4(const StepArgs& a, long long id, int* si, long long* ti) {
+  int s = 0;
+  while (id >= a.seg[s].len / kTma4Tile) {
+    id -= a.seg[s].len / kTma4Tile;
+    ++s;
+  }
+  *si = s;
+  *ti = id;
+}
+
+template <int N, bool kDevBias>
+__global__ void __launch_bounds__(kStepThreads, 1) step_tma4_kernel(const __grid_constant__ StepArgs a) {
+  float bc1, bc2;
+  if (!step_bias<kDevBias>(a, &bc1, &bc2)) return;  // before any barrier or copy
+  using L = Tma4Tile<N>;
+  constexpr int S = L::kStages;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t bars[S];
+  long long n_tiles = 0;
+  for (int s = 0; s < a.nseg; ++s) n_tiles += a.seg[s].len / kTma4Tile;
+  const float clip = a.clip ? *a.clip : 1.0f;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  auto issue = [&](long long id, int stage) {  // thread 0 only
+    int si;
+    long long ti;
+    locate_tile4(a, id, &si, &ti);
+    const Seg& sg = a.seg[si];
+    unsigned char* st = smem + static_cast<size_t>(stage) * L::kStageBytes;
+    const long long e0 = ti * kTma4Tile;
+    if (!ZFS_CHECK(ti >= 0 && e0 + kTma4Tile <= sg.len && sg.base + e0 + kTma4Tile <= a.total_padded)) {
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[stage])) : "memory");
+      return;
+    }
+    mbar_expect_tx(&bars[stage], L::kStageBytes);
+    if (a.inject_missing_copy && id == 0) return;  // test hook: this tile's wait must run out
+    for (int r = 0; r < N; ++r)
+      bulk_load(st + r * L::kBytes, static_cast<const float*>(sg.g[r]) + e0, L::kBytes, &bars[stage]);
+    const long long j0 = sg.base + e0;
+    bulk_load(st + N * L::kBytes, a.master + j0, L::kBytes, &bars[stage]);
+    bulk_load(st + (N + 1) * L::kBytes, a.m + j0, L::kBytes, &bars[stage]);
+    bulk_load(st + (N + 2) * L::kBytes, a.v + j0, L::kBytes, &bars[stage]);
+  };
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      const long long id = blockIdx.x + static_cast<long long>(i) * gridDim.x;
+      if (id < n_tiles) issue(id, i);
+    }
+  }
+  long long gave_up_at = -1;
+  const int t4 = threadIdx.x * 4;
+  for (long long k = 0;; ++k) {
+    const long long id = blockIdx.x + k * gridDim.x;
+    if (id >= n_tiles) break;
+    const int stage = static_cast<int>(k % S);
+    const uint32_t parity = static_cast<uint32_t>((k / S) & 1);
+    const bool mine = !mbar_try_wait(&bars[stage], parity) && !wait_tile(&bars[stage], parity);
+    if (__syncthreads_or(mine ? 1 : 0)) {
+      gave_up_at = k;
+      if (threadIdx.x == 0) atomicAdd(&g_step_timeouts, 1u);
+      break;
+    }
+    const unsigned char* st = smem + static_cast<size_t>(stage) * L::kStageBytes;
+    float4 g = *reinterpret_cast<const float4*>(st + t4 * 4);
+#pragma unroll
+    for (int r = 1; r < N; ++r) {
+      const float4 x = *reinterpret_cast<const float4*>(st + r * L::kBytes + t4 * 4);
+      g.x = __fadd_rn(g.x, x.x); g.y = __fadd_rn(g.y, x.y); g.z = __fadd_rn(g.z, x.z); g.w = __fadd_rn(g.w, x.w);
+    }
+    const float4 w4 = *reinterpret_cast<const float4*>(st + N * L::kBytes + t4 * 4);
+    const float4 m4 = *reinterpret_cast<const float4*>(st + (N + 1) * L::kBytes + t4 * 4);
+    const float4 v4 = *reinterpret_cast<const float4*>(st + (N + 2) * L::kBytes + t4 * 4);
+    __syncthreads();  // every thread holds its operands: the stage can be refilled
+    if (threadIdx.x == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      const long long next = id + static_cast<long long>(S) * gridDim.x;
+      if (next < n_tiles) issue(next, stage);
+    }
+    float gg[4] = {g.x, g.y, g.z, g.w};
+    float w[4] = {w4.x, w4.y, w4.z, w4.w}, m[4] = {m4.x, m4.y, m4.z, m4.w}, v[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) adam(a, bc1, bc2, __fmul_rn(__fmul_rn(gg[e], a.inv_n), clip), w[e], m[e], v[e]);
+    int si;
+    long long ti;
+    locate_tile4(a, id, &si, &ti);
+    if (!ZFS_CHECK((ti + 1) * kTma4Tile <= a.seg[si].len && a.seg[si].base + (ti + 1) * kTma4Tile <= a.total_padded)) {
+      continue;
+    }
+    const long long j = a.seg[si].base + ti * kTma4Tile + t4;
+    st_stream_f4(a.master + j, make_float4(w[0], w[1], w[2], w[3]));
+    st_stream_f4(a.m + j, make_float4(m[0], m[1], m[2], m[3]));
+    st_stream_f4(a.v + j, make_float4(v[0], v[1], v[2], v[3]));
+    uint2 out;
+    out.x = pack_bf16x2(w[0], w[1]);
+    out.y = pack_bf16x2(w[2], w[3]);
+    __stcs(reinterpret_cast<uint2*>(a.p16 + j), out);
+  }
+  if (gave_up_at >= 0) {
+    for (long long jj = gave_up_at; jj < gave_up_at + S; ++jj) {
+      if (blockIdx.x + jj * gridDim.x >= n_tiles) break;
+      const int s = static_cast<int>(jj % S);
+      const uint32_t parity = static_cast<uint32_t>((jj / S) & 1);
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try_wait(&bars[s], parity) && global_ns() - t0 < kTmaDrainNs) {
+      }
+    }
+    return;
+  }
+  // The part of each segment after its last full tile, element by element.
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (int s = 0; s < a.nseg; ++s) {
+    const Seg& sg = a.seg[s];
+    for (long long k = (sg.len / kTma4Tile) * kTma4Tile + tid; k < sg.len; k += stride) {
+      step_scalar_element(a, sg, k, clip, bc1, bc2);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Scalar kernel: one element per thread-iteration, any alignment, any N.
 // ---------------------------------------------------------------------------
 template <bool kDevBias>
@@ -511,6 +659,7 @@ struct DeviceInfo {
   int vec_blocks_per_sm[2][2][kMaxRanks + 1] = {};
   int scalar_blocks_per_sm[2] = {};
   int tma_smem_set[2][2][kMaxRanks + 1] = {};
+  int tma4_smem_set[2][kMaxRanks + 1] = {};
 };
 
 // Shared memory of one SM usable by CTAs, and what each CTA reserves.
@@ -597,6 +746,28 @@ cudaError_t launch_tma(const StepArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int N, bool kDevBias>
+cudaError_t launch_tma4(const StepArgs& a, cudaStream_t stream) {
+  constexpr uint32_t kSmem = Tma4Tile<N>::kSmemBytes;
+  static_assert(kSmem + 128 <= 227 * 1024, "staged tiles must fit one CTA's shared memory (227 KB)");
+  const int dev = current_device();
+  {
+    std::lock_guard<std::mutex> lock(g_info_mutex);
+    int& done = g_info[dev].tma4_smem_set[kDevBias ? 1 : 0][N];
+    if (!done) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(step_tma4_kernel<N, kDevBias>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      if (e != cudaSuccess) return e;
+      done = 1;
+    }
+  }
+  int per_sm = static_cast<int>(kMaxSmemPerSm / (kSmem + kSmemReservedPerCta));
+  if (per_sm < 1) per_sm = 1;
+  if (per_sm > kTma4CtasPerSm) per_sm = kTma4CtasPerSm;
+  step_tma4_kernel<N, kDevBias><<<static_cast<unsigned>(cached_sms(dev) * per_sm), kStepThreads, kSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
 // The staged kernel where it measured faster and its tiles fit in shared memory.
 template <bool kDevBias>
 cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launched) {
@@ -615,6 +786,13 @@ cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launche
     switch (a.n_ranks) {
       case 8: return launch_tma<8, true, kDevBias>(a, stream);
       case 9: return launch_tma<9, true, kDevBias>(a, stream);
+      case 10: return launch_tma4<10, kDevBias>(a, stream);
+      case 11: return launch_tma4<11, kDevBias>(a, stream);
+      case 12: return launch_tma4<12, kDevBias>(a, stream);
+      case 13: return launch_tma4<13, kDevBias>(a, stream);
+      case 14: return launch_tma4<14, kDevBias>(a, stream);
+      case 15: return launch_tma4<15, kDevBias>(a, stream);
+      case 16: return launch_tma4<16, kDevBias>(a, stream);
       default: break;
     }
   }
