@@ -524,7 +524,9 @@ zero_status zero_step_count(const zero_ctx* ctx, int64_t* t);
  */
 zero_status zero_last_launches(const zero_ctx* ctx, int32_t* launches);
 
-/* Set the learning rate used by later steps (a scheduler's lr update). */
+/* Set the learning rate used by later steps (a scheduler's lr update).  A
+ * step already captured into a CUDA graph keeps the lr (and the AdamW factor
+ * 1 - lr*wd) it was captured with: capture it again after a change. */
 zero_status zero_set_lr(zero_ctx* ctx, float lr);
 
 /* Release the context's host metadata.  Device buffers stay the caller's. */

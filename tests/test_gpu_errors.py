@@ -107,6 +107,11 @@ def test_stage3_gather_argument_checks():
         assert _status(lambda: fs.gather_weights(0, None)) == B.ZERO_EINVAL
         buf = torch.empty(4224 + 1, dtype=torch.bfloat16, device="cuda")
         assert _status(lambda: B.zero_gather_weights(fs.ctx, 0, buf.data_ptr() + 1, 0)) == B.ZERO_EINVAL
+        # the runner refuses a buffer shorter than the padded unit, or not bf16
+        with pytest.raises(ValueError, match="padded"):
+            fs.gather_weights(0, buf[2:])
+        with pytest.raises(ValueError, match="bf16"):
+            fs.gather_weights(0, torch.empty(4224, dtype=torch.float32, device="cuda"))
         # unaligned (2-byte) destination works through the element-wise copy
         fs.gather_weights(0, buf[1:])
         torch.cuda.synchronize()

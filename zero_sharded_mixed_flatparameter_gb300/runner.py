@@ -44,7 +44,8 @@ class FlatStep:
             B.zero_destroy(plan)
         # Optional guard regions around every buffer (canary checks in tests);
         # a multiple of 8 elements keeps the interior 16-byte aligned.
-        assert guard % 8 == 0
+        if guard < 0 or guard % 8:
+            raise ValueError("guard must be a non-negative multiple of 8 elements")
         self.guard = guard
         n = self.padded + 2 * guard
 
@@ -191,6 +192,14 @@ class FlatStep:
             B.zero_step(self.ctx, self.stream_handle(stream))
 
     def gather_weights(self, unit: int, out: Optional[torch.Tensor], stream=None) -> None:
+        """ZeRO-3: copy unit `unit` (-1: every unit) of the bf16 parameters,
+        pads included, into `out`; a no-op for stages 0-2 (out may be None)."""
+        if out is not None and self.stage == 3:
+            need = self._need(unit)
+            if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.device != self.device:
+                raise ValueError("the gather buffer must be a contiguous bf16 device tensor")
+            if out.numel() < need:
+                raise ValueError(f"the gather buffer must hold the padded {need} elements, got {out.numel()}")
         B.zero_gather_weights(self.ctx, unit, out.data_ptr() if out is not None else 0, self.stream_handle(stream))
 
     def post_step(self, stream=None) -> None:
