@@ -224,10 +224,16 @@ def zero_param_offset(ctx: int, param: int) -> int:
     return off.value
 
 
+MAX_RANKS = 16  # the library's upper bound on n_ranks
+
+
 def zero_state_bytes(ctx: int, stage: int, n_ranks: int):
-    out = (ctypes.c_int64 * n_ranks)()
+    """Per-rank bytes of `stage` for the context's n_ranks ranks (n_ranks is
+    the context's; the library writes that many entries, so the array has
+    room for the largest n_ranks whatever the caller passes)."""
+    out = (ctypes.c_int64 * MAX_RANKS)()
     _check(load().zero_state_bytes(ctx, stage, out), ctx)
-    return list(out)
+    return list(out)[:n_ranks]
 
 
 def zero_stage3_peak_bytes(ctx: int):
