@@ -60,9 +60,10 @@ def test_inactive_clip_equals_no_clip():
     fs_plain.close()
 
 
-@pytest.mark.parametrize("n,gd", [(5, "fp32"), (16, "bf16"), (3, "bf16")])
+@pytest.mark.parametrize("n,gd", [(5, "fp32"), (16, "bf16"), (3, "bf16"), (6, "fp32"), (7, "fp32"), (12, "fp32")])
 def test_odd_layouts_clipped(n, gd):
-    # units straddling chunk boundaries, an exact multiple of the chunk, empty units
+    # units straddling chunk boundaries, an exact multiple of the chunk, empty
+    # units; fp32 from 7 replicas on loads one group at a time
     pl = si.from_units([16384 * 2, 16384 + 1, 0, 7, 16384 * 3 - 5, 33])
     pb = make_problem(pl, n, 3, grad_dtype=gd, steps=3, seed=43 + n, max_norm=0.1)
     _clip_parity(pb, mode="separate")

@@ -162,9 +162,26 @@ __device__ __forceinline__ void keep8(const NormSeg& s, long long e0, const floa
 // element-wise paths visit elements in the same order, so the chunk's sum does
 // not depend on the gradients' alignment.  Full groups are loaded two at a
 // time before either is accumulated (more bytes in flight per thread; the
-// loose register bound allows it), which does not change the order.
+// loose register bound allows it), which does not change the order — except
+// for fp32 gradients from kNormPairMaxRanksFp32 + 1 replicas on: two groups'
+// loads then need more than 128 registers, which leaves one CTA per SM, so
+// those instances load one group at a time at three CTAs per SM (measured on
+// GB300 over 73.5 M elements, GB/s of gradient reads: N = 7 fp32 6988-7012
+// against 6328, N = 8 7054 against 6423, N = 16 7211-7228 against 7122; at
+// N = 5, 6 either way within 1 %; the norm bits are the same, as the order
+// is).
+constexpr int kNormPairMaxRanksFp32 = 6;
+
 template <int N, bool kFp32>
-__global__ void __launch_bounds__(kStepThreads, 1) grad_sq_kernel(const __grid_constant__ NormArgs a) {
+struct NormShape {
+  static constexpr bool kPairs = !kFp32 || N <= kNormPairMaxRanksFp32;
+  static constexpr int kMinBlocks = kPairs ? 1 : 3;
+};
+
+template <int N, bool kFp32>
+__global__ void __launch_bounds__(kStepThreads, NormShape<N, kFp32>::kMinBlocks)
+    grad_sq_kernel(const __grid_constant__ NormArgs a) {
+  constexpr bool kPairs = NormShape<N, kFp32>::kPairs;
   __shared__ double smem[kStepThreads / 32];
   const long long b = blockIdx.x;
   int si = 0;
@@ -177,7 +194,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) grad_sq_kernel(const __grid_c
   const long long len = ZFS_CHECK(k >= 0 && k < s.n_chunks && c1 <= s.len) ? c1 - c0 : 0;
   SqAcc acc;
   long long grp = threadIdx.x;
-  for (; s.vec_ok && (grp + kStepThreads) * kVec + kVec <= len; grp += 2 * kStepThreads) {
+  for (; kPairs && s.vec_ok && (grp + kStepThreads) * kVec + kVec <= len; grp += 2 * kStepThreads) {
     float g0[kVec], g1[kVec];
     reduced8<N, kFp32>(a, s, c0 + grp * kVec, g0);
     reduced8<N, kFp32>(a, s, c0 + (grp + kStepThreads) * kVec, g1);
