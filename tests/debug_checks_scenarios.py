@@ -40,6 +40,8 @@ def main():
     scenario("tile-staged N = 9 fp32", make_problem(big, 9, 3, grad_dtype="fp32", steps=1, seed=213), mode="all")
     scenario("tile-staged N = 12 fp32 (1,024-element tiles)",
              make_problem(big, 12, 2, grad_dtype="fp32", steps=1, seed=218), mode="separate")
+    scenario("tile-staged N = 2 bf16 (4 elements per thread)", make_problem(big, 2, 3, steps=1, seed=219),
+             mode="separate")
     scenario("clipped N = 8", make_problem(odd, 8, 2, steps=2, seed=214, max_norm=0.05))
     scenario("clipped, reduced gradient kept", make_problem(odd, 8, 1, steps=2, seed=215, max_norm=0.05),
              clip_keep=True)

@@ -33,6 +33,8 @@ def _refs(pb):
     ("tile-staged N = 16", si.from_units([4_200_005, 2_000_000, 2_300_003]), 16, 2, "bf16", 0.0, False),
     ("fp32 N = 9 staged, clipped", si.from_units([4_200_005, 4_300_003]), 9, 1, "fp32", 0.5, False),
     ("fp32 N = 12 staged, 1,024-element tiles", si.from_units([4_200_005, 4_300_003]), 12, 2, "fp32", 0.0, False),
+    ("bf16 N = 2 staged, 4 elements per thread, clipped", si.from_units([4_200_005, 4_300_003]), 2, 3, "bf16", 0.5,
+     False),
 ])
 def test_capturable_mode_matches_oracle(name, pl, n, stage, gd, max_norm, keep):
     steps = 3

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
 // ---------------------------------------------------------------------------
 // Staged kernel for many replicas: TMA (1-D bulk copy) of whole tiles.
 //
-// With N >= kTmaMinRanks bf16 replicas (N = 8 or 9 fp32) the step is
+// With N >= 11 bf16 replicas (N = 8 or 9 fp32) the step is
 // read-heavy and has 3 + N input streams.  Here one thread per CTA moves each
 // kTmaTile-element tile of every input stream into shared memory with one
 // cp.async.bulk per stream (4-8 KB contiguous requests), completing on an
@@ -188,7 +188,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
 // 6770 / 6645, N = 12 6942 / 6640, N = 13 7059 / 6653, N = 14 7178 / 6645,
 // N = 16 7200 / 6618; fp32 N = 8 7164 / 6651, N = 9 7190 / 6634.  At bf16
 // N <= 10 (N = 8: 6143 / 6806), fp32 N = 7 and fp32 N >= 10 the
-// register-staged kernel is as fast or faster, so it stays the default there;
+// register-staged kernel is as fast or faster than this kernel (fp32 N >= 10
+// and bf16 N = 1, 2 have their own staged shape, step_tma4_kernel);
 // so it does for launches of fewer than kTmaMinElems elements, where one CTA
 // per SM works through too few tiles to hide the latency of each (N = 16
 // bf16: 2363 / 3152 GB/s at 1 M elements, 5481 / 5479 at 6 M, 6179 / 5962
@@ -466,38 +467,40 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
 // on (7,133-7,179 GB/s; three stages 6,651-6,949), against 6,800-6,889 GB/s
 // for the register-staged kernel at N = 10..16.
 // ---------------------------------------------------------------------------
-constexpr long long kTma4Tile = kStepThreads * 4;
-constexpr int kTma4CtasPerSm = 1;
-
-template <int N>
+// Tile geometry: kThreads threads x 4 elements per tile, kStages tiles in
+// flight per CTA.
+template <int N, bool kFp32, int kThreads, int kStages>
 struct Tma4Tile {
-  static constexpr uint32_t kBytes = kTma4Tile * 4;  // every stream is fp32
-  static constexpr uint32_t kStageBytes = (N + 3) * kBytes;
-  static constexpr int kStages = N <= 11 ? 3 : 2;
+  static constexpr long long kElems = kThreads * 4;
+  static constexpr uint32_t kGradBytes = kElems * (kFp32 ? 4 : 2);
+  static constexpr uint32_t kStateBytes = kElems * 4;
+  static constexpr uint32_t kStageBytes = N * kGradBytes + 3 * kStateBytes;
   static constexpr uint32_t kSmemBytes = kStageBytes * kStages;
 };
 
-// Full kTma4Tile-element tiles of a launch, segment after segment.
+// Full kElems-element tiles of a launch, segment after segment.
+template <long long kElems>
 __device__ __forceinline__ void locate_tile4(const StepArgs& a, long long id, int* si, long long* ti) {
   int s = 0;
-  while (id >= a.seg[s].len / kTma4Tile) {
-    id -= a.seg[s].len / kTma4Tile;
+  while (id >= a.seg[s].len / kElems) {
+    id -= a.seg[s].len / kElems;
     ++s;
   }
   *si = s;
   *ti = id;
 }
 
-template <int N, bool kDevBias>
-__global__ void __launch_bounds__(kStepThreads, 1) step_tma4_kernel(const __grid_constant__ StepArgs a) {
+template <int N, bool kFp32, int kThreads, int kStages, bool kDevBias>
+__global__ void __launch_bounds__(kThreads, 1) step_tma4_kernel(const __grid_constant__ StepArgs a) {
   float bc1, bc2;
   if (!step_bias<kDevBias>(a, &bc1, &bc2)) return;  // before any barrier or copy
-  using L = Tma4Tile<N>;
-  constexpr int S = L::kStages;
+  using L = Tma4Tile<N, kFp32, kThreads, kStages>;
+  constexpr int S = kStages;
+  constexpr long long T = L::kElems;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t bars[S];
   long long n_tiles = 0;
-  for (int s = 0; s < a.nseg; ++s) n_tiles += a.seg[s].len / kTma4Tile;
+  for (int s = 0; s < a.nseg; ++s) n_tiles += a.seg[s].len / T;
   const float clip = a.clip ? *a.clip : 1.0f;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -507,22 +510,24 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma4_kernel(const __grid
   auto issue = [&](long long id, int stage) {  // thread 0 only
     int si;
     long long ti;
-    locate_tile4(a, id, &si, &ti);
+    locate_tile4<T>(a, id, &si, &ti);
     const Seg& sg = a.seg[si];
     unsigned char* st = smem + static_cast<size_t>(stage) * L::kStageBytes;
-    const long long e0 = ti * kTma4Tile;
-    if (!ZFS_CHECK(ti >= 0 && e0 + kTma4Tile <= sg.len && sg.base + e0 + kTma4Tile <= a.total_padded)) {
+    const long long e0 = ti * T;
+    if (!ZFS_CHECK(ti >= 0 && e0 + T <= sg.len && sg.base + e0 + T <= a.total_padded)) {
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[stage])) : "memory");
       return;
     }
     mbar_expect_tx(&bars[stage], L::kStageBytes);
     if (a.inject_missing_copy && id == 0) return;  // test hook: this tile's wait must run out
     for (int r = 0; r < N; ++r)
-      bulk_load(st + r * L::kBytes, static_cast<const float*>(sg.g[r]) + e0, L::kBytes, &bars[stage]);
+      bulk_load(st + r * L::kGradBytes, static_cast<const unsigned char*>(sg.g[r]) + e0 * (kFp32 ? 4 : 2),
+                L::kGradBytes, &bars[stage]);
     const long long j0 = sg.base + e0;
-    bulk_load(st + N * L::kBytes, a.master + j0, L::kBytes, &bars[stage]);
-    bulk_load(st + (N + 1) * L::kBytes, a.m + j0, L::kBytes, &bars[stage]);
-    bulk_load(st + (N + 2) * L::kBytes, a.v + j0, L::kBytes, &bars[stage]);
+    unsigned char* st_state = st + N * L::kGradBytes;
+    bulk_load(st_state, a.master + j0, L::kStateBytes, &bars[stage]);
+    bulk_load(st_state + L::kStateBytes, a.m + j0, L::kStateBytes, &bars[stage]);
+    bulk_load(st_state + 2 * L::kStateBytes, a.v + j0, L::kStateBytes, &bars[stage]);
   };
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -544,32 +549,46 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma4_kernel(const __grid
       break;
     }
     const unsigned char* st = smem + static_cast<size_t>(stage) * L::kStageBytes;
-    float4 g = *reinterpret_cast<const float4*>(st + t4 * 4);
+    float gg[4];
+    if constexpr (kFp32) {
+      const float4 x0 = *reinterpret_cast<const float4*>(st + t4 * 4);
+      gg[0] = x0.x; gg[1] = x0.y; gg[2] = x0.z; gg[3] = x0.w;
 #pragma unroll
-    for (int r = 1; r < N; ++r) {
-      const float4 x = *reinterpret_cast<const float4*>(st + r * L::kBytes + t4 * 4);
-      g.x = __fadd_rn(g.x, x.x); g.y = __fadd_rn(g.y, x.y); g.z = __fadd_rn(g.z, x.z); g.w = __fadd_rn(g.w, x.w);
+      for (int r = 1; r < N; ++r) {
+        const float4 x = *reinterpret_cast<const float4*>(st + r * L::kGradBytes + t4 * 4);
+        gg[0] = __fadd_rn(gg[0], x.x); gg[1] = __fadd_rn(gg[1], x.y);
+        gg[2] = __fadd_rn(gg[2], x.z); gg[3] = __fadd_rn(gg[3], x.w);
+      }
+    } else {
+      const uint2 x0 = *reinterpret_cast<const uint2*>(st + t4 * 2);
+      gg[0] = bf16_lo(x0.x); gg[1] = bf16_hi(x0.x); gg[2] = bf16_lo(x0.y); gg[3] = bf16_hi(x0.y);
+#pragma unroll
+      for (int r = 1; r < N; ++r) {
+        const uint2 x = *reinterpret_cast<const uint2*>(st + r * L::kGradBytes + t4 * 2);
+        gg[0] = __fadd_rn(gg[0], bf16_lo(x.x)); gg[1] = __fadd_rn(gg[1], bf16_hi(x.x));
+        gg[2] = __fadd_rn(gg[2], bf16_lo(x.y)); gg[3] = __fadd_rn(gg[3], bf16_hi(x.y));
+      }
     }
-    const float4 w4 = *reinterpret_cast<const float4*>(st + N * L::kBytes + t4 * 4);
-    const float4 m4 = *reinterpret_cast<const float4*>(st + (N + 1) * L::kBytes + t4 * 4);
-    const float4 v4 = *reinterpret_cast<const float4*>(st + (N + 2) * L::kBytes + t4 * 4);
+    const unsigned char* st_state = st + N * L::kGradBytes;
+    const float4 w4 = *reinterpret_cast<const float4*>(st_state + t4 * 4);
+    const float4 m4 = *reinterpret_cast<const float4*>(st_state + L::kStateBytes + t4 * 4);
+    const float4 v4 = *reinterpret_cast<const float4*>(st_state + 2 * L::kStateBytes + t4 * 4);
     __syncthreads();  // every thread holds its operands: the stage can be refilled
     if (threadIdx.x == 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       const long long next = id + static_cast<long long>(S) * gridDim.x;
       if (next < n_tiles) issue(next, stage);
     }
-    float gg[4] = {g.x, g.y, g.z, g.w};
     float w[4] = {w4.x, w4.y, w4.z, w4.w}, m[4] = {m4.x, m4.y, m4.z, m4.w}, v[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) adam(a, bc1, bc2, __fmul_rn(__fmul_rn(gg[e], a.inv_n), clip), w[e], m[e], v[e]);
     int si;
     long long ti;
-    locate_tile4(a, id, &si, &ti);
-    if (!ZFS_CHECK((ti + 1) * kTma4Tile <= a.seg[si].len && a.seg[si].base + (ti + 1) * kTma4Tile <= a.total_padded)) {
+    locate_tile4<T>(a, id, &si, &ti);
+    if (!ZFS_CHECK((ti + 1) * T <= a.seg[si].len && a.seg[si].base + (ti + 1) * T <= a.total_padded)) {
       continue;
     }
-    const long long j = a.seg[si].base + ti * kTma4Tile + t4;
+    const long long j = a.seg[si].base + ti * T + t4;
     st_stream_f4(a.master + j, make_float4(w[0], w[1], w[2], w[3]));
     st_stream_f4(a.m + j, make_float4(m[0], m[1], m[2], m[3]));
     st_stream_f4(a.v + j, make_float4(v[0], v[1], v[2], v[3]));
@@ -594,7 +613,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma4_kernel(const __grid
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (int s = 0; s < a.nseg; ++s) {
     const Seg& sg = a.seg[s];
-    for (long long k = (sg.len / kTma4Tile) * kTma4Tile + tid; k < sg.len; k += stride) {
+    for (long long k = (sg.len / T) * T + tid; k < sg.len; k += stride) {
       step_scalar_element(a, sg, k, clip, bc1, bc2);
     }
   }
@@ -653,13 +672,16 @@ StepKernel vec_kernel_for(int n) {
 
 constexpr int kMaxDevices = 64;
 
+constexpr int kMaxSmemKernels = 128;
+
 struct DeviceInfo {
   int sms = 0;
   // [device-side bias][fp32 gradients][N]
   int vec_blocks_per_sm[2][2][kMaxRanks + 1] = {};
   int scalar_blocks_per_sm[2] = {};
-  int tma_smem_set[2][2][kMaxRanks + 1] = {};
-  int tma4_smem_set[2][kMaxRanks + 1] = {};
+  // Staged kernels whose dynamic shared memory limit is raised on the device.
+  const void* smem_set[kMaxSmemKernels] = {};
+  int n_smem_set = 0;
 };
 
 // Shared memory of one SM usable by CTAs, and what each CTA reserves.
@@ -668,6 +690,22 @@ constexpr long long kSmemReservedPerCta = 1024;
 
 std::mutex g_info_mutex;
 DeviceInfo g_info[kMaxDevices];
+
+// Raises `fn`'s dynamic shared memory limit to `bytes` once per device.  The
+// record lives in this file's tables (internal linkage), not in statics of
+// the launch templates: those would be one object process-wide, shared with
+// any other copy of the library loaded alongside, which then would skip the
+// call for its own kernels.
+cudaError_t ensure_smem(int dev, const void* fn, uint32_t bytes) {
+  std::lock_guard<std::mutex> lock(g_info_mutex);
+  DeviceInfo& d = g_info[dev];
+  for (int i = 0; i < d.n_smem_set; ++i)
+    if (d.smem_set[i] == fn) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  if (d.n_smem_set < kMaxSmemKernels) d.smem_set[d.n_smem_set++] = fn;
+  return cudaSuccess;
+}
 
 int current_device() {
   int dev = 0;
@@ -728,16 +766,8 @@ cudaError_t launch_tma(const StepArgs& a, cudaStream_t stream) {
   constexpr uint32_t kSmem = TmaTile<N, kFp32>::kSmemBytes;
   static_assert(kSmem + 128 <= 227 * 1024, "staged tiles must fit one CTA's shared memory (227 KB)");
   const int dev = current_device();
-  {
-    std::lock_guard<std::mutex> lock(g_info_mutex);
-    int& done = g_info[dev].tma_smem_set[kDevBias ? 1 : 0][kFp32 ? 1 : 0][N];
-    if (!done) {
-      const cudaError_t e = cudaFuncSetAttribute(step_tma_kernel<N, kFp32, kDevBias>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-      if (e != cudaSuccess) return e;
-      done = 1;
-    }
-  }
+  const cudaError_t e = ensure_smem(dev, reinterpret_cast<const void*>(step_tma_kernel<N, kFp32, kDevBias>), kSmem);
+  if (e != cudaSuccess) return e;
   int per_sm = static_cast<int>(kMaxSmemPerSm / (kSmem + kSmemReservedPerCta));
   if (per_sm < 1) per_sm = 1;
   if (per_sm > kStepCtasPerSm) per_sm = kStepCtasPerSm;
@@ -746,34 +776,48 @@ cudaError_t launch_tma(const StepArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int N, bool kDevBias>
+template <int N, bool kFp32, int kThreads, int kStages, int kCtasPerSm, bool kDevBias>
 cudaError_t launch_tma4(const StepArgs& a, cudaStream_t stream) {
-  constexpr uint32_t kSmem = Tma4Tile<N>::kSmemBytes;
+  constexpr uint32_t kSmem = Tma4Tile<N, kFp32, kThreads, kStages>::kSmemBytes;
   static_assert(kSmem + 128 <= 227 * 1024, "staged tiles must fit one CTA's shared memory (227 KB)");
+  auto kernel = step_tma4_kernel<N, kFp32, kThreads, kStages, kDevBias>;
   const int dev = current_device();
-  {
-    std::lock_guard<std::mutex> lock(g_info_mutex);
-    int& done = g_info[dev].tma4_smem_set[kDevBias ? 1 : 0][N];
-    if (!done) {
-      const cudaError_t e =
-          cudaFuncSetAttribute(step_tma4_kernel<N, kDevBias>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-      if (e != cudaSuccess) return e;
-      done = 1;
-    }
-  }
+  const cudaError_t e = ensure_smem(dev, reinterpret_cast<const void*>(kernel), kSmem);
+  if (e != cudaSuccess) return e;
   int per_sm = static_cast<int>(kMaxSmemPerSm / (kSmem + kSmemReservedPerCta));
   if (per_sm < 1) per_sm = 1;
-  if (per_sm > kTma4CtasPerSm) per_sm = kTma4CtasPerSm;
-  step_tma4_kernel<N, kDevBias><<<static_cast<unsigned>(cached_sms(dev) * per_sm), kStepThreads, kSmem, stream>>>(a);
+  if (per_sm > kCtasPerSm) per_sm = kCtasPerSm;
+  kernel<<<static_cast<unsigned>(cached_sms(dev) * per_sm), kThreads, kSmem, stream>>>(a);
   return cudaGetLastError();
 }
 
-// The staged kernel where it measured faster and its tiles fit in shared memory.
+// fp32 replicas from N = 10: 256 threads (1,024-element tiles), three stages
+// at N = 10, 11 and two from N = 12 (measured, see step_tma4_kernel).
+template <int N, bool kDevBias>
+cudaError_t launch_tma4_fp32(const StepArgs& a, cudaStream_t stream) {
+  return launch_tma4<N, true, kStepThreads, (N <= 11 ? 3 : 2), 1, kDevBias>(a, stream);
+}
+
+// bf16 replicas at N = 1, 2: 256 threads, two stages, two CTAs per SM.
+// Measured on GB300 over 100 M elements: N = 1 6607 GB/s, N = 2 6557,
+// against 6332 and 6344 for the register-staged kernel; from N = 4 on the
+// register-staged kernel is as fast or faster (N = 4: 6658-6807 staged in
+// the shapes tried, 6698; N = 8: 6394-6599 against 6773).
+template <int N, bool kDevBias>
+cudaError_t launch_tma4_bf16(const StepArgs& a, cudaStream_t stream) {
+  return launch_tma4<N, false, kStepThreads, 2, 2, kDevBias>(a, stream);
+}
+
+// A staged kernel where one measured faster than the register-staged kernel
+// (launches of at least kTmaMinElems elements): bf16 N = 1, 2 and N >= 11,
+// fp32 N >= 8.  Other rank counts return with *launched = false.
 template <bool kDevBias>
 cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launched) {
   *launched = true;
   if (!a.grad_fp32) {
     switch (a.n_ranks) {
+      case 1: return launch_tma4_bf16<1, kDevBias>(a, stream);
+      case 2: return launch_tma4_bf16<2, kDevBias>(a, stream);
       case 11: return launch_tma<11, false, kDevBias>(a, stream);
       case 12: return launch_tma<12, false, kDevBias>(a, stream);
       case 13: return launch_tma<13, false, kDevBias>(a, stream);
@@ -786,13 +830,13 @@ cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launche
     switch (a.n_ranks) {
       case 8: return launch_tma<8, true, kDevBias>(a, stream);
       case 9: return launch_tma<9, true, kDevBias>(a, stream);
-      case 10: return launch_tma4<10, kDevBias>(a, stream);
-      case 11: return launch_tma4<11, kDevBias>(a, stream);
-      case 12: return launch_tma4<12, kDevBias>(a, stream);
-      case 13: return launch_tma4<13, kDevBias>(a, stream);
-      case 14: return launch_tma4<14, kDevBias>(a, stream);
-      case 15: return launch_tma4<15, kDevBias>(a, stream);
-      case 16: return launch_tma4<16, kDevBias>(a, stream);
+      case 10: return launch_tma4_fp32<10, kDevBias>(a, stream);
+      case 11: return launch_tma4_fp32<11, kDevBias>(a, stream);
+      case 12: return launch_tma4_fp32<12, kDevBias>(a, stream);
+      case 13: return launch_tma4_fp32<13, kDevBias>(a, stream);
+      case 14: return launch_tma4_fp32<14, kDevBias>(a, stream);
+      case 15: return launch_tma4_fp32<15, kDevBias>(a, stream);
+      case 16: return launch_tma4_fp32<16, kDevBias>(a, stream);
       default: break;
     }
   }
@@ -802,7 +846,7 @@ cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launche
 
 template <bool kDevBias>
 cudaError_t launch_step_vec_t(const StepArgs& a, cudaStream_t stream) {
-  if (a.total_elems >= kTmaMinElems && a.n_ranks >= (a.grad_fp32 ? kTmaMinRanksFp32 : kTmaMinRanks)) {
+  if (a.total_elems >= kTmaMinElems) {
     bool launched = false;
     const cudaError_t e = try_launch_tma<kDevBias>(a, stream, &launched);
     if (launched) return e;
