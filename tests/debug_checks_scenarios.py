@@ -42,6 +42,7 @@ def main():
              make_problem(big, 12, 2, grad_dtype="fp32", steps=1, seed=218), mode="separate")
     scenario("tile-staged N = 2 bf16 (4 elements per thread)", make_problem(big, 2, 3, steps=1, seed=219),
              mode="separate")
+    scenario("tile-staged N = 4 bf16 (512-thread CTAs)", make_problem(big, 4, 2, steps=1, seed=220), mode="all")
     scenario("clipped N = 8", make_problem(odd, 8, 2, steps=2, seed=214, max_norm=0.05))
     scenario("clipped, reduced gradient kept", make_problem(odd, 8, 1, steps=2, seed=215, max_norm=0.05),
              clip_keep=True)
@@ -73,7 +74,7 @@ def main():
     import numpy as np
     import torch
     from gpu_common import gpu_flatstep, to_np, upload_grads
-    pb = make_problem(si.toy_mlp(), 4, 2, steps=1, seed=220)
+    pb = make_problem(si.toy_mlp(), 4, 2, steps=1, seed=221)
     fs = gpu_flatstep(pb)
     before = tuple(to_np(x).copy() for x in (fs.master, fs.exp_avg, fs.exp_avg_sq, fs.param16))
     fs.reduce_grads(-1, upload_grads(pb, 1))

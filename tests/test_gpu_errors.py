@@ -125,8 +125,9 @@ def test_stage3_gather_argument_checks():
         fs.close()
 
 
-@pytest.mark.parametrize("n,gd,tile,ctas_per_sm", [(16, "bf16", 2048, 1), (12, "fp32", 1024, 1), (2, "bf16", 1024, 2)])
-def test_staged_wait_runs_out_and_the_device_stays_usable(n, gd, tile, ctas_per_sm):
+@pytest.mark.parametrize("n,gd,tile,ctas_per_sm,threads", [(16, "bf16", 2048, 1, 256), (12, "fp32", 1024, 1, 256),
+                                                            (2, "bf16", 1024, 2, 256), (4, "bf16", 2048, 1, 512)])
+def test_staged_wait_runs_out_and_the_device_stays_usable(n, gd, tile, ctas_per_sm, threads):
     # The tile-staged step kernel bounds every wait for its bulk copies.  The
     # test hook announces the launch's first tile to its mbarrier without
     # issuing the copy, so CTA 0's wait runs out (after ~1 s): it counts a
@@ -153,13 +154,13 @@ def test_staged_wait_runs_out_and_the_device_stays_usable(n, gd, tile, ctas_per_
         assert B.zero_kernel_timeouts(fs.ctx) == before + 1
         assert 0.5 < waited < 10.0, waited
         # CTA 0's elements: tiles 0, G, 2G, ... (G = the grid: SMs x CTAs per
-        # SM) and the first 256 elements after the last full tile
+        # SM) and the first `threads` elements after the last full tile
         grid = torch.cuda.get_device_properties(0).multi_processor_count * ctas_per_sm
         full = padded // tile
         mine = np.zeros(padded, bool)
         for tid in range(0, full, grid):
             mine[tid * tile:(tid + 1) * tile] = True
-        mine[full * tile:min(full * tile + 256, padded)] = True
+        mine[full * tile:min(full * tile + threads, padded)] = True
         ref = oracle_run(pb, steps=1)
         got = tuple(to_np(x) for x in (fs.master, fs.exp_avg, fs.exp_avg_sq, fs.param16))
         for name, g, r, i0 in zip(("master", "m", "v", "param16"), got, ref, init):

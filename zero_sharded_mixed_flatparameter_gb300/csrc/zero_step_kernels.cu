@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
 // N = 16 7200 / 6618; fp32 N = 8 7164 / 6651, N = 9 7190 / 6634.  At bf16
 // N <= 10 (N = 8: 6143 / 6806), fp32 N = 7 and fp32 N >= 10 the
 // register-staged kernel is as fast or faster than this kernel (fp32 N >= 10
-// and bf16 N = 1, 2 have their own staged shape, step_tma4_kernel);
+// and bf16 N = 1..4 have their own staged shapes, step_tma4_kernel);
 // so it does for launches of fewer than kTmaMinElems elements, where one CTA
 // per SM works through too few tiles to hide the latency of each (N = 16
 // bf16: 2363 / 3152 GB/s at 1 M elements, 5481 / 5479 at 6 M, 6179 / 5962
@@ -798,18 +798,23 @@ cudaError_t launch_tma4_fp32(const StepArgs& a, cudaStream_t stream) {
   return launch_tma4<N, true, kStepThreads, (N <= 11 ? 3 : 2), 1, kDevBias>(a, stream);
 }
 
-// bf16 replicas at N = 1, 2: 256 threads, two stages, two CTAs per SM.
-// Measured on GB300 over 100 M elements: N = 1 6607 GB/s, N = 2 6557,
-// against 6332 and 6344 for the register-staged kernel; from N = 4 on the
-// register-staged kernel is as fast or faster (N = 4: 6658-6807 staged in
-// the shapes tried, 6698; N = 8: 6394-6599 against 6773).
+// bf16 replicas at N = 1..4.  Measured on GB300 over 100 M elements (GB/s):
+// N = 1, 2 with 256 threads, two stages, two CTAs per SM: 6575-6623 and
+// 6542-6557 against 6317-6344 for the register-staged kernel; N = 3, 4 with
+// 512 threads, two stages, one CTA per SM: 6652-6680 and 6779-6807 against
+// 6568-6581 and 6671-6724.  From N = 5 on the register-staged kernel is as
+// fast or faster (N = 5: 6765 / 6778; N = 8: 6394-6599 / 6773).
 template <int N, bool kDevBias>
 cudaError_t launch_tma4_bf16(const StepArgs& a, cudaStream_t stream) {
-  return launch_tma4<N, false, kStepThreads, 2, 2, kDevBias>(a, stream);
+  if constexpr (N <= 2) {
+    return launch_tma4<N, false, kStepThreads, 2, 2, kDevBias>(a, stream);
+  } else {
+    return launch_tma4<N, false, 2 * kStepThreads, 2, 1, kDevBias>(a, stream);
+  }
 }
 
 // A staged kernel where one measured faster than the register-staged kernel
-// (launches of at least kTmaMinElems elements): bf16 N = 1, 2 and N >= 11,
+// (launches of at least kTmaMinElems elements): bf16 N = 1..4 and N >= 11,
 // fp32 N >= 8.  Other rank counts return with *launched = false.
 template <bool kDevBias>
 cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launched) {
@@ -818,6 +823,8 @@ cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launche
     switch (a.n_ranks) {
       case 1: return launch_tma4_bf16<1, kDevBias>(a, stream);
       case 2: return launch_tma4_bf16<2, kDevBias>(a, stream);
+      case 3: return launch_tma4_bf16<3, kDevBias>(a, stream);
+      case 4: return launch_tma4_bf16<4, kDevBias>(a, stream);
       case 11: return launch_tma<11, false, kDevBias>(a, stream);
       case 12: return launch_tma<12, false, kDevBias>(a, stream);
       case 13: return launch_tma<13, false, kDevBias>(a, stream);
