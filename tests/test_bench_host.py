@@ -1,0 +1,69 @@
+"""Host-side helpers of bench.py (no GPU): the kernel each workload's step
+takes (the roofline line names it), the algorithmic bytes per parameter,
+and the rule that the recorded DRAM traffic is reported only for the kernel
+sources it was taken on."""
+
+import os
+
+import pytest
+
+import bench
+
+
+@pytest.mark.parametrize("n,gd,keep,elems,want", [
+    (8, "bf16", False, 73_417_728, "step_vec_kernel"),        # the default workload
+    (8, "bf16", False, 2 ** 23 - 1, "step_vec_kernel"),
+    (1, "bf16", False, 2 ** 23, "step_tma4_kernel"),
+    (2, "bf16", False, 10 ** 9, "step_tma4_kernel"),
+    (4, "bf16", False, 10 ** 9, "step_tma4_kernel"),
+    (5, "bf16", False, 10 ** 9, "step_vec_kernel"),
+    (10, "bf16", False, 10 ** 9, "step_vec_kernel"),
+    (11, "bf16", False, 10 ** 9, "step_tma_kernel"),
+    (16, "bf16", False, 10 ** 9, "step_tma_kernel"),
+    (16, "bf16", False, 10 ** 6, "step_vec_kernel"),          # small launches stay register-staged
+    (2, "fp32", False, 2_030_174_208, "step_vec_kernel"),     # the stage-buffer workload
+    (7, "fp32", False, 10 ** 9, "step_vec_kernel"),
+    (8, "fp32", False, 10 ** 9, "step_tma_kernel"),
+    (9, "fp32", False, 10 ** 9, "step_tma_kernel"),
+    (10, "fp32", False, 10 ** 9, "step_tma4_kernel"),
+    (16, "fp32", False, 10 ** 9, "step_tma4_kernel"),
+    (16, "bf16", True, 10 ** 9, "step_vec_kernel"),           # kept reduced gradient: one fp32 replica
+])
+def test_step_kernel_name(n, gd, keep, elems, want):
+    assert bench.step_kernel_name(n, gd, keep, elems) == want
+
+
+def test_bytes_per_param():
+    assert bench.bytes_per_param(8, "bf16") == 42
+    assert bench.bytes_per_param(2, "fp32") == 34
+    assert bench.bytes_per_param(1, "bf16") == 28
+
+
+def test_workload_shapes():
+    wl = bench.workload("llama1024_zero2_n8")
+    assert (wl["n"], wl["stage"], wl["grad_dtype"]) == (8, 2, "bf16")
+    assert sum(wl["pl"].numel) == 73_417_728
+    wl = bench.workload("flat32:4e6:12")
+    assert (wl["n"], wl["stage"], wl["grad_dtype"], sum(wl["pl"].numel)) == (12, 1, "fp32", 4_000_000)
+    with pytest.raises(SystemExit):
+        bench.workload("no_such_workload")
+
+
+def test_traffic_only_for_the_recorded_sources(tmp_path, monkeypatch):
+    sha = bench.kernel_source_sha()
+    assert len(sha) == 16 and sha == bench.kernel_source_sha()
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "step_kernel_dram_traffic.txt").write_text(
+        "# comment\n"
+        f"workload=w1 kernel_sha={sha} dram_bytes_per_launch=123\n"
+        "workload=w2 kernel_sha=0000000000000000 dram_bytes_per_launch=456\n")
+    # the sources are read from the real tree, the record from the temporary one
+    real_root = bench.ROOT
+    monkeypatch.setattr(bench, "kernel_source_sha", lambda: sha)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("w1") == 123.0
+    assert bench.recorded_traffic("w2") is None          # taken on other sources
+    assert bench.recorded_traffic("w3") is None          # not recorded
+    monkeypatch.setattr(bench, "ROOT", real_root)
+    assert os.path.exists(os.path.join(real_root, "profiles", "step_kernel_dram_traffic.txt"))
