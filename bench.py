@@ -86,8 +86,9 @@ def measured_peaks():
 def step_kernel_name(n: int, grad_dtype: str, clip_keep: bool, elems: int) -> str:
     """The step kernel the library launches for this workload: over >= 2^23
     elements the tile-staged one with 2,048-element tiles for N >= 11 bf16 or
-    N = 8, 9 fp32 replicas and the one with 4 elements per thread for N >= 10
-    fp32 or N = 1..4 bf16 replicas; the register-staged one otherwise (a kept
+    N = 8, 9 fp32 replicas and the one with 4 elements per thread for N = 7
+    or N >= 10 fp32 or N = 1..4 bf16 replicas; the register-staged one
+    otherwise (a kept
     fp32 reduced gradient is one fp32 replica)."""
     if clip_keep:
         n, grad_dtype = 1, "fp32"
@@ -97,7 +98,7 @@ def step_kernel_name(n: int, grad_dtype: str, clip_keep: bool, elems: int) -> st
         if n <= 4:
             return "step_tma4_kernel"
         return "step_tma_kernel" if n >= 11 else "step_vec_kernel"
-    if n >= 10:
+    if n >= 10 or n == 7:
         return "step_tma4_kernel"
     return "step_tma_kernel" if n in (8, 9) else "step_vec_kernel"
 

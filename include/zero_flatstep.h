@@ -471,7 +471,7 @@ zero_status zero_cpu_adam(const zero_config* cfg, int64_t t, const float* grad, 
 
 /*
  * zero_kernel_timeouts — how many bounded waits of the tile-staged step
- * kernels (used for N = 1..4 or N >= 11 bf16 and N >= 8 fp32 replicas when a
+ * kernels (used for N = 1..4 or N >= 11 bf16 and N >= 7 fp32 replicas when a
  * launch covers at least 2^23 elements) gave up on the current device since
  * the library was loaded.  A wait gives up only if a
  * bulk copy never lands; the CTA then leaves the rest of its tiles unchanged,

@@ -22,7 +22,8 @@ import bench
     (16, "bf16", False, 10 ** 9, "step_tma_kernel"),
     (16, "bf16", False, 10 ** 6, "step_vec_kernel"),          # small launches stay register-staged
     (2, "fp32", False, 2_030_174_208, "step_vec_kernel"),     # the stage-buffer workload
-    (7, "fp32", False, 10 ** 9, "step_vec_kernel"),
+    (6, "fp32", False, 10 ** 9, "step_vec_kernel"),
+    (7, "fp32", False, 10 ** 9, "step_tma4_kernel"),
     (8, "fp32", False, 10 ** 9, "step_tma_kernel"),
     (9, "fp32", False, 10 ** 9, "step_tma_kernel"),
     (10, "fp32", False, 10 ** 9, "step_tma4_kernel"),

@@ -188,8 +188,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
 // 6770 / 6645, N = 12 6942 / 6640, N = 13 7059 / 6653, N = 14 7178 / 6645,
 // N = 16 7200 / 6618; fp32 N = 8 7164 / 6651, N = 9 7190 / 6634.  At bf16
 // N <= 10 (N = 8: 6143 / 6806), fp32 N = 7 and fp32 N >= 10 the
-// register-staged kernel is as fast or faster than this kernel (fp32 N >= 10
-// and bf16 N = 1..4 have their own staged shapes, step_tma4_kernel);
+// register-staged kernel is as fast or faster than this kernel (fp32 N = 7,
+// N >= 10 and bf16 N = 1..4 have their own staged shapes, step_tma4_kernel);
 // so it does for launches of fewer than kTmaMinElems elements, where one CTA
 // per SM works through too few tiles to hide the latency of each (N = 16
 // bf16: 2363 / 3152 GB/s at 1 M elements, 5481 / 5479 at 6 M, 6179 / 5962
@@ -792,10 +792,18 @@ cudaError_t launch_tma4(const StepArgs& a, cudaStream_t stream) {
 }
 
 // fp32 replicas from N = 10: 256 threads (1,024-element tiles), three stages
-// at N = 10, 11 and two from N = 12 (measured, see step_tma4_kernel).
+// at N = 10, 11 and two from N = 12 (measured, see step_tma4_kernel).  At
+// N = 7: 512 threads, two stages (100 M elements: 7038-7047 GB/s against
+// 6661-6673 for the register-staged kernel and 6678 for step_tma_kernel; at
+// N = 2, 4, 6 every staged shape tried was slower than the register-staged
+// kernel).
 template <int N, bool kDevBias>
 cudaError_t launch_tma4_fp32(const StepArgs& a, cudaStream_t stream) {
-  return launch_tma4<N, true, kStepThreads, (N <= 11 ? 3 : 2), 1, kDevBias>(a, stream);
+  if constexpr (N < 10) {
+    return launch_tma4<N, true, 2 * kStepThreads, 2, 1, kDevBias>(a, stream);
+  } else {
+    return launch_tma4<N, true, kStepThreads, (N <= 11 ? 3 : 2), 1, kDevBias>(a, stream);
+  }
 }
 
 // bf16 replicas at N = 1..4.  Measured on GB300 over 100 M elements (GB/s):
@@ -815,7 +823,7 @@ cudaError_t launch_tma4_bf16(const StepArgs& a, cudaStream_t stream) {
 
 // A staged kernel where one measured faster than the register-staged kernel
 // (launches of at least kTmaMinElems elements): bf16 N = 1..4 and N >= 11,
-// fp32 N >= 8.  Other rank counts return with *launched = false.
+// fp32 N >= 7.  Other rank counts return with *launched = false.
 template <bool kDevBias>
 cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launched) {
   *launched = true;
@@ -835,6 +843,7 @@ cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launche
     }
   } else {
     switch (a.n_ranks) {
+      case 7: return launch_tma4_fp32<7, kDevBias>(a, stream);
       case 8: return launch_tma<8, true, kDevBias>(a, stream);
       case 9: return launch_tma<9, true, kDevBias>(a, stream);
       case 10: return launch_tma4_fp32<10, kDevBias>(a, stream);
