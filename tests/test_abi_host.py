@@ -107,6 +107,19 @@ def test_zero3_peak_lecture_mlp(B):
         B.zero_destroy(ctx)
 
 
+def test_ledger_binding_with_fewer_ranks_than_the_context(B):
+    # The library writes one entry per rank of the context; the binding's
+    # array has room for the largest rank count whatever the caller asks for.
+    pl = si.lecture_mlp()
+    ctx = B.zero_plan(B.make_config(3, 16), pl.numel, pl.unit)
+    try:
+        full = B.zero_state_bytes(ctx, 2, 16)
+        assert len(full) == 16 and len(set(full)) == 1
+        assert B.zero_state_bytes(ctx, 2, 1) == full[:1]
+    finally:
+        B.zero_destroy(ctx)
+
+
 @pytest.mark.parametrize("field,value", [
     ("stage", 4), ("stage", -1), ("n_ranks", 0), ("n_ranks", 17), ("grad_dtype", 2), ("adamw", 2),
     ("beta1", 1.0), ("beta2", -0.1), ("eps", -1.0), ("lr", float("inf")), ("weight_decay", -0.1),
