@@ -1,4 +1,4 @@
-"""Failure detection of the C ABI on a GPU machine: every bad call returns a
+"""Failure detection of the C ABI on a GPU: every bad call returns a
 status (never a fault) and leaves the context unchanged; the failures are
 made on the host (bad pointers, wrong order of calls).  The one device-side
 failure tested is a bounded wait that runs out because the test hook never
