@@ -6,11 +6,14 @@ reduce_grads (registration of the N replica gradients) -> zero_step (the fused
 rank-order fp32 reduce, Adam, bf16 cast) -> gather_weights (ZeRO-3 per-unit
 copies; nothing to do for stages 0-2) -> post_step.
 
-Default workload: Llama-style model, hidden 1024, intermediate 2048, 16/4
-heads, 8 layers, vocab 1024 (73,417,728 params) flattened into one
-FlatParameter, N = 8 simulated ranks, ZeRO-2, bf16 gradients ~N(0, 1e-3),
-fp32 Adam.  Every step moves (2N + 26) B/param = 3.08 GB, well above the
-129 MB L2, so no flush is needed between steps.
+Default workload: the pipeline-stage-sized buffer of the Llama-style model
+with hidden 2048, intermediate 8192, 32/8 heads, vocab 40960 — 32 decoder
+layers plus the input embedding, 2,030,174,208 params in one FlatParameter —
+with N = 2 simulated ranks, ZeRO-1, fp32 gradients ~N(0, 1e-3) and fp32 Adam:
+(4N + 26) = 34 B/param, 69 GB per step, far above the 129 MB L2 (no flush
+is needed between steps).  The same line carries a clipped leg on the same
+buffers and, under ``also``, the Llama-1024 ZeRO-2 N = 8 and Llama-2048
+ZeRO-3 N = 8 workloads timed the same way.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 the host instead (a bounded sample of the same workload).
@@ -31,6 +34,8 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+DEFAULT_WORKLOAD = "stage_buffer_zero1_fp32_n2"
+ALSO_WORKLOADS = ("llama1024_zero2_n8", "llama2048_zero3_n8")
 METRIC = "fused ZeRO step params/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
@@ -330,13 +335,284 @@ def host_copy_gbs(n: int = 128 * 1024 * 1024, reps: int = 5) -> float:
 
 
 # ---------------------------------------------------------------------------
+# The workload's description, printed identically by both arms.
+# ---------------------------------------------------------------------------
+OPTIMIZER = "Adam fp32 (lr 1e-3, betas 0.9/0.999, eps 1e-8)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def config_for(name: str, wl, world: int, graph: bool = False) -> dict:
+    """The line's ``config``: a function of the workload and the launch only,
+    so that the GPU arm and the reference arm print the same dict."""
+    pl, n = wl["pl"], wl["n"]
+    moved = bytes_per_param(n, wl["grad_dtype"]) * pl.total
+    if moved > L2_BYTES:
+        l2 = f"inputs larger than L2: {moved / 1e9:.2f} GB moved per step (L2 129 MB)"
+    else:
+        l2 = f"working set fits L2: {moved / 1e6:.1f} MB moved per step (L2 129 MB), not flushed"
+    return {"workload": name, "layout": pl.name, "params": pl.total, "units": pl.n_units,
+            "n_ranks_simulated": n, "zero_stage": wl["stage"], "grad_dtype": wl["grad_dtype"],
+            "optimizer": OPTIMIZER, "parallelism": f"{world} GPU replica(s); N={n} DP ranks simulated per GPU",
+            "l2": l2, "cuda_graph": bool(graph)}
+
+
+# ---------------------------------------------------------------------------
 # Our arm.
 # ---------------------------------------------------------------------------
+class Workbench:
+    """One workload resident on the device: the FlatStep context (master, m, v,
+    bf16 parameters), the N replica gradients, the ZeRO-3 unit buffers and,
+    with ``accum``, the bf16 micro-step gradients."""
+
+    def __init__(self, name: str, device, rank: int, accum: int = 0, offload_kw=None):
+        import torch
+        import synth_inputs as si
+        from zero_sharded_mixed_flatparameter_gb300.runner import FlatStep
+        self.name, self.device, self.accum = name, device, accum
+        self.wl = wl = workload(name)
+        pl, n = wl["pl"], wl["n"]
+        init_flat = si.normal_fp32(pl.total, 0.02, 1 + rank, device=device)
+        offs = [0]
+        for k in pl.numel:
+            offs.append(offs[-1] + k)
+        init = [init_flat[offs[p]:offs[p + 1]] for p in range(len(pl.numel))]
+        self.fs = FlatStep(pl.numel, pl.unit, stage=wl["stage"], n_ranks=n, grad_dtype=wl["grad_dtype"],
+                           init_params=init, device=device, **(offload_kw or {}))
+        del init, init_flat
+        self.padded = self.fs.padded
+        self.grads = si.replica_grads(n, self.padded, wl["grad_std"], 100 + rank, wl["grad_dtype"], device=device,
+                                      outlier_fraction=wl["outliers"])
+        self.units = [self.fs.layout(i) for i in range(self.fs.n_units)]
+        self.micro = []
+        if accum > 0:
+            if wl["grad_dtype"] != "fp32":
+                raise SystemExit("--accum needs an fp32-gradient workload (the accumulators are the step's gradients)")
+            self.micro = si.replica_grads(n, self.padded, wl["grad_std"], 200 + rank, "bf16", device=device)
+        self.gather_bufs = []
+        if wl["stage"] == 3:
+            self.gather_bufs = [torch.empty(max(u[1], 1), dtype=torch.bfloat16, device=device) for u in self.units]
+        self.stream = torch.cuda.current_stream(device)
+
+    def one_step(self, ev=None, clip_ev=None, accum_ev=None, gather_ev=None, clip: float = 0.0,
+                 clip_keep: bool = False, grads=None) -> int:
+        """reduce_grads -> (clip) -> zero_step -> (gathers) -> post_step; the
+        optional event pairs bracket the step kernel, the norm pass, the
+        accumulation and the gathers.  Returns the kernels launched."""
+        fs, s = self.fs, self.stream
+        grads = self.grads if grads is None else grads
+        launches = 0
+        if self.micro:
+            if accum_ev is not None:
+                accum_ev[0].record(s)
+            for k in range(self.accum):
+                fs.accumulate_grads(-1, self.micro, grads, first=(k == 0))
+                launches += fs.last_launches()
+            if accum_ev is not None:
+                accum_ev[1].record(s)
+        if self.wl["per_unit"]:
+            for i, (numel, pad, shard, base) in enumerate(self.units):
+                fs.reduce_grads(i, [g[base:base + pad] for g in grads])
+        else:
+            fs.reduce_grads(-1, grads)
+        if clip > 0:
+            if clip_ev is not None:
+                clip_ev[0].record(s)
+            fs.clip_grad_norm(clip, keep_reduced=clip_keep)
+            if clip_ev is not None:
+                clip_ev[1].record(s)
+            launches += fs.last_launches()
+        if ev is not None:
+            ev[0].record(s)
+        fs.step()
+        if ev is not None:
+            ev[1].record(s)
+        launches += fs.last_launches()
+        if gather_ev is not None and self.gather_bufs:
+            gather_ev[0].record(s)
+        for i, buf in enumerate(self.gather_bufs):
+            fs.gather_weights(i, buf)
+            launches += fs.last_launches()
+        if gather_ev is not None and self.gather_bufs:
+            gather_ev[1].record(s)
+        fs.post_step()
+        return launches
+
+    def close(self):
+        import torch
+        self.fs.close()
+        self.grads = self.micro = self.gather_bufs = None
+        torch.cuda.empty_cache()
+
+
+def _pairs(k: int, on: bool = True):
+    import torch
+    if not on:
+        return [None] * k
+    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+
+
+def _ms(pairs):
+    if not pairs or pairs[0] is None:
+        return None
+    return [a.elapsed_time(b) for a, b in pairs]
+
+
+def timed_steps(wb: Workbench, steps: int, world: int, clip: float = 0.0, clip_keep: bool = False,
+                graph=None, graph_launches: int = 0) -> dict:
+    """EXACTLY ``steps`` steps between a barrier + synchronize on both sides,
+    bracketed by CUDA events on the launching stream; per-launch events give
+    the step kernel's (and norm pass's, gathers', accumulation's) durations;
+    nvidia-smi samples the clocks inside the window."""
+    import torch
+    device = wb.device
+    ev = _pairs(steps)
+    clip_ev = _pairs(steps, clip > 0 and graph is None)
+    accum_ev = _pairs(steps, bool(wb.micro) and graph is None)
+    gather_ev = _pairs(steps, bool(wb.gather_bufs) and graph is None)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(device)
+        t0 = time.time()
+        start.record(wb.stream)
+        for k in range(steps):
+            if graph is not None:
+                ev[k][0].record(wb.stream)
+                graph.replay()
+                ev[k][1].record(wb.stream)
+                launches += graph_launches
+            else:
+                launches += wb.one_step(ev[k], clip_ev[k], accum_ev[k], gather_ev[k], clip=clip, clip_keep=clip_keep)
+        end.record(wb.stream)
+        torch.cuda.synchronize(device)
+        t1 = time.time()
+        barrier(world)
+        clocks.mark(t0, t1)
+    return {"total_ms": start.elapsed_time(end), "step_ms": _ms(ev), "clip_ms": _ms(clip_ev),
+            "accum_ms": _ms(accum_ev), "gather_ms": _ms(gather_ev), "launches": launches,
+            "clocks": clocks.summary()}
+
+
+def preroll(device, min_seconds: float = 0.3) -> dict:
+    """Clock ramp before the warm-up: repeated fills of a 1 GiB scratch buffer
+    (not a step, not counted as warm-up), reported in the line."""
+    import torch
+    buf = torch.empty(1 << 30, dtype=torch.uint8, device=device)
+    fills, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < min_seconds:
+        for _ in range(8):
+            buf.fill_(fills & 0xFF)
+            fills += 1
+        torch.cuda.synchronize(device)
+    dt = time.perf_counter() - t0
+    del buf
+    torch.cuda.empty_cache()
+    return {"what": "fills of a 1 GiB scratch buffer before the warm-up (clock ramp; not steps)",
+            "fills": fills, "seconds": round(dt, 3)}
+
+
+def kernel_stats(ms, bytes_per_launch: int, peak: float) -> dict:
+    mean, med = statistics.mean(ms), statistics.median(ms)
+    return {"kernel_ms_mean": mean, "kernel_ms_median": med, "kernel_ms_min": min(ms),
+            "gbs_mean": bytes_per_launch / (mean / 1e3) / 1e9, "gbs_median": bytes_per_launch / (med / 1e3) / 1e9,
+            "frac_mean": bytes_per_launch / (mean / 1e3) / 1e9 / peak}
+
+
+def also_block(name: str, device, rank: int, args, peak: float) -> dict:
+    """Another workload timed the same way (device-resident, exact warm-up,
+    per-launch events), for the line's ``also`` map.  The timed step count is
+    --steps, raised so that the window lasts at least 0.25 s (clock record)."""
+    import torch
+    wb = Workbench(name, device, rank)
+    try:
+        for _ in range(args.warmup):
+            wb.one_step()
+        torch.cuda.synchronize(device)
+        wl, n = wb.wl, wb.wl["n"]
+        bpp = bytes_per_param(n, wl["grad_dtype"])
+        per_step_s = bpp * wb.padded / (0.9 * peak * 1e9)  # estimate, for the window length only
+        steps = max(args.steps, int(0.25 / per_step_s) + 1)
+        r = timed_steps(wb, steps, 1)
+        out = {"config": config_for(name, wl, 1), "padded_params": wb.padded, "steps": steps,
+               "warmup": args.warmup, "value": wl["pl"].total * steps / (r["total_ms"] / 1e3), "unit": UNIT,
+               "ms_per_step": r["total_ms"] / steps, "bytes_per_param": bpp,
+               "kernel": step_kernel_name(n, wl["grad_dtype"], False, wb.padded),
+               **kernel_stats(r["step_ms"], bpp * wb.padded, peak), "gpu_launches": r["launches"],
+               "clocks": r["clocks"]}
+        if r["gather_ms"]:
+            g = statistics.mean(r["gather_ms"])
+            out["gather"] = {"units": len(wb.gather_bufs), "gather_ms_mean": g,
+                             "gather_ms_median": statistics.median(r["gather_ms"]), "gather_bytes": 4 * wb.padded,
+                             "gather_gbs": 4 * wb.padded / (g / 1e3) / 1e9,
+                             "gather_frac": 4 * wb.padded / (g / 1e3) / 1e9 / peak}
+        return out
+    finally:
+        wb.close()
+
+
+def e2e_leg(wb: Workbench, steps: int, warm: int, world: int) -> dict:
+    """The same steps through the public API with HOST buffers: every step
+    copies its N replica gradients from pinned host memory and reads the
+    updated bf16 parameters back.  The host link (not HBM) bounds this, so the
+    copies are pipelined: step k+1's gradients travel on a copy stream into
+    the second of two device buffer sets while step k runs and its parameters
+    are read back on the compute stream."""
+    import torch
+    device, stream, padded = wb.device, wb.stream, wb.padded
+    host_grads = []
+    for g in wb.grads:
+        h = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+        h.copy_(g)
+        host_grads.append(h)
+    host_out = torch.empty(padded, dtype=torch.bfloat16, pin_memory=True)
+    bufs = [wb.grads, [torch.empty_like(g) for g in wb.grads]]
+    copy_stream = torch.cuda.Stream(device)
+    h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
+    step_done = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def run(k_steps):
+        with torch.cuda.stream(copy_stream):
+            for hg, g in zip(host_grads, bufs[0]):
+                g.copy_(hg, non_blocking=True)
+            h2d_done[0].record(copy_stream)
+        for k in range(k_steps):
+            cur, nxt = k % 2, (k + 1) % 2
+            if k + 1 < k_steps:
+                with torch.cuda.stream(copy_stream):
+                    if k >= 1:
+                        copy_stream.wait_event(step_done[nxt])
+                    for hg, g in zip(host_grads, bufs[nxt]):
+                        g.copy_(hg, non_blocking=True)
+                    h2d_done[nxt].record(copy_stream)
+            stream.wait_event(h2d_done[cur])
+            wb.one_step(grads=bufs[cur])
+            step_done[cur].record(stream)
+            host_out.copy_(wb.fs.param16, non_blocking=True)
+
+    run(warm)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    run(steps)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    e2e_ms = aggregate([e0.elapsed_time(e1)], "max", world, device)[0]
+    params_all = aggregate([float(wb.wl["pl"].total * steps)], "sum", world, device)[0]
+    esz = 2 if wb.wl["grad_dtype"] == "bf16" else 4
+    return {"value": params_all / (e2e_ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": wb.wl["n"] * padded * esz, "d2h_bytes_per_step": padded * 2,
+            "ms_per_step": e2e_ms / steps,
+            "pipelining": "double-buffered: step k+1's H2D overlaps step k and its D2H"}
+
+
 def run_ours(args):
     import torch
-    import synth_inputs as si
+    from zero_sharded_mixed_flatparameter_gb300 import binding as B
     from zero_sharded_mixed_flatparameter_gb300 import build_lib
-    from zero_sharded_mixed_flatparameter_gb300.runner import FlatStep
 
     world, rank, local = dist_env()
     if world > 1:
@@ -348,80 +624,20 @@ def run_ours(args):
     if rank == 0:
         build_lib.build()
     barrier(world)
-    wl = workload(args.workload)
-    pl, n = wl["pl"], wl["n"]
+    B.load()
+    timeouts_before = B.zero_kernel_timeouts()
+    peak, peak_kind = measured_peaks()
+    pre = preroll(device)
 
-    init_flat = si.normal_fp32(pl.total, 0.02, 1 + rank, device=device)
-    offs = [0]
-    for k in pl.numel:
-        offs.append(offs[-1] + k)
-    init = [init_flat[offs[p]:offs[p + 1]] for p in range(len(pl.numel))]
     offload_kw = {}
     if args.offload:
         offload_kw = dict(offload=True, offload_chunk=args.offload_chunk, offload_threads=args.offload_threads)
-    fs = FlatStep(pl.numel, pl.unit, stage=wl["stage"], n_ranks=n, grad_dtype=wl["grad_dtype"], init_params=init,
-                  device=device, **offload_kw)
-    del init, init_flat
-    padded = fs.padded
-    grads = si.replica_grads(n, padded, wl["grad_std"], 100 + rank, wl["grad_dtype"], device=device,
-                             outlier_fraction=wl["outliers"])
-    units = [fs.layout(i) for i in range(fs.n_units)]
-    micro = []
-    if args.accum > 0:
-        if wl["grad_dtype"] != "fp32":
-            raise SystemExit("--accum needs an fp32-gradient workload (the accumulators are the step's gradients)")
-        micro = si.replica_grads(n, padded, wl["grad_std"], 200 + rank, "bf16", device=device)
-    gather_bufs = []
-    if wl["stage"] == 3:
-        gather_bufs = [torch.empty(max(u[1], 1), dtype=torch.bfloat16, device=device) for u in units]
-    stream = torch.cuda.current_stream(device)
+    wb = Workbench(args.workload, device, rank, accum=args.accum, offload_kw=offload_kw)
+    wl, fs, padded, n = wb.wl, wb.fs, wb.padded, wb.wl["n"]
+    pl = wl["pl"]
 
-    def one_step(ev_pair=None, clip_pair=None, accum_pair=None, gather_pair=None):
-        launches = 0
-        if micro:
-            if accum_pair is not None:
-                accum_pair[0].record(stream)
-            for k in range(args.accum):
-                fs.accumulate_grads(-1, micro, grads, first=(k == 0))
-                launches += fs.last_launches()
-            if accum_pair is not None:
-                accum_pair[1].record(stream)
-        if wl["per_unit"]:
-            for i, (numel, pad, shard, base) in enumerate(units):
-                fs.reduce_grads(i, [g[base:base + pad] for g in grads])
-        else:
-            fs.reduce_grads(-1, grads)
-        if args.clip > 0:
-            if clip_pair is not None:
-                clip_pair[0].record(stream)
-            fs.clip_grad_norm(args.clip, keep_reduced=args.clip_keep)
-            if clip_pair is not None:
-                clip_pair[1].record(stream)
-            launches += fs.last_launches()
-        if ev_pair is not None:
-            ev_pair[0].record(stream)
-        fs.step()
-        if ev_pair is not None:
-            ev_pair[1].record(stream)
-        launches += fs.last_launches()
-        if gather_pair is not None and gather_bufs:
-            gather_pair[0].record(stream)
-        for i, buf in enumerate(gather_bufs):
-            fs.gather_weights(i, buf)
-            launches += fs.last_launches()
-        if gather_pair is not None and gather_bufs:
-            gather_pair[1].record(stream)
-        fs.post_step()
-        return launches
-
-    # Warm-up: W steps, extended until at least 0.3 s of device work has run so
-    # that clocks have ramped before the timed region (the count is reported).
-    warm_done, t_warm = 0, time.perf_counter()
-    while warm_done < args.warmup or time.perf_counter() - t_warm < 0.3:
-        one_step()
-        warm_done += 1
-        if warm_done % 16 == 0:
-            torch.cuda.synchronize(device)
+    for _ in range(args.warmup):  # exactly --warmup steps
+        wb.one_step(clip=args.clip, clip_keep=args.clip_keep)
     torch.cuda.synchronize(device)
 
     # --graph: the step (registration, clip, step, gathers, post_step) is
@@ -430,53 +646,20 @@ def run_ours(args):
     # the launch shapes.
     graph, graph_launches = None, 0
     if args.graph:
-        fs.enable_capturable(max_steps=warm_done + args.steps + 2)
-        graph_launches = one_step()
+        fs.enable_capturable(max_steps=args.warmup + args.steps + 2)
+        graph_launches = wb.one_step(clip=args.clip, clip_keep=args.clip_keep)
         torch.cuda.synchronize(device)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            one_step()
+            wb.one_step(clip=args.clip, clip_keep=args.clip_keep)
         torch.cuda.synchronize(device)
 
-    # ---- device-resident timed region ----
-    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clip_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)] if args.clip > 0 else [None] * args.steps
-    accum_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(args.steps)] if args.accum > 0 else [None] * args.steps
-    gather_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                    for _ in range(args.steps)] if gather_bufs else [None] * args.steps
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches = 0
-    with ClockSampler(device.index if device.index is not None else 0) as clocks:
-        barrier(world)
-        torch.cuda.synchronize(device)
-        t_region0 = time.time()
-        start.record(stream)
-        for k in range(args.steps):
-            if graph is not None:
-                pairs[k][0].record(stream)
-                graph.replay()
-                pairs[k][1].record(stream)
-                launches += graph_launches
-            else:
-                launches += one_step(pairs[k], clip_pairs[k], accum_pairs[k], gather_pairs[k])
-        end.record(stream)
-        torch.cuda.synchronize(device)
-        t_region1 = time.time()
-        barrier(world)
-        clocks.mark(t_region0, t_region1)
-    total_ms = start.elapsed_time(end)
-    step_kernel_ms = [a.elapsed_time(b) for a, b in pairs]
-    clip_ms = [a.elapsed_time(b) for a, b in clip_pairs] if args.clip > 0 and graph is None else None
-    accum_ms = [a.elapsed_time(b) for a, b in accum_pairs] if args.accum > 0 and graph is None else None
-    gather_ms = [a.elapsed_time(b) for a, b in gather_pairs] if gather_bufs and graph is None else None
+    r = timed_steps(wb, args.steps, world, clip=args.clip, clip_keep=args.clip_keep, graph=graph,
+                    graph_launches=graph_launches)
     if graph is not None:
-        fs.disable_capturable()  # the end-to-end leg below runs eagerly
+        fs.disable_capturable()  # the legs below run eagerly
         del graph
-    clock = clocks.summary()
-
-    total_ms_max, kern_ms_max = aggregate([total_ms, statistics.mean(step_kernel_ms)], "max", world, device)
+    total_ms_max, kern_ms_max = aggregate([r["total_ms"], statistics.mean(r["step_ms"])], "max", world, device)
     params_all = aggregate([float(pl.total * args.steps)], "sum", world, device)[0]
     value = params_all / (total_ms_max / 1e3)
 
@@ -484,72 +667,47 @@ def run_ours(args):
     bpp = 4 + 26 if (args.clip > 0 and args.clip_keep) else bytes_per_param(n, wl["grad_dtype"])
     bytes_per_launch = bpp * padded
     achieved_gbs = bytes_per_launch / (kern_ms_max / 1e3) / 1e9
-    peak, peak_kind = measured_peaks()
-    traffic = recorded_traffic(args.workload)
+    gbytes = (2 if wl["grad_dtype"] == "bf16" else 4) * n * padded  # replica gradient bytes (norm pass reads)
 
-    # ---- end to end through the public API with host buffers ----
-    # Every step copies its N replica gradients from pinned host memory and
-    # reads the updated bf16 parameters back.  The host link (not HBM) bounds
-    # this, so the copies are pipelined: step k+1's gradients travel on a copy
-    # stream into the second of two device buffer sets while step k runs and
-    # its parameters are read back on the compute stream.
+    # Clipped leg: unless the timed region already clipped, --steps more
+    # steps with global-norm clipping to --clip-leg on the same buffers (after
+    # --warmup clipped warm-up steps), timed the same way.
+    clip_block = None
+    if args.clip > 0 and r["clip_ms"]:
+        c = statistics.mean(r["clip_ms"])
+        nb = gbytes + (4 * padded if args.clip_keep else 0)
+        clip_block = {"max_norm": args.clip, "keep_reduced": args.clip_keep, "leg": "the timed region itself",
+                      "norm_pass_ms_mean": c, "norm_pass_ms_median": statistics.median(r["clip_ms"]),
+                      "norm_pass_bytes": nb, "norm_pass_gbs": nb / (c / 1e3) / 1e9,
+                      "note": "the clipped step is the norm pass (grad_sq + finalize kernels) plus the step kernel"}
+    elif args.clip_leg > 0 and not args.offload and not args.graph:
+        for _ in range(args.warmup):
+            wb.one_step(clip=args.clip_leg)
+        torch.cuda.synchronize(device)
+        rc = timed_steps(wb, args.steps, world, clip=args.clip_leg)
+        c = statistics.mean(rc["clip_ms"])
+        clip_block = {"max_norm": args.clip_leg, "keep_reduced": False,
+                      "leg": f"{args.steps} clipped steps after the timed region, same buffers, "
+                             f"after {args.warmup} clipped warm-up steps",
+                      "value": pl.total * args.steps / (rc["total_ms"] / 1e3), "unit": UNIT,
+                      "ms_per_step": rc["total_ms"] / args.steps,
+                      "norm_pass_ms_mean": c, "norm_pass_ms_median": statistics.median(rc["clip_ms"]),
+                      "norm_pass_bytes": gbytes, "norm_pass_gbs": gbytes / (c / 1e3) / 1e9,
+                      "norm_pass_frac": gbytes / (c / 1e3) / 1e9 / peak,
+                      "step_kernel": kernel_stats(rc["step_ms"], bytes_per_launch, peak),
+                      "gpu_launches": rc["launches"], "clocks": rc["clocks"],
+                      "note": "the clipped step is the norm pass (grad_sq + finalize kernels) plus the step kernel"}
+
     e2e = None
     if not args.no_e2e and not args.offload:
-        host_grads = [g.to("cpu").pin_memory() for g in grads]
-        host_out = torch.empty(padded, dtype=torch.bfloat16).pin_memory()
-        bufs = [grads, [torch.empty_like(g) for g in grads]]
-        copy_stream = torch.cuda.Stream(device)
-        h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
-        step_done = [torch.cuda.Event(), torch.cuda.Event()]
+        e2e = e2e_leg(wb, args.steps, min(args.warmup, 3) + 1, world)
+    wb.close()
+    del wb, fs
 
-        def e2e_run(steps):
-            with torch.cuda.stream(copy_stream):
-                for hg, g in zip(host_grads, bufs[0]):
-                    g.copy_(hg, non_blocking=True)
-                h2d_done[0].record(copy_stream)
-            for k in range(steps):
-                cur, nxt = k % 2, (k + 1) % 2
-                if k + 1 < steps:
-                    with torch.cuda.stream(copy_stream):
-                        if k >= 1:
-                            copy_stream.wait_event(step_done[nxt])
-                        for hg, g in zip(host_grads, bufs[nxt]):
-                            g.copy_(hg, non_blocking=True)
-                        h2d_done[nxt].record(copy_stream)
-                stream.wait_event(h2d_done[cur])
-                if wl["per_unit"]:
-                    for i, (numel, pad, shard, base) in enumerate(units):
-                        fs.reduce_grads(i, [g[base:base + pad] for g in bufs[cur]])
-                else:
-                    fs.reduce_grads(-1, bufs[cur])
-                fs.step()
-                for i, buf in enumerate(gather_bufs):
-                    fs.gather_weights(i, buf)
-                fs.post_step()
-                step_done[cur].record(stream)
-                host_out.copy_(fs.param16, non_blocking=True)
-
-        e2e_run(min(args.warmup, 3) + 1)
-        torch.cuda.synchronize(device)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        torch.cuda.synchronize(device)
-        e0.record(stream)
-        e2e_run(args.steps)
-        e1.record(stream)
-        torch.cuda.synchronize(device)
-        barrier(world)
-        e2e_ms = aggregate([e0.elapsed_time(e1)], "max", world, device)[0]
-        esz = 2 if wl["grad_dtype"] == "bf16" else 4
-        e2e = {"value": params_all / (e2e_ms / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": n * padded * esz, "d2h_bytes_per_step": padded * 2,
-               "ms_per_step": e2e_ms / args.steps,
-               "pipelining": "double-buffered: step k+1's H2D overlaps step k and its D2H"}
-        del host_grads, host_out, bufs
-
-    fs.close()
-    del grads
-    torch.cuda.empty_cache()
+    also = None
+    if world == 1 and not args.offload and not args.graph and args.also:
+        also = {name: also_block(name, device, rank, args, peak) for name in args.also.split(",") if name}
+    timeouts = B.zero_kernel_timeouts() - timeouts_before
 
     cpu = cpu_adam = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -558,9 +716,12 @@ def run_ours(args):
 
     roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                 "frac": achieved_gbs / peak, "peak_source": f"hbm_gbs {peak_kind}",
-                "traffic": traffic, "algorithmic_bytes_per_launch": bytes_per_launch,
-                "bytes_per_param": bpp, "kernel": step_kernel_name(n, wl["grad_dtype"], args.clip_keep, padded),
-                "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms),
+                "traffic": recorded_traffic(args.workload), "algorithmic_bytes_per_launch": bytes_per_launch,
+                "bytes_per_param": bpp, "padded_params": padded,
+                "kernel": step_kernel_name(n, wl["grad_dtype"], args.clip_keep, padded),
+                "kernel_ms_mean": kern_ms_max, "kernel_ms_median": statistics.median(r["step_ms"]),
+                "kernel_ms_min": min(r["step_ms"]),
+                "gbs_at_median": bytes_per_launch / (statistics.median(r["step_ms"]) / 1e3) / 1e9,
                 "timed": "whole replayed step (CUDA graph)" if args.graph else "step kernel launch"}
     offload = None
     if args.offload:
@@ -575,62 +736,64 @@ def run_ours(args):
                     "frac": host_gbs / host_peak, "peak_source": "host memory copy measured in this run (torch CPU copy)",
                     "traffic": None, "algorithmic_bytes_per_launch": 36 * padded, "bytes_per_param": 36,
                     "kernel": "zero_offload_step (host Adam; reduce_out_kernel on the GPU)",
-                    "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(step_kernel_ms)}
+                    "kernel_ms_mean": kern_ms_max, "kernel_ms_min": min(r["step_ms"])}
         offload = {"chunk": args.offload_chunk, "threads": args.offload_threads or os.cpu_count(),
                    "d2h_bytes_per_step": 4 * padded, "h2d_bytes_per_step": 2 * padded,
                    "link_gbs": 6 * padded / (kern_ms_max / 1e3) / 1e9,
                    "note": "fp32 master/m/v in host memory; per chunk: GPU reduce -> D2H -> host Adam -> H2D, "
                            "3 chunks in flight"}
 
+    gather = None
+    if r["gather_ms"]:
+        g = statistics.mean(r["gather_ms"])
+        gather = {"units": pl.n_units, "gather_ms_mean": g, "gather_bytes": 4 * padded,
+                  "gather_gbs": 4 * padded / (g / 1e3) / 1e9,
+                  "note": "ZeRO-3 per-unit gathers of the bf16 shards into unit buffers (2 B read + 2 B written)"}
+    accum = None
+    if r["accum_ms"]:
+        a_ms = statistics.mean(r["accum_ms"])
+        ab = n * padded * (6 + 10 * (args.accum - 1))
+        accum = {"micro_steps": args.accum, "accumulate_ms_mean": a_ms, "accumulate_bytes": ab,
+                 "accumulate_gbs": ab / (a_ms / 1e3) / 1e9,
+                 "note": "K micro-steps of bf16 grads accumulated into the fp32 replica gradients, then the step"}
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": warm_done, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; bf16/fp32 grads, fp32 state)",
-            "config": {"workload": args.workload, "layout": pl.name, "params": pl.total, "padded_params": padded,
-                       "units": fs.n_units, "n_ranks_simulated": n, "zero_stage": wl["stage"],
-                       "grad_dtype": wl["grad_dtype"], "optimizer": "Adam fp32 (lr 1e-3, betas 0.9/0.999, eps 1e-8)",
-                       "parallelism": f"{world} GPU replica(s); N={n} DP ranks simulated per GPU",
-                       "l2": f"inputs larger than L2: {bytes_per_launch / 1e9:.2f} GB moved per step (L2 129 MB)",
-                       "cuda_graph": bool(args.graph)},
+            "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; bf16/fp32 grads, fp32 state)",
+            "config": config_for(args.workload, wl, world, getattr(args, "graph", False)),
             "hbm_gbs": None if args.offload else achieved_gbs,
             "hbm_frac_of_peak": None if args.offload else achieved_gbs / peak,
             "roofline": roofline,
+            "preroll": pre,
             "offload": offload,
-            "clip": None if clip_ms is None else {
-                "max_norm": args.clip, "norm_pass_ms_mean": statistics.mean(clip_ms),
-                "keep_reduced": args.clip_keep,
-                "norm_pass_bytes": ((2 if wl["grad_dtype"] == "bf16" else 4) * n + (4 if args.clip_keep else 0)) * padded,
-                "norm_pass_gbs": ((2 if wl["grad_dtype"] == "bf16" else 4) * n + (4 if args.clip_keep else 0)) * padded
-                / (statistics.mean(clip_ms) / 1e3) / 1e9,
-                "note": "the clipped step is the norm pass (grad_sq + finalize kernels) plus the step kernel"},
-            "gather": None if gather_ms is None else {
-                "units": len(gather_bufs), "gather_ms_mean": statistics.mean(gather_ms),
-                "gather_bytes": 4 * padded, "gather_gbs": 4 * padded / (statistics.mean(gather_ms) / 1e3) / 1e9,
-                "note": "ZeRO-3 per-unit gathers of the bf16 shards into unit buffers (2 B read + 2 B written)"},
-            "accum": None if accum_ms is None else {
-                "micro_steps": args.accum, "accumulate_ms_mean": statistics.mean(accum_ms),
-                "accumulate_bytes": n * padded * (6 + 10 * (args.accum - 1)),
-                "accumulate_gbs": n * padded * (6 + 10 * (args.accum - 1)) / (statistics.mean(accum_ms) / 1e3) / 1e9,
-                "note": "K micro-steps of bf16 grads accumulated into the fp32 replica gradients, then the step"},
+            "clip": clip_block,
+            "gather": gather,
+            "accum": accum,
+            "also": also,
             "cpu_baseline": cpu,
             "cpu_adam": cpu_adam,
             "e2e": e2e,
-            "gpu_launches": launches,
-            "clocks": clock,
+            "gpu_launches": r["launches"],
+            "kernel_timeouts": timeouts,
+            "clocks": r["clocks"],
         }
+        if timeouts:
+            line["error"] = (f"{timeouts} bounded wait(s) of a tile-staged kernel gave up during the run: "
+                             "some steps were partial, the figures are not valid")
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+    if timeouts:
+        raise SystemExit(1)
 
 
 # ---------------------------------------------------------------------------
 # Roofline sweep: one flat fp32 buffer of 1M..1B params x N = 1..16.
 # ---------------------------------------------------------------------------
-L2_BYTES = 129 * 1024 * 1024
-
-
 def run_sweep(args):
     import torch
     import synth_inputs as si
@@ -756,8 +919,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "layout": wl["pl"].name, "params": wl["pl"].total,
-                   "n_ranks_simulated": wl["n"], "zero_stage": wl["stage"], "grad_dtype": wl["grad_dtype"]},
+        "config": config_for(args.workload, wl, world, getattr(args, "graph", False)),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"each step: one literal per-rank oracle step on a contiguous {sample_params:,}-param "
                                    f"window of the workload (N={wl['n']}, {wl['grad_dtype']} grads), single-threaded"},
@@ -769,10 +931,14 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=None, help="timed steps (default 2000; 50 with --offload)")
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default 100; 50 with --offload)")
+    ap.add_argument("--warmup", type=int, default=5, help="untimed warm-up steps (exactly this many)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama1024_zero2_n8")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--also", default=",".join(ALSO_WORKLOADS),
+                    help="comma-separated workloads timed after the main one (1 GPU), reported under 'also'")
+    ap.add_argument("--clip-leg", type=float, default=1.0,
+                    help="max norm of the clipped leg timed after the main region (0: no leg)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--graph", action="store_true",
@@ -795,7 +961,7 @@ def main():
                     help="global-norm clipping to this max norm before every step (0: off)")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = 50 if args.offload else 2000
+        args.steps = 50 if args.offload else 100
     if args.graph and args.offload:
         ap.error("--graph and --offload exclude each other (the offload step runs on host threads)")
     if args.warmup < 3 and args.impl == "ours":

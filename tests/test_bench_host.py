@@ -68,3 +68,23 @@ def test_traffic_only_for_the_recorded_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic("w3") is None          # not recorded
     monkeypatch.setattr(bench, "ROOT", real_root)
     assert os.path.exists(os.path.join(real_root, "profiles", "step_kernel_dram_traffic.txt"))
+
+
+def test_default_workload_is_the_stage_buffer():
+    # the default line is the largest single-GPU workload: the 2.03 B-param
+    # stage buffer, N = 2, ZeRO-1, fp32 gradients (34 B/param)
+    assert bench.DEFAULT_WORKLOAD == "stage_buffer_zero1_fp32_n2"
+    wl = bench.workload(bench.DEFAULT_WORKLOAD)
+    assert (wl["n"], wl["stage"], wl["grad_dtype"], wl["pl"].total) == (2, 1, "fp32", 2_030_174_208)
+    cfg = bench.config_for(bench.DEFAULT_WORKLOAD, wl, 1)
+    assert cfg["params"] == 2_030_174_208 and cfg["units"] == 1 and cfg["n_ranks_simulated"] == 2
+    assert cfg["l2"].startswith("inputs larger than L2: 69.03 GB")
+    for name in bench.ALSO_WORKLOADS:
+        bench.workload(name)
+
+
+def test_config_is_a_function_of_the_workload_only():
+    wl = bench.workload("llama2048_zero3_n8")
+    a, b = bench.config_for("llama2048_zero3_n8", wl, 1), bench.config_for("llama2048_zero3_n8", wl, 1)
+    assert a == b and a["units"] == 10 and a["zero_stage"] == 3
+    assert bench.config_for("toy_mlp_n4", bench.workload("toy_mlp_n4"), 1)["l2"].startswith("working set fits L2")

@@ -70,3 +70,7 @@ def test_reference_arm_runs_on_rank0_only():
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert out[1] == ""
+    # the same config dict the GPU arm prints for this workload and launch
+    import bench
+    assert line["config"] == bench.config_for("toy_mlp_n4", bench.workload("toy_mlp_n4"), 2)
+    assert (line["steps"], line["warmup"]) == (2, 1)
