@@ -145,8 +145,12 @@ zero_status zero_param_offset(const zero_ctx* ctx, int32_t param, int64_t* offse
  * zero_state_bytes — per-rank model-state bytes of this layout under `stage`
  * (lecture notes §2.3 and §9 item 2: bf16 params 2, bf16 grads 2, optimizer
  * state K = 12 bytes per element; stage 1 shards K, stage 2 also the grads,
- * stage 3 also the params): 16P, 4P + 12S, 2P + 14S, 16S with P the padded
- * total and S the per-rank shard total.  per_rank_bytes has n_ranks entries.
+ * stage 3 also the params): 16P, 4P + 12S, 2P + 14S, 16S with P the total
+ * and S the per-rank shard total of the layout as `stage` pads it with the
+ * context's N — no padding for stage 0, each unit padded to a multiple of N
+ * for stages 1-3 (notes §3.6) — whatever stage the context itself runs (a
+ * stage-0 context, which does not pad, still reports the shards a sharded
+ * stage would hold).  per_rank_bytes has n_ranks entries.
  */
 zero_status zero_state_bytes(const zero_ctx* ctx, int32_t stage, int64_t* per_rank_bytes);
 
@@ -154,7 +158,8 @@ zero_status zero_state_bytes(const zero_ctx* ctx, int32_t stage, int64_t* per_ra
  * zero_stage3_peak_bytes — ZeRO-3 model-state peak of one rank during
  * backward (lecture notes §3.5 and §11 Exercise 5): resident shards, plus the
  * grad shards of units already reduce-scattered, plus the full bf16 params and
- * grads of the unit being processed (units processed last to first).
+ * grads of the unit being processed (units processed last to first), each
+ * unit padded to a multiple of N as stage 3 pads it.
  * peak_unit receives the unit where the peak occurs (-1 if none).
  */
 zero_status zero_stage3_peak_bytes(const zero_ctx* ctx, int64_t* peak_bytes, int32_t* peak_unit);
@@ -284,14 +289,19 @@ zero_status zero_clip_grad_norm_ex(zero_ctx* ctx, float max_norm, int32_t flags,
  * cannot hand in a workspace.  The pages have no counterpart: this is a
  * property of this library's interface, not of the method.
  * Same computation and result as zero_clip_grad_norm; the scratch is a fixed
- * 1 MiB array in the library's own device memory (created on every GPU that
- * loads the library, held until exit), so layouts needing more than that —
- * about 2.1e9 padded elements — are rejected with ZERO_EINVAL.  The call
- * allocates nothing.  Its first call on a device looks up the array's device
- * address (set-up, once per device, for the current device); make that first
- * call before any stream capture.  All calls on a device share the array and
- * it keeps the last call's contents: calls whose device work can overlap race
- * on it, and between a call and the same context's zero_step no other
+ * 1 MiB array in the library's own device memory (one per CUDA context that
+ * loads the library's device code — normally one per GPU — held until that
+ * context ends), so layouts needing more than that — about 2.1e9 padded
+ * elements — are rejected with ZERO_EINVAL.  The call allocates nothing.
+ * Its first call in a CUDA context looks up the array's device address in
+ * that context (set-up, once per context, keyed on the context's unique id,
+ * so a second context on the same GPU or the primary context re-created
+ * after cudaDeviceReset gets its own lookup); that first lookup may load the
+ * library's device code into the context, which creates the array.  So make
+ * the first call in each context before any stream capture and before any
+ * region that must not allocate.  All calls in a context share the array
+ * and it keeps the last call's contents: calls whose device work can overlap
+ * race on it, and between a call and the same zero_ctx's zero_step no other
  * static-scratch clip may run unless all are ordered on one stream.
  * Errors: as zero_clip_grad_norm; ZERO_EINVAL when the layout is too large.
  */

@@ -6,17 +6,25 @@
 // that forbids allocation, an embedding that has no allocation API of its own
 // to offer).  zero_clip_grad_norm_static gives them the same computation with
 // its scratch in a fixed array that lives in the library's own device memory:
-// the array below, kStaticClipBytes long, is created on every GPU that loads
-// the library and held until the process exits.  The call allocates nothing.
+// the array below, kStaticClipBytes long, is created in every CUDA context
+// that loads the library's device code and held until that context ends.
+// The call allocates nothing.
 //
-// The array is shared by every call on a device and keeps the last call's
+// The array is shared by every call in a context and keeps the last call's
 // contents.  Nothing in it has to start at zero: each call writes every chunk
 // partial it later reads, and writes the norm and coefficient itself.  Calls
-// whose device work can overlap (different streams, different contexts) race
-// on it; the coefficient one call leaves there is read by that context's next
+// whose device work can overlap (different streams) race on it; the
+// coefficient one call leaves there is read by that zero_ctx's next
 // zero_step, so no other static-scratch clip may run between the two unless
 // all of them are ordered on one stream.
+//
+// Each CUDA context has its own copy of a __device__ array, at its own
+// address.  The address is therefore looked up once per context — keyed on
+// the context's unique id, which the driver never reuses within a process —
+// and not once per device ordinal: a non-primary context, or the primary
+// context created again after cudaDeviceReset, gets its own lookup.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -33,9 +41,50 @@ constexpr long long kStaticClipBytes = 1LL << 20;
 
 static __device__ __align__(256) unsigned char g_clip_scratch[kStaticClipBytes];
 
-constexpr int kMaxDevices = 64;
+// Driver calls reached through the runtime's entry-point query, so that the
+// library needs no link-time dependency on the driver library.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+std::once_flag g_driver_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+void load_driver_calls() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess && fn) {
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+  }
+  fn = nullptr;
+  q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess && fn) {
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(fn);
+  }
+}
+
+// The unique id of the calling thread's current context; false when no
+// context is current or the driver cannot say.
+bool current_context_id(unsigned long long* id) {
+  std::call_once(g_driver_once, load_driver_calls);
+  if (!g_ctx_get_current || !g_ctx_get_id) return false;
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Addresses of the array in the contexts seen so far (a small ring: an
+// evicted context is simply looked up again).
+constexpr int kCachedContexts = 64;
+struct CachedAddress {
+  unsigned long long ctx_id;
+  void* address;
+};
 std::mutex g_mutex;
-void* g_scratch_address[kMaxDevices] = {};
+CachedAddress g_cache[kCachedContexts] = {};
+int g_cache_next = 0;
 
 }  // namespace
 
@@ -53,28 +102,46 @@ extern "C" zero_status zero_clip_grad_norm_static(zero_ctx* ctx, float max_norm,
     return static_cast<zero_status>(zfs_report_error(ctx, ZERO_EINVAL, msg));
   }
   int device = -1;
-  cudaError_t e = cudaGetDevice(&device);
-  if (e != cudaSuccess || device < 0 || device >= kMaxDevices) {
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0) {
     return static_cast<zero_status>(zfs_report_error(ctx, ZERO_ECUDA, "cannot query the current device"));
   }
   void* scratch = nullptr;
-  {
-    // Set-up, once per device, with that device current: in host code the
-    // array's name only stands in for the device object, so its device
-    // address is looked up here and passed to the kernels.
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_address[device]) {
-      void* address = nullptr;
-      e = cudaGetSymbolAddress(&address, g_clip_scratch);
-      if (e != cudaSuccess || !address) {
-        char msg[256];
-        std::snprintf(msg, sizeof msg, "cudaGetSymbolAddress of the static clip scratch failed: %s",
-                      cudaGetErrorString(e));
-        return static_cast<zero_status>(zfs_report_error(ctx, ZERO_ECUDA, msg));
+  unsigned long long ctx_id = 0;
+  bool have_id = current_context_id(&ctx_id);
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (have_id) {
+    for (const CachedAddress& c : g_cache) {
+      if (c.address && c.ctx_id == ctx_id) {
+        scratch = c.address;
+        break;
       }
-      g_scratch_address[device] = address;
     }
-    scratch = g_scratch_address[device];
+  }
+  if (!scratch) {
+    // Set-up, once per context, with the caller's device current: in host
+    // code the array's name only stands in for the device object, so its
+    // device address is looked up here and passed to the kernels.  The first
+    // lookup in a context may load the library's device code into it.
+    void* address = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&address, g_clip_scratch);
+    if (e != cudaSuccess || !address) {
+      char msg[256];
+      std::snprintf(msg, sizeof msg, "cudaGetSymbolAddress of the static clip scratch failed: %s",
+                    cudaGetErrorString(e));
+      return static_cast<zero_status>(zfs_report_error(ctx, ZERO_ECUDA, msg));
+    }
+    cudaPointerAttributes attr{};
+    e = cudaPointerGetAttributes(&attr, address);
+    if (e != cudaSuccess || attr.type != cudaMemoryTypeDevice || attr.device != device) {
+      return static_cast<zero_status>(zfs_report_error(
+          ctx, ZERO_ECUDA, "the static clip scratch is not device memory of the current device"));
+    }
+    scratch = address;
+    if (!have_id) have_id = current_context_id(&ctx_id);  // the lookup may have made the context current
+    if (have_id) {
+      g_cache[g_cache_next] = CachedAddress{ctx_id, address};
+      g_cache_next = (g_cache_next + 1) % kCachedContexts;
+    }
   }
   return zero_clip_grad_norm(ctx, max_norm, scratch, kStaticClipBytes, stream);
 }
