@@ -69,8 +69,11 @@ def test_layout_matches_oracle(B, oracle_lib, pl, n, stage):
         for p in range(len(pl.numel)):
             assert B.zero_param_offset(ctx, p) == lay.param_offset[p]
         for s in range(4):
-            assert B.zero_state_bytes(ctx, s, n) == list(oracle_lib.state_bytes(lay.unit_padded, n, s))
-        assert B.zero_stage3_peak_bytes(ctx) == oracle_lib.zero3_backward_peak(lay.unit_padded, n)
+            # the ledger of stage s is that of the layout as stage s pads it
+            lay_s = oracle_lib.layout(pl.numel, pl.unit, n, s)
+            assert B.zero_state_bytes(ctx, s, n) == list(oracle_lib.state_bytes(lay_s.unit_padded, n, s))
+        lay3 = oracle_lib.layout(pl.numel, pl.unit, n, 3)
+        assert B.zero_stage3_peak_bytes(ctx) == oracle_lib.zero3_backward_peak(lay3.unit_padded, n)
     finally:
         B.zero_destroy(ctx)
 
@@ -103,6 +106,27 @@ def test_zero3_peak_lecture_mlp(B):
     try:
         assert B.zero_stage3_peak_bytes(ctx) == (161_632, 1)
         assert B.zero_state_bytes(ctx, 3, 4) == [130_624] * 4
+    finally:
+        B.zero_destroy(ctx)
+
+
+@pytest.mark.parametrize("ctx_stage", [0, 1, 2, 3])
+def test_ledger_independent_of_the_context_stage(B, oracle_lib, ctx_stage):
+    # Units whose sizes are not multiples of N: a stage-0 context does not pad
+    # (F = 1), yet its stage-1..3 ledger must count the shards those stages
+    # pad to a multiple of N (ceil(psi / N) per rank), exactly as a context of
+    # that stage reports it.
+    numel, unit, n = [1552, 7, 33, 1], [0, 1, 1, 2], 3
+    ctx = B.zero_plan(B.make_config(ctx_stage, n), numel, unit)
+    try:
+        for s in range(4):
+            lay_s = oracle_lib.layout(numel, unit, n, s)
+            assert B.zero_state_bytes(ctx, s, n) == list(oracle_lib.state_bytes(lay_s.unit_padded, n, s))
+        # by hand: stage 3 holds 16 B per element of ceil(psi / N) per unit
+        assert B.zero_state_bytes(ctx, 3, n)[0] == 16 * (518 + 14 + 1)
+        assert B.zero_state_bytes(ctx, 0, n)[0] == 16 * (1552 + 7 + 33 + 1)
+        lay3 = oracle_lib.layout(numel, unit, n, 3)
+        assert B.zero_stage3_peak_bytes(ctx) == oracle_lib.zero3_backward_peak(lay3.unit_padded, n)
     finally:
         B.zero_destroy(ctx)
 

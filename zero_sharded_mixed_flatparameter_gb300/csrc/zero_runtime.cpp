@@ -360,6 +360,15 @@ bool all_registered(const zero_ctx* ctx, int32_t* missing) {
   return true;
 }
 
+// Length of unit i padded as stage `stage` pads it with this context's N:
+// stage 0 (plain data parallelism) does not pad, stages 1-3 pad to a
+// multiple of N (CMU 15-779 Lecture 13 notes §3.6).  The ledger of a stage is
+// that of this layout run as that stage, whatever the context's own stage.
+int64_t padded_as_stage(const zero_ctx* ctx, int32_t i, int32_t stage) {
+  const int64_t F = stage == 0 ? 1 : ctx->cfg.n_ranks;
+  return (ctx->unit_numel[i] + F - 1) / F * F;
+}
+
 }  // namespace
 
 int zfs_report_error(zero_ctx* ctx, int status, const char* message) {
@@ -541,8 +550,9 @@ zero_status zero_state_bytes(const zero_ctx* ctx, int32_t stage, int64_t* per_ra
   const int64_t N = ctx->cfg.n_ranks;
   int64_t P = 0, S = 0;
   for (int32_t i = 0; i < ctx->n_units; ++i) {
-    P += ctx->unit_padded[i];
-    S += ctx->unit_padded[i] / N;
+    const int64_t padded = padded_as_stage(ctx, i, stage);
+    P += padded;
+    S += padded / N;
   }
   int64_t bytes;
   switch (stage) {
@@ -559,17 +569,18 @@ zero_status zero_stage3_peak_bytes(const zero_ctx* ctx, int64_t* peak_bytes, int
   if (!ctx || !peak_bytes) return fail(nullptr, ZERO_EINVAL, "NULL argument");
   const int64_t N = ctx->cfg.n_ranks;
   int64_t S = 0;
-  for (int32_t i = 0; i < ctx->n_units; ++i) S += ctx->unit_padded[i] / N;
+  for (int32_t i = 0; i < ctx->n_units; ++i) S += padded_as_stage(ctx, i, 3) / N;
   const int64_t resident = 14 * S;  // bf16 param shard 2 + fp32 master/m/v 12
   int64_t best = resident, reduced = 0;
   int32_t where = -1;
   for (int32_t k = ctx->n_units - 1; k >= 0; --k) {
-    const int64_t at = resident + reduced + 4 * ctx->unit_padded[k];
+    const int64_t padded = padded_as_stage(ctx, k, 3);
+    const int64_t at = resident + reduced + 4 * padded;
     if (at > best) {
       best = at;
       where = k;
     }
-    reduced += 2 * (ctx->unit_padded[k] / N);
+    reduced += 2 * (padded / N);
   }
   *peak_bytes = best;
   if (peak_unit) *peak_unit = where;
