@@ -286,3 +286,55 @@ def test_non_finite_gradients(gd, keep):
     fs.close()
     for a, b in zip(gpu_norms, ref_norms):
         assert _same_norm(a, b), (a, b)
+
+
+def _scale_grads(pb, scale, lo=None, hi=None):
+    """Multiplies replica gradients [lo, hi) of every step by `scale` (host
+    arrays; bf16 patterns are rescaled through fp32 and rounded back)."""
+    for reps in pb.grads:
+        for k, flat in enumerate(reps):
+            sl = slice(lo, hi)
+            if pb.grad_dtype == "bf16":
+                f = torch.from_numpy(flat[sl].view(np.int16)).view(torch.bfloat16).float() * scale
+                flat[sl] = f.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            else:
+                flat[sl] = (flat[sl].astype(np.float64) * scale).astype(np.float32)
+
+
+@pytest.mark.parametrize("gd,scale", [("fp32", 1e-28), ("bf16", 1e-18), ("fp32", 1e-40), ("bf16", 0.0)])
+def test_norm_of_tiny_and_zero_gradients(gd, scale):
+    # Sums of squares below 2^-60 (and all-zero gradients) take the kernel's
+    # exact fp64 path: gradients ~1e-30 (squares underflow fp32), ~1e-20
+    # (squares are fp32 denormals), fp32 denormal gradients and zeros.  The
+    # layout spans several chunks and a ragged tail; norms follow the oracle
+    # to 1e-12 (0 exactly for zeros) and every state element bit for bit.
+    pl = si.from_units([16384 * 2 + 5, 1552, 9])
+    pb = make_problem(pl, 3, 2, grad_dtype=gd, steps=2, seed=91, max_norm=0.5)
+    _scale_grads(pb, scale)
+    norms = _clip_parity(pb, mode="units")
+    if scale == 0.0:
+        assert norms == [0.0, 0.0]
+    else:
+        assert all(0.0 < x < 2.0 ** -30 for x in norms)
+
+
+@pytest.mark.parametrize("gd", ["fp32", "bf16"])
+def test_norm_with_tiny_and_normal_elements_mixed(gd):
+    # Chunk 0: every thread's first group tiny, the rest normal (the fast
+    # path, where the tiny squares' product errors may be lost: far below the
+    # tolerance); chunk 1 entirely tiny (the exact path for all its threads);
+    # the rest normal.  Norms follow the oracle and the stages agree bit for bit.
+    pl = si.from_units([16384 * 3 + 77])
+    out = {}
+    for stage in (0, 2, 3):
+        pb = make_problem(pl, 2, stage, grad_dtype=gd, steps=2, seed=92, max_norm=0.5)
+        _scale_grads(pb, 1e-25, 0, 2048)
+        _scale_grads(pb, 1e-25, 16384, 2 * 16384)
+        _clip_parity(pb, mode="units")
+        norms = []
+        fs = run_gpu(pb, mode="separate", norms=norms)
+        out[stage] = (norms, to_np(fs.master)[:pl.total].copy())
+        fs.close()
+    for stage in (2, 3):
+        assert out[stage][0] == out[0][0]
+        assert np.array_equal(out[stage][1].view(np.uint32), out[0][1].view(np.uint32))

@@ -19,19 +19,22 @@ namespace {
 // the product's rounding error comes exactly from one fma, the sum's from
 // the two-sum identity, giving ~48-bit accuracy at fp32 throughput (fp64 is
 // scarce on this part: a per-element fp64 operation would cap the pass far
-// below HBM speed).  Both error terms are exact while |g| is in
-// [2^-51, 2^60] (or g = 0); other values (and inf/NaN) are summed exactly in
-// fp64 instead, on a separate, rarely taken path.  Elements are added in the
-// same order on every path, so the sum does not depend on which one ran.
+// below HBM speed).
+//
+// The pair is exact as long as nothing overflows and no product error
+// underflows.  Instead of testing every element (a range test per element
+// cost a quarter of the pass's throughput at few replicas: measured on GB300
+// over 2.03 B fp32 elements of two replicas, 5.58 TB/s of reads with the
+// test, 7.45 without), a thread checks its result once: when the pair is not
+// finite (an inf or NaN gradient, or an overflow) or the sum is below 2^-60
+// (where product errors of tiny gradients may have been lost), the thread
+// sums its elements again, in the same order, as fp64 squares (exact) with
+// fp64 additions.  Which way a thread's sum goes is a function of its
+// elements alone, so it is the same on every path.
 struct SqAcc {
   float hi = 0.0f, lo = 0.0f;
-  double wide = 0.0;
 
-  __device__ __forceinline__ static bool in_range(float g) {
-    const float ag = fabsf(g);
-    return ag == 0.0f || (ag >= 0x1p-51f && ag <= 0x1p60f);
-  }
-  __device__ __forceinline__ void add_pair(float g) {
+  __device__ __forceinline__ void add(float g) {
     const float p = __fmul_rn(g, g);
     const float e = __fmaf_rn(g, g, -p);  // exact: g*g = p + e
     const float t = __fadd_rn(hi, p);
@@ -40,42 +43,16 @@ struct SqAcc {
     hi = t;
     lo = __fadd_rn(lo, __fadd_rn(err, e));
   }
-  __device__ __forceinline__ void add_wide(float g) {
-    const double d = static_cast<double>(g);
-    wide = __dadd_rn(wide, __dmul_rn(d, d));
+  __device__ __forceinline__ void add8(const float* g) {
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) add(g[e]);
   }
-  // One element (tails and unaligned gradients).
-  __device__ __forceinline__ void add1(float g) {
-    if (in_range(g)) {
-      add_pair(g);
-    } else {
-      add_wide(g);
-    }
-  }
-  // Eight consecutive elements: one range test for the group.
-  __device__ __forceinline__ void add8(const float* g);
+  // The pair holds the sum to ~48 bits (see above).
+  __device__ __forceinline__ bool exact() const { return isfinite(hi) && isfinite(lo) && hi >= 0x1p-60f; }
   __device__ __forceinline__ double total() const {
-    return __dadd_rn(__dadd_rn(static_cast<double>(hi), static_cast<double>(lo)), wide);
+    return __dadd_rn(static_cast<double>(hi), static_cast<double>(lo));
   }
 };
-
-// Out of line on purpose: inlined, the compiler may evaluate this path for
-// every group.
-__device__ __noinline__ void add8_mixed(SqAcc* acc, const float* g) {
-  for (int e = 0; e < kVec; ++e) acc->add1(g[e]);
-}
-
-__device__ __forceinline__ void SqAcc::add8(const float* g) {
-  bool ok = true;
-#pragma unroll
-  for (int e = 0; e < kVec; ++e) ok = ok & in_range(g[e]);
-  if (ok) {
-#pragma unroll
-    for (int e = 0; e < kVec; ++e) add_pair(g[e]);
-  } else {
-    add8_mixed(this, g);
-  }
-}
 
 // Fixed-order sum of one double per thread across the CTA (warp tree, then
 // warps in order).  Result valid in thread 0.
@@ -159,17 +136,16 @@ __device__ __forceinline__ void keep8(const NormSeg& s, long long e0, const floa
 
 // One CTA per chunk.  Thread t takes the chunk's 8-element groups t, t+256,
 // ... in order and accumulates their elements in order; the vector and the
-// element-wise paths visit elements in the same order, so the chunk's sum does
-// not depend on the gradients' alignment.  Full groups are loaded two at a
-// time before either is accumulated (more bytes in flight per thread; the
-// loose register bound allows it), which does not change the order — except
-// for fp32 gradients from kNormPairMaxRanksFp32 + 1 replicas on: two groups'
-// loads then need more than 128 registers, which leaves one CTA per SM, so
-// those instances load one group at a time at three CTAs per SM (measured on
-// GB300 over 73.5 M elements, GB/s of gradient reads: N = 7 fp32 6988-7012
-// against 6328, N = 8 7054 against 6423, N = 16 7211-7228 against 7122; at
-// N = 5, 6 either way within 1 %; the norm bits are the same, as the order
-// is).
+// element-wise paths visit elements in the same order, so the chunk's sum
+// does not depend on the gradients' alignment.  Full groups are loaded two at a time before either is
+// accumulated (more bytes in flight per thread; the loose register bound
+// allows it), which does not change the order — except for fp32 gradients
+// from kNormPairMaxRanksFp32 + 1 replicas on: two groups' loads then need
+// more than 128 registers, which leaves one CTA per SM, so those instances
+// load one group at a time at three CTAs per SM (measured on GB300 over
+// 73.5 M elements, GB/s of gradient reads: N = 7 fp32 6988-7012 against
+// 6328, N = 8 7054 against 6423, N = 16 7211-7228 against 7122; at N = 5, 6
+// either way within 1 %; the norm bits are the same, as the order is).
 constexpr int kNormPairMaxRanksFp32 = 6;
 
 template <int N, bool kFp32>
@@ -177,6 +153,21 @@ struct NormShape {
   static constexpr bool kPairs = !kFp32 || N <= kNormPairMaxRanksFp32;
   static constexpr int kMinBlocks = kPairs ? 1 : 3;
 };
+
+// A thread's elements of one chunk again, in the same order, as exact fp64
+// squares summed in fp64: the rare path of SqAcc::exact() == false.
+__device__ __noinline__ double exact_thread_sum(const NormArgs& a, const NormSeg& s, long long c0, long long len) {
+  double w = 0.0;
+  for (long long grp = threadIdx.x; grp * kVec < len; grp += kStepThreads) {
+    for (int e = 0; e < kVec; ++e) {
+      if (grp * kVec + e < len) {
+        const double d = static_cast<double>(reduced1(a, s, c0 + grp * kVec + e));
+        w = __dadd_rn(w, __dmul_rn(d, d));
+      }
+    }
+  }
+  return w;
+}
 
 template <int N, bool kFp32>
 __global__ void __launch_bounds__(kStepThreads, NormShape<N, kFp32>::kMinBlocks)
@@ -217,12 +208,13 @@ __global__ void __launch_bounds__(kStepThreads, NormShape<N, kFp32>::kMinBlocks)
         if (grp * kVec + e < len) {
           const float g = reduced1(a, s, e0 + e);
           if (s.keep) s.keep[e0 + e] = g;
-          acc.add1(g);
+          acc.add(g);
         }
       }
     }
   }
-  const double total = block_sum<kStepThreads>(acc.total(), smem);
+  const double mine = acc.exact() ? acc.total() : exact_thread_sum(a, s, c0, len);
+  const double total = block_sum<kStepThreads>(mine, smem);
   if (threadIdx.x == 0) a.partials[s.out_start + k] = total;
 }
 
