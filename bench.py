@@ -35,7 +35,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "stage_buffer_zero1_fp32_n2"
-ALSO_WORKLOADS = ("llama1024_zero2_n8", "llama2048_zero3_n8")
+ALSO_WORKLOADS = ("llama1024_zero2_n8", "llama2048_zero3_n8", "llama2048_zero3_n6", "llama2048_zero3_n6_unitbufs")
 METRIC = "fused ZeRO step params/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
@@ -52,6 +52,16 @@ def workload(name: str):
     if name == "llama2048_zero3_n8":
         return dict(pl=si.llama_2048_units(), n=8, stage=3, grad_dtype="bf16", grad_std=1e-3, per_unit=True,
                     outliers=0.0)
+    if name.startswith("llama2048_zero3_n") and name[len("llama2048_zero3_n"):].split("_")[0].isdigit():
+        # the same units at another N; "_unitbufs": every unit's gradients in
+        # buffers of their own (at N = 3, 6, ... the unit bases are then not
+        # multiples of 8 and the step takes the shifted-gradient kernel)
+        rest = name[len("llama2048_zero3_n"):]
+        n = int(rest.split("_")[0])
+        if rest not in (str(n), f"{n}_unitbufs"):
+            raise SystemExit(f"unknown workload {name}")
+        return dict(pl=si.llama_2048_units(), n=n, stage=3, grad_dtype="bf16", grad_std=1e-3, per_unit=True,
+                    outliers=0.0, unit_bufs=rest.endswith("_unitbufs"))
     if name == "stage_buffer_zero1_fp32_n2":
         return dict(pl=si.llama_2048_stage_buffer(), n=2, stage=1, grad_dtype="fp32", grad_std=1e-3,
                     per_unit=False, outliers=0.0)
@@ -89,12 +99,13 @@ def measured_peaks():
 
 
 def step_kernel_name(n: int, grad_dtype: str, clip_keep: bool, elems: int) -> str:
-    """The step kernel the library launches for this workload: over >= 2^23
+    """The step kernel the library launches for an aligned segment (base a
+    multiple of 8, gradients 16-byte aligned; the others take the
+    shifted-gradient kernel, see Workbench.kernel_name): over >= 2^23
     elements the tile-staged one with 2,048-element tiles for N >= 11 bf16 or
     N = 8, 9 fp32 replicas and the one with 4 elements per thread for N = 7
     or N >= 10 fp32 or N = 1..4 bf16 replicas; the register-staged one
-    otherwise (a kept
-    fp32 reduced gradient is one fp32 replica)."""
+    otherwise (a kept fp32 reduced gradient is one fp32 replica)."""
     if clip_keep:
         n, grad_dtype = 1, "fp32"
     if elems < 2 ** 23:
@@ -380,9 +391,17 @@ class Workbench:
                            init_params=init, device=device, **(offload_kw or {}))
         del init, init_flat
         self.padded = self.fs.padded
-        self.grads = si.replica_grads(n, self.padded, wl["grad_std"], 100 + rank, wl["grad_dtype"], device=device,
-                                      outlier_fraction=wl["outliers"])
         self.units = [self.fs.layout(i) for i in range(self.fs.n_units)]
+        self.unit_grads = None
+        if wl.get("unit_bufs"):
+            # one buffer per unit and replica, as a per-unit gradient hook hands them over
+            self.grads = None
+            self.unit_grads = [si.replica_grads(n, pad, wl["grad_std"], 100 + 31 * i + rank, wl["grad_dtype"],
+                                                device=device, pad_from=numel)
+                               for i, (numel, pad, shard, base) in enumerate(self.units)]
+        else:
+            self.grads = si.replica_grads(n, self.padded, wl["grad_std"], 100 + rank, wl["grad_dtype"],
+                                          device=device, outlier_fraction=wl["outliers"])
         self.micro = []
         if accum > 0:
             if wl["grad_dtype"] != "fp32":
@@ -409,7 +428,10 @@ class Workbench:
                 launches += fs.last_launches()
             if accum_ev is not None:
                 accum_ev[1].record(s)
-        if self.wl["per_unit"]:
+        if self.unit_grads is not None:
+            for i, g in enumerate(self.unit_grads):
+                fs.reduce_grads(i, g)
+        elif self.wl["per_unit"]:
             for i, (numel, pad, shard, base) in enumerate(self.units):
                 fs.reduce_grads(i, [g[base:base + pad] for g in grads])
         else:
@@ -437,10 +459,27 @@ class Workbench:
         fs.post_step()
         return launches
 
+    def shifted_units(self) -> int:
+        """Units whose step segment the shifted-gradient kernel takes (a unit
+        base that is not a multiple of 8 with gradients in a buffer of its
+        own); one flat buffer, or views of it, is one aligned segment."""
+        if self.unit_grads is None:
+            return 0
+        return sum(1 for (numel, pad, shard, base) in self.units if base % 8 and pad)
+
+    def kernel_name(self, clip_keep: bool = False) -> str:
+        n, gd = self.wl["n"], self.wl["grad_dtype"]
+        k = self.shifted_units()
+        if k == 0 or clip_keep:
+            return step_kernel_name(n, gd, clip_keep, self.padded)
+        if k == len(self.units):
+            return "step_shift_kernel"
+        return f"step_shift_kernel ({k} units) + {step_kernel_name(n, gd, False, self.padded)}"
+
     def close(self):
         import torch
         self.fs.close()
-        self.grads = self.micro = self.gather_bufs = None
+        self.grads = self.unit_grads = self.micro = self.gather_bufs = None
         torch.cuda.empty_cache()
 
 
@@ -537,7 +576,7 @@ def also_block(name: str, device, rank: int, args, peak: float) -> dict:
         out = {"config": config_for(name, wl, 1), "padded_params": wb.padded, "steps": steps,
                "warmup": args.warmup, "value": wl["pl"].total * steps / (r["total_ms"] / 1e3), "unit": UNIT,
                "ms_per_step": r["total_ms"] / steps, "bytes_per_param": bpp,
-               "kernel": step_kernel_name(n, wl["grad_dtype"], False, wb.padded),
+               "kernel": wb.kernel_name(),
                **kernel_stats(r["step_ms"], bpp * wb.padded, peak), "gpu_launches": r["launches"],
                "clocks": r["clocks"]}
         if r["gather_ms"]:
@@ -699,8 +738,9 @@ def run_ours(args):
                       "note": "the clipped step is the norm pass (grad_sq + finalize kernels) plus the step kernel"}
 
     e2e = None
-    if not args.no_e2e and not args.offload:
+    if not args.no_e2e and not args.offload and wb.grads is not None:
         e2e = e2e_leg(wb, args.steps, min(args.warmup, 3) + 1, world)
+    kernel = wb.kernel_name(args.clip > 0 and args.clip_keep)
     wb.close()
     del wb, fs
 
@@ -718,7 +758,7 @@ def run_ours(args):
                 "frac": achieved_gbs / peak, "peak_source": f"hbm_gbs {peak_kind}",
                 "traffic": recorded_traffic(args.workload), "algorithmic_bytes_per_launch": bytes_per_launch,
                 "bytes_per_param": bpp, "padded_params": padded,
-                "kernel": step_kernel_name(n, wl["grad_dtype"], args.clip_keep, padded),
+                "kernel": kernel,
                 "kernel_ms_mean": kern_ms_max, "kernel_ms_median": statistics.median(r["step_ms"]),
                 "kernel_ms_min": min(r["step_ms"]),
                 "gbs_at_median": bytes_per_launch / (statistics.median(r["step_ms"]) / 1e3) / 1e9,

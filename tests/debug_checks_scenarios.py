@@ -35,6 +35,10 @@ def main():
     odd = si.from_units([1552, 7, 9312, 33, 17])
     scenario("odd units N = 3 (padding, unaligned unit starts)", make_problem(odd, 3, 3, steps=2, seed=210))
     scenario("odd units N = 16 fp32", make_problem(odd, 16, 2, grad_dtype="fp32", steps=2, seed=211))
+    scenario("odd units N = 3, one buffer per unit (shifted gradients)", make_problem(odd, 3, 3, steps=2, seed=222),
+             mode="separate")
+    scenario("odd units N = 5 fp32, one buffer per unit (shifted gradients)",
+             make_problem(odd, 5, 2, grad_dtype="fp32", steps=2, seed=223), mode="separate")
     big = si.from_units([4_200_005, 1552, 2_500_000, 7, 2_000_000])
     scenario("tile-staged N = 16 bf16", make_problem(big, 16, 2, steps=1, seed=212), mode="separate")
     scenario("tile-staged N = 9 fp32", make_problem(big, 9, 3, grad_dtype="fp32", steps=1, seed=213), mode="all")

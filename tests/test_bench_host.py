@@ -88,3 +88,13 @@ def test_config_is_a_function_of_the_workload_only():
     a, b = bench.config_for("llama2048_zero3_n8", wl, 1), bench.config_for("llama2048_zero3_n8", wl, 1)
     assert a == b and a["units"] == 10 and a["zero_stage"] == 3
     assert bench.config_for("toy_mlp_n4", bench.workload("toy_mlp_n4"), 1)["l2"].startswith("working set fits L2")
+
+
+def test_llama2048_workloads_at_other_rank_counts():
+    wl = bench.workload("llama2048_zero3_n6_unitbufs")
+    assert (wl["n"], wl["stage"], wl["unit_bufs"], wl["pl"].n_units) == (6, 3, True, 10)
+    wl = bench.workload("llama2048_zero3_n3")
+    assert (wl["n"], wl["unit_bufs"]) == (3, False)
+    for bad in ("llama2048_zero3_n6_x", "llama2048_zero3_nx"):
+        with pytest.raises(SystemExit):
+            bench.workload(bad)

@@ -64,14 +64,21 @@ struct StepArgs {
   int inject_missing_copy; // test hook: the tile-staged kernel announces the
                            // launch's first tile but issues none of its copies
   Seg seg[kMaxSegs];
+  // Shifted-gradient kernel only: segment s's body starts at seg[s].base (a
+  // multiple of kVec), its head[s] < kVec elements before it are the body's
+  // elements -head[s] .. -1, and replica r's gradient at the body's start
+  // lies gshift[s][r] elements past a 16-byte boundary.
+  unsigned char head[kMaxSegs];
+  unsigned char gshift[kMaxSegs][kMaxRanks];
 };
 
 // Launchers.  Each returns the cudaError_t of its launch.
 // Vector kernel: every segment has base % kVec == 0 and 16-byte aligned
 // gradient pointers; the last kVec-1 elements of a segment may be ragged.
 cudaError_t launch_step_vec(const StepArgs& a, cudaStream_t stream);
-// Scalar kernel: any alignment (used for segments the vector kernel cannot take).
-cudaError_t launch_step_scalar(const StepArgs& a, cudaStream_t stream);
+// Shifted-gradient kernel: segments of any alignment, described by their
+// aligned body, head and per-replica gradient shift (see StepArgs).
+cudaError_t launch_step_shift(const StepArgs& a, cudaStream_t stream);
 
 // Multiprocessor count of the current device (cached per device).
 int sm_count();

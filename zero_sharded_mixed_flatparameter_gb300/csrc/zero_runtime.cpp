@@ -252,6 +252,11 @@ void fill_scalars(const zero_ctx* ctx, int64_t t, zfs::StepArgs* a) {
 struct PlannedSeg {
   int64_t base, len;
   const void* g[zfs::kMaxRanks];
+  // Segments for the shifted-gradient kernel: base, len and g describe the
+  // aligned body; head elements precede it; shift[r] is replica r's gradient
+  // offset from a 16-byte boundary at the body's start, in elements.
+  int head = 0;
+  unsigned char shift[zfs::kMaxRanks] = {};
 };
 
 // One segment per non-empty unit, merged with the previous one when every
@@ -291,6 +296,23 @@ bool vector_ok(const PlannedSeg& s, int N) {
   return true;
 }
 
+// A segment the aligned kernels cannot take, as the shifted-gradient kernel
+// takes it: the first (kVec - base % kVec) % kVec elements become the head,
+// so that the body's state arrays are aligned, and each replica's gradient
+// offset from a 16-byte boundary at the body's start is recorded.
+PlannedSeg peel(const PlannedSeg& s, int N, size_t esz) {
+  PlannedSeg out = s;
+  const int64_t h = std::min<int64_t>(s.len, (zfs::kVec - s.base % zfs::kVec) % zfs::kVec);
+  out.head = static_cast<int>(h);
+  out.base = s.base + h;
+  out.len = s.len - h;
+  for (int r = 0; r < N; ++r) {
+    out.g[r] = static_cast<const char*>(s.g[r]) + h * static_cast<int64_t>(esz);
+    out.shift[r] = static_cast<unsigned char>((reinterpret_cast<uintptr_t>(out.g[r]) % 16) / esz);
+  }
+  return out;
+}
+
 // Launch one kernel per batch of up to kMaxSegs segments of one kind.
 zero_status launch_batches(zero_ctx* ctx, const std::vector<PlannedSeg>& segs, bool vec, int64_t t,
                            cudaStream_t stream, int32_t* launches) {
@@ -322,13 +344,15 @@ zero_status launch_batches(zero_ctx* ctx, const std::vector<PlannedSeg>& segs, b
       s.len = segs[i].len;
       s.vec_start = vecs;
       for (int r = 0; r < N; ++r) s.g[r] = segs[i].g[r];
+      a.head[n] = static_cast<unsigned char>(segs[i].head);
+      for (int r = 0; r < N; ++r) a.gshift[n][r] = segs[i].shift[r];
       vecs += s.len / zfs::kVec;
-      elems += s.len;
+      elems += s.len + segs[i].head;
     }
     a.nseg = n;
     a.total_vec = vecs;
     a.total_elems = elems;
-    const cudaError_t e = vec ? zfs::launch_step_vec(a, stream) : zfs::launch_step_scalar(a, stream);
+    const cudaError_t e = vec ? zfs::launch_step_vec(a, stream) : zfs::launch_step_shift(a, stream);
     if (e != cudaSuccess) return fail_cuda(ctx, "step kernel launch", e);
     ++*launches;
   }
@@ -700,17 +724,21 @@ zero_status zero_step(zero_ctx* ctx, void* stream) {
       launches = 1;
     }
   } else {
-    std::vector<PlannedSeg> vec_segs, scalar_segs;
+    std::vector<PlannedSeg> vec_segs, shift_segs;
     try {
       for (const PlannedSeg& sg : build_segments(ctx)) {
-        (vector_ok(sg, ctx->cfg.n_ranks) ? vec_segs : scalar_segs).push_back(sg);
+        if (vector_ok(sg, ctx->cfg.n_ranks)) {
+          vec_segs.push_back(sg);
+        } else {
+          shift_segs.push_back(peel(sg, ctx->cfg.n_ranks, grad_bytes(ctx->cfg)));
+        }
       }
     } catch (const std::bad_alloc&) {
       return fail(ctx, ZERO_ENOMEM, "cannot allocate segment list");
     }
     st = launch_batches(ctx, vec_segs, true, t, s, &launches);
     if (st != ZERO_OK) return st;
-    st = launch_batches(ctx, scalar_segs, false, t, s, &launches);
+    st = launch_batches(ctx, shift_segs, false, t, s, &launches);
     if (st != ZERO_OK) return st;
   }
   if (ctx->inject == ZERO_INJECT_SHORT_BOUNDS) ctx->inject = 0;

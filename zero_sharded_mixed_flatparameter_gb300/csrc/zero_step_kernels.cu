@@ -620,22 +620,176 @@ __global__ void __launch_bounds__(kThreads, 1) step_tma4_kernel(const __grid_con
 }
 
 // ---------------------------------------------------------------------------
-// Scalar kernel: one element per thread-iteration, any alignment, any N.
+// Kernel for segments the aligned kernels cannot take: the segment's flat
+// base is not a multiple of 8, or a replica's gradient is not 16-byte aligned
+// where the segment's 8-element vectors start.  Padding every unit to a
+// multiple of N (CMU 15-779 Lecture 13 notes §3.6) moves later unit bases
+// off 8-element boundaries for many layouts and rank counts, and gradients
+// that arrive as one buffer per unit are each aligned on their own.
+//
+// The host peels the segment's first (8 - base % 8) % 8 elements (the head)
+// so that the body's master, m, v and bf16 parameters are 16-byte aligned,
+// and records per replica how many elements (phi) its gradient sits past a
+// 16-byte boundary at the body's start.  A thread takes 8 body elements per
+// iteration as step_vec8 does; for a replica with phi != 0 it loads the
+// aligned 16-byte word that holds the vector's first elements, takes the
+// next word from the neighbouring lane by warp shuffle (that lane loaded it
+// as its own first word), loads it itself only where the neighbour holds
+// another vector, and funnel-shifts the 32 bytes into place.  DRAM traffic is
+// that of the aligned kernel; the arithmetic and its order are step_vec8's,
+// so the results are bit-identical.  Heads and ragged ends (at most 7
+// elements each per segment) go element by element.
 // ---------------------------------------------------------------------------
-template <bool kDevBias>
-__global__ void __launch_bounds__(kStepThreads) step_scalar_kernel(const __grid_constant__ StepArgs a) {
+constexpr unsigned kFullWarp = 0xffffffffu;
+
+// Elements phi .. phi + 7 of the 16 bf16 in (lo, hi), 0 <= phi < 8.
+__device__ __forceinline__ uint4 shift_bf16x8(const uint4& lo, const uint4& hi, int phi) {
+  const uint32_t u[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  const int k = phi >> 1;  // whole 32-bit words
+  uint32_t t[6], v[5];
+#pragma unroll
+  for (int i = 0; i < 6; ++i) t[i] = (k & 2) ? u[i + 2] : u[i];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) v[i] = (k & 1) ? t[i + 1] : t[i];
+  const uint32_t sh = static_cast<uint32_t>(phi & 1) * 16;  // and a half word
+  return make_uint4(__funnelshift_r(v[0], v[1], sh), __funnelshift_r(v[1], v[2], sh),
+                    __funnelshift_r(v[2], v[3], sh), __funnelshift_r(v[3], v[4], sh));
+}
+
+// Elements phi .. phi + 7 of the 12 fp32 in (w0, w1, w2), 0 <= phi < 4.
+__device__ __forceinline__ void shift_f32x8(const float4& w0, const float4& w1, const float4& w2, int phi, float* x) {
+  const float u[12] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w, w2.x, w2.y, w2.z, w2.w};
+  float t[9];
+#pragma unroll
+  for (int i = 0; i < 9; ++i) t[i] = (phi & 2) ? u[i + 2] : u[i];
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) x[i] = (phi & 1) ? t[i + 1] : t[i];
+}
+
+__device__ __forceinline__ float4 u4_as_f4(const uint4& w) {
+  return make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w));
+}
+
+__device__ __forceinline__ uint4 shfl_down_u4(const uint4& w) {
+  return make_uint4(__shfl_down_sync(kFullWarp, w.x, 1), __shfl_down_sync(kFullWarp, w.y, 1),
+                    __shfl_down_sync(kFullWarp, w.z, 1), __shfl_down_sync(kFullWarp, w.w, 1));
+}
+
+// One iteration of the shifted-gradient kernel: vector vi of segment si.
+// Called by every lane of the warp (the shuffles need all 32).  `active`: vi
+// is a vector of the segment; `own_next`: the next lane does not hold vector
+// vi + 1 (it is lane 31's successor, or inactive, or at the stride's wrap),
+// so this lane loads the word past its vector itself.  Every load of the
+// iteration — gradient words, that extra word, master, m, v — is issued
+// before any of them is used, as in step_vec8; the shuffles then pass each
+// lane its neighbour's first word.
+template <int N, bool kFp32>
+__device__ __forceinline__ void shifted_vec8(const StepArgs& a, const Seg& s, int si, long long vi, bool active,
+                                             bool own_next, float clip, float bc1, float bc2) {
+  const long long j = s.base + vi * kVec;
+  const bool ok = active && ZFS_CHECK(vi >= 0 && (vi + 1) * kVec <= s.len && j >= 0 && j + kVec <= a.total_padded);
+  constexpr int kWords = kFp32 ? 2 : 1;  // 16-byte words per replica and vector
+  uint4 w[N][kWords + 1];
+#pragma unroll
+  for (int r = 0; r < N; ++r) {
+    const int phi = a.gshift[si][r];
+    const uint4* base = reinterpret_cast<const uint4*>(static_cast<const char*>(s.g[r]) - phi * (kFp32 ? 4 : 2)) +
+                        vi * kWords;
+#pragma unroll
+    for (int q = 0; q < kWords; ++q) w[r][q] = ok ? ld_stream(base + q) : make_uint4(0u, 0u, 0u, 0u);
+    w[r][kWords] = (ok && own_next && phi != 0) ? ld_stream(base + kWords) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  const float4 zero = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  const float4 w0 = ok ? ld_stream_f4(a.master + j) : zero, w1 = ok ? ld_stream_f4(a.master + j + 4) : zero;
+  const float4 m0 = ok ? ld_stream_f4(a.m + j) : zero, m1 = ok ? ld_stream_f4(a.m + j + 4) : zero;
+  const float4 v0 = ok ? ld_stream_f4(a.v + j) : zero, v1 = ok ? ld_stream_f4(a.v + j + 4) : zero;
+  float g[kVec];
+#pragma unroll
+  for (int r = 0; r < N; ++r) {
+    const int phi = a.gshift[si][r];  // uniform over the launch
+    float x[kVec];
+    if (phi != 0) {
+      const uint4 nb = shfl_down_u4(w[r][0]);
+      if (!own_next) w[r][kWords] = nb;
+    }
+    if constexpr (!kFp32) {
+      const uint4 y = phi != 0 ? shift_bf16x8(w[r][0], w[r][1], phi) : w[r][0];
+      x[0] = bf16_lo(y.x); x[1] = bf16_hi(y.x); x[2] = bf16_lo(y.y); x[3] = bf16_hi(y.y);
+      x[4] = bf16_lo(y.z); x[5] = bf16_hi(y.z); x[6] = bf16_lo(y.w); x[7] = bf16_hi(y.w);
+    } else {
+      shift_f32x8(u4_as_f4(w[r][0]), u4_as_f4(w[r][1]), u4_as_f4(w[r][2]), phi, x);
+    }
+    if (r == 0) {
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) g[e] = x[e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) g[e] = __fadd_rn(g[e], x[e]);
+    }
+  }
+  if (!ok) return;
+  float wv[kVec] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  float mv[kVec] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+  float vv[kVec] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) adam(a, bc1, bc2, __fmul_rn(__fmul_rn(g[e], a.inv_n), clip), wv[e], mv[e], vv[e]);
+  st_stream_f4(a.master + j, make_float4(wv[0], wv[1], wv[2], wv[3]));
+  st_stream_f4(a.master + j + 4, make_float4(wv[4], wv[5], wv[6], wv[7]));
+  st_stream_f4(a.m + j, make_float4(mv[0], mv[1], mv[2], mv[3]));
+  st_stream_f4(a.m + j + 4, make_float4(mv[4], mv[5], mv[6], mv[7]));
+  st_stream_f4(a.v + j, make_float4(vv[0], vv[1], vv[2], vv[3]));
+  st_stream_f4(a.v + j + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
+  uint4 out;
+  out.x = pack_bf16x2(wv[0], wv[1]);
+  out.y = pack_bf16x2(wv[2], wv[3]);
+  out.z = pack_bf16x2(wv[4], wv[5]);
+  out.w = pack_bf16x2(wv[6], wv[7]);
+  st_stream(a.p16 + j, out);
+}
+
+// One head or tail element k of the body (k < 0: the head) of segment si.
+__device__ __forceinline__ void shifted_element(const StepArgs& a, const Seg& s, int si, long long k, float clip,
+                                                float bc1, float bc2) {
+  const long long j = s.base + k;
+  if (!ZFS_CHECK(k >= -static_cast<long long>(a.head[si]) && k < s.len && j >= 0 && j < a.total_padded)) return;
+  const float g = __fmul_rn(reduce_scalar(a, s, k), clip);
+  float w = a.master[j], m = a.m[j], v = a.v[j];
+  adam(a, bc1, bc2, g, w, m, v);
+  a.master[j] = w;
+  a.m[j] = m;
+  a.v[j] = v;
+  a.p16[j] = to_bf16_bits(w);
+}
+
+template <int N, bool kFp32, bool kDevBias>
+__global__ void __launch_bounds__(kStepThreads, 1) step_shift_kernel(const __grid_constant__ StepArgs a) {
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const int lane = threadIdx.x & 31;
   float bc1, bc2;
-  if (!step_bias<kDevBias>(a, &bc1, &bc2)) return;
+  if (!step_bias<kDevBias>(a, &bc1, &bc2)) return;  // the same for every thread
   const float clip = a.clip ? *a.clip : 1.0f;
-  long long start = 0;
-  for (int s = 0; s < a.nseg; ++s) {
-    const Seg& seg = a.seg[s];
-    for (long long k = first_index(tid, start, stride); k < seg.len; k += stride) {
-      step_scalar_element(a, seg, k, clip, bc1, bc2);
+  for (int si = 0; si < a.nseg; ++si) {
+    const Seg& seg = a.seg[si];
+    const long long nvec = seg.len / kVec;
+    // The loop runs while any lane of the warp has a vector: the shuffles
+    // need every lane.
+    for (long long vi = first_index(tid, seg.vec_start, stride); __any_sync(kFullWarp, vi < nvec); vi += stride) {
+      const bool active = vi < nvec;
+      const long long nb_vi = __shfl_down_sync(kFullWarp, vi, 1);
+      const int nb_active = __shfl_down_sync(kFullWarp, active ? 1 : 0, 1);
+      const bool own_next = !(lane < 31 && nb_active && nb_vi == vi + 1);
+      shifted_vec8<N, kFp32>(a, seg, si, vi, active, own_next, clip, bc1, bc2);
     }
-    start += seg.len;
+  }
+  // Heads and ragged ends: 16 threads per segment, at most 7 + 7 elements.
+  for (int si = 0; si < a.nseg; ++si) {
+    const Seg& seg = a.seg[si];
+    const long long q = tid - static_cast<long long>(si) * 2 * kVec;
+    if (q < 0 || q >= 2 * kVec) continue;
+    const long long head = a.head[si];
+    const long long k = q < head ? q - head : (seg.len / kVec) * kVec + (q - head);
+    if (q < head || (q - head < kVec && k < seg.len)) shifted_element(a, seg, si, k, clip, bc1, bc2);
   }
 }
 
@@ -678,7 +832,7 @@ struct DeviceInfo {
   int sms = 0;
   // [device-side bias][fp32 gradients][N]
   int vec_blocks_per_sm[2][2][kMaxRanks + 1] = {};
-  int scalar_blocks_per_sm[2] = {};
+  int shift_blocks_per_sm[2][2][kMaxRanks + 1] = {};
   // Staged kernels whose dynamic shared memory limit is raised on the device.
   const void* smem_set[kMaxSmemKernels] = {};
   int n_smem_set = 0;
@@ -885,14 +1039,43 @@ cudaError_t launch_step_vec_t(const StepArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <bool kFp32, bool kDevBias>
+StepKernel shift_kernel_for(int n) {
+  switch (n) {
+    case 1: return step_shift_kernel<1, kFp32, kDevBias>;
+    case 2: return step_shift_kernel<2, kFp32, kDevBias>;
+    case 3: return step_shift_kernel<3, kFp32, kDevBias>;
+    case 4: return step_shift_kernel<4, kFp32, kDevBias>;
+    case 5: return step_shift_kernel<5, kFp32, kDevBias>;
+    case 6: return step_shift_kernel<6, kFp32, kDevBias>;
+    case 7: return step_shift_kernel<7, kFp32, kDevBias>;
+    case 8: return step_shift_kernel<8, kFp32, kDevBias>;
+    case 9: return step_shift_kernel<9, kFp32, kDevBias>;
+    case 10: return step_shift_kernel<10, kFp32, kDevBias>;
+    case 11: return step_shift_kernel<11, kFp32, kDevBias>;
+    case 12: return step_shift_kernel<12, kFp32, kDevBias>;
+    case 13: return step_shift_kernel<13, kFp32, kDevBias>;
+    case 14: return step_shift_kernel<14, kFp32, kDevBias>;
+    case 15: return step_shift_kernel<15, kFp32, kDevBias>;
+    case 16: return step_shift_kernel<16, kFp32, kDevBias>;
+    default: return nullptr;
+  }
+}
+
 template <bool kDevBias>
-cudaError_t launch_step_scalar_t(const StepArgs& a, cudaStream_t stream) {
+cudaError_t launch_step_shift_t(const StepArgs& a, cudaStream_t stream) {
+  StepKernel k = a.grad_fp32 ? shift_kernel_for<true, kDevBias>(a.n_ranks) : shift_kernel_for<false, kDevBias>(a.n_ranks);
+  if (!k) return cudaErrorInvalidValue;
   const int dev = current_device();
   const int sms = cached_sms(dev);
-  const int bps = resident_blocks(&g_info[dev].scalar_blocks_per_sm[kDevBias ? 1 : 0],
-                                  reinterpret_cast<const void*>(step_scalar_kernel<kDevBias>));
-  const long long grid = grid_for(a.total_elems, sms, bps);
-  step_scalar_kernel<kDevBias><<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(a);
+  int bps = resident_blocks(&g_info[dev].shift_blocks_per_sm[kDevBias ? 1 : 0][a.grad_fp32 ? 1 : 0][a.n_ranks],
+                            reinterpret_cast<const void*>(k));
+  if (bps > kStepCtasPerSm) bps = kStepCtasPerSm;  // as the register-staged kernel
+  // enough threads for the heads and ragged ends: 16 per segment
+  long long work = a.total_vec;
+  if (work < static_cast<long long>(a.nseg) * 2 * kVec) work = static_cast<long long>(a.nseg) * 2 * kVec;
+  const long long grid = grid_for(work, sms, bps);
+  k<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -900,8 +1083,8 @@ cudaError_t launch_step_vec(const StepArgs& a, cudaStream_t stream) {
   return a.dev_t ? launch_step_vec_t<true>(a, stream) : launch_step_vec_t<false>(a, stream);
 }
 
-cudaError_t launch_step_scalar(const StepArgs& a, cudaStream_t stream) {
-  return a.dev_t ? launch_step_scalar_t<true>(a, stream) : launch_step_scalar_t<false>(a, stream);
+cudaError_t launch_step_shift(const StepArgs& a, cudaStream_t stream) {
+  return a.dev_t ? launch_step_shift_t<true>(a, stream) : launch_step_shift_t<false>(a, stream);
 }
 
 cudaError_t launch_count_step(long long* t, cudaStream_t stream) {
