@@ -2,6 +2,8 @@
 // gradient-norm pass of global-norm clipping, fp32 gradient accumulation,
 // make_master's fills and copies, checkpoint copies and the ZeRO-3 gather.
 
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -371,11 +373,53 @@ __global__ void gather_vec_kernel(const uint4* __restrict__ src, uint4* __restri
   if (i < n16) dst[i] = src[i];
 }
 
-__global__ void gather_scalar_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
-                                     long long begin, long long n) {
-  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long k = begin + tid; k < n; k += stride) dst[k] = src[k];
+// Units that are not 16-byte aligned on both sides, or not a whole number
+// of vectors (a unit's flat base is not a multiple of 8 when padding to a
+// multiple of N moved it, CMU 15-779 Lecture 13 notes §3.6): the first
+// `head` elements are copied one by one so that the destination is aligned
+// from there on; thread i then writes destination vector i, built from the
+// aligned source word that holds its first element, shifted by phi elements
+// with the next word — which the neighbouring lane loaded as its own (warp
+// shuffle), or, for lane 31 and the last vector, this lane loads itself.
+// The threads after the last vector copy the head and the ragged tail.
+__global__ void gather_shift_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, long long n,
+                                    int head, int phi, long long nvec) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const bool active = i < nvec;
+  const uint4* words = reinterpret_cast<const uint4*>(src + head - phi);  // 16-byte aligned
+  const bool own_next = active && (lane == 31 || i + 1 >= nvec);
+  uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = make_uint4(0u, 0u, 0u, 0u);
+  if (active && ZFS_CHECK(head + 8 * i + 8 <= n)) {
+    w0 = words[i];
+    if (own_next && phi != 0) w1 = words[i + 1];
+  }
+  if (phi != 0) {  // uniform over the launch; every lane takes part in the shuffle
+    const uint4 nb = make_uint4(__shfl_down_sync(0xffffffffu, w0.x, 1), __shfl_down_sync(0xffffffffu, w0.y, 1),
+                                __shfl_down_sync(0xffffffffu, w0.z, 1), __shfl_down_sync(0xffffffffu, w0.w, 1));
+    if (!own_next) w1 = nb;
+  }
+  if (active && ZFS_CHECK(head + 8 * i + 8 <= n)) {
+    uint4 out = w0;
+    if (phi != 0) {
+      const uint32_t u[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      const int k = phi >> 1;
+      uint32_t t[6], v[5];
+#pragma unroll
+      for (int q = 0; q < 6; ++q) t[q] = (k & 2) ? u[q + 2] : u[q];
+#pragma unroll
+      for (int q = 0; q < 5; ++q) v[q] = (k & 1) ? t[q + 1] : t[q];
+      const uint32_t sh = static_cast<uint32_t>(phi & 1) * 16;
+      out = make_uint4(__funnelshift_r(v[0], v[1], sh), __funnelshift_r(v[1], v[2], sh),
+                       __funnelshift_r(v[2], v[3], sh), __funnelshift_r(v[3], v[4], sh));
+    }
+    reinterpret_cast<uint4*>(dst + head)[i] = out;
+  }
+  const long long q = i - nvec;  // head and tail: at most 7 + 7 elements
+  if (q >= 0 && q < 16) {
+    const long long k = q < head ? q : head + 8 * nvec + (q - head);
+    if ((q < head || q - head < 8) && k < n) dst[k] = src[k];
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -539,28 +583,25 @@ cudaError_t launch_copy_f32(const float* src, float* dst, long long n, cudaStrea
 cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaStream_t stream, int* launches) {
   if (n <= 0) return cudaSuccess;
   const bool aligned = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (reinterpret_cast<uintptr_t>(dst) % 16 == 0);
-  long long begin = 0;
-  if (aligned) {
+  if (aligned && n % 8 == 0) {
+    // one thread per vector: under 2^31 blocks for any unit a device can hold
     const long long n16 = n / 8;
-    if (n16 > 0) {
-      // one thread per vector: under 2^31 blocks for any unit a device can hold
-      const long long grid = (n16 + kStepThreads - 1) / kStepThreads;
-      gather_vec_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(
-          reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), n16);
-      const cudaError_t e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
-      ++*launches;
-    }
-    begin = n16 * 8;
+    const long long grid = (n16 + kStepThreads - 1) / kStepThreads;
+    gather_vec_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(
+        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), n16);
+  } else {
+    // the destination aligned after `head` elements; the source's offset
+    // from a 16-byte boundary there, in elements
+    const long long head = std::min<long long>(n, (8 - static_cast<long long>(reinterpret_cast<uintptr_t>(dst) / 2 % 8)) % 8);
+    const int phi = static_cast<int>(reinterpret_cast<uintptr_t>(src + head) / 2 % 8);
+    const long long nvec = (n - head) / 8;
+    const long long grid = (nvec + 2 * kVec + kStepThreads - 1) / kStepThreads;
+    gather_shift_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(src, dst, n, static_cast<int>(head),
+                                                                                   phi, nvec);
   }
-  if (begin < n) {
-    const long long grid = grid_for(n - begin, sm_count(), 8);
-    gather_scalar_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(src, dst, begin, n);
-    const cudaError_t e = cudaGetLastError();
-    if (e == cudaSuccess) ++*launches;
-    return e;
-  }
-  return cudaSuccess;
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ++*launches;
+  return e;
 }
 
 }  // namespace zfs
