@@ -55,12 +55,15 @@
 //    near one fp64 ulp instead of the n * 2^-53 bound of a plain running sum.
 //    Coefficient min(1, max_norm / (norm + 1e-6)) evaluated in fp64 and
 //    rounded once to fp32; the reduced gradient is multiplied by it (one fp32
-//    multiply) before Adam.
+//    multiply) before Adam.  The cap at 1 keeps a NaN (torch's
+//    clip_grad_norm_ clamps the coefficient with torch.clamp, which passes
+//    NaN through): a NaN norm makes every clipped gradient NaN.
 //
 // Parity pins: every function here is pinned by a "not gpu" test against
 // values printed on the pages, closed forms, invariants or brute force.
 
 #include <cmath>
+#include <limits>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -219,9 +222,10 @@ double grad_norm(const Hyper& h, const StepScalars& s, const void* const* grads,
 }
 
 // Clip coefficient: scale the gradient down to max_norm when its norm is
-// larger; 1 otherwise.
+// larger; 1 otherwise; NaN when the norm is NaN.
 float clip_coefficient(double norm, float max_norm) {
   const double coef = static_cast<double>(max_norm) / (norm + 1e-6);
+  if (std::isnan(coef)) return std::numeric_limits<float>::quiet_NaN();
   return coef < 1.0 ? static_cast<float>(coef) : 1.0f;
 }
 

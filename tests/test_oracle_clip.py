@@ -78,9 +78,34 @@ def test_norm_of_non_finite_gradients(oracle_lib):
     h2 = Hyper(n_ranks=2)
     assert oracle_lib.grad_norm(h2, [top, top]) == math.inf
     # the coefficient: an infinite norm scales everything to 0, a NaN norm
-    # leaves the gradient unscaled (the reading taken for NaN)
+    # gives a NaN coefficient (the cap at 1 passes NaN through)
     assert oracle_lib.clip_coef(math.inf, 1.0) == 0.0
-    assert oracle_lib.clip_coef(math.nan, 1.0) == 1.0
+    assert math.isnan(oracle_lib.clip_coef(math.nan, 1.0))
+
+
+def test_non_finite_clip_follows_torch_clip_grad_norm(oracle_lib):
+    # torch's own clip_grad_norm_ (the routine whose convention the clipping
+    # follows) on the reduced gradient: a NaN anywhere makes every clipped
+    # gradient NaN; an inf makes that element NaN (inf * 0) and every other 0.
+    # The oracle's clipped first step must show the same pattern: a NaN
+    # gradient turns the whole state NaN, an inf gradient that element only
+    # (the others see g = 0: m = v = 0 and the weight keeps its value).
+    h = Hyper(n_ranks=1, grad_dtype="fp32")
+    for bad in (math.nan, math.inf):
+        g = np.array([0.5, -0.25, bad, 2.0], np.float32)
+        p = torch.nn.Parameter(torch.zeros(4))
+        p.grad = torch.from_numpy(g.copy())
+        torch.nn.utils.clip_grad_norm_([p], max_norm=1.0)
+        clipped = p.grad.numpy()
+        lay = oracle_lib.layout([4], [0], 1, 1)
+        w0 = np.array([1.0, 2.0, 3.0, 4.0], np.float32)
+        master, m, v, p16 = oracle_lib.make_master([4], lay, [w0])
+        oracle_lib.zero_step(h, 1, 1, lay, [g], master, m, v, p16, max_norm=1.0)
+        # the oracle's clipped gradient is m / (1 - beta1) after one step from m = 0
+        assert np.array_equal(np.isnan(clipped), np.isnan(m)), (bad, clipped, m)
+        finite = ~np.isnan(clipped)
+        assert np.array_equal(clipped[finite] == 0.0, m[finite] == 0.0)
+        assert np.array_equal(np.isnan(master), np.isnan(clipped))
 
 
 def test_clip_coefficient(oracle_lib):
