@@ -28,6 +28,7 @@ from .oracle import (  # noqa: F401
     layout,
     library_path,
     make_master,
+    nonfinite_count,
     reduce_element,
     state_bytes,
     step_scalars,

@@ -78,6 +78,8 @@ def _load():
         lib.oracle_grad_norm.restype = ctypes.c_double
         lib.oracle_clip_coef.argtypes = [ctypes.c_double, f32]
         lib.oracle_clip_coef.restype = f32
+        lib.oracle_nonfinite_count.argtypes = [vp, vp, i64, vp]
+        lib.oracle_nonfinite_count.restype = i64
         lib.oracle_step_window.restype = None
         lib.oracle_export.argtypes = [i32, vp, vp, vp, vp]
         lib.oracle_export.restype = None
@@ -266,6 +268,14 @@ def grad_norm(hyper: Hyper, grads) -> float:
     f, i = hyper.pack()
     arrs, ptrs = _grad_ptrs(grads, hyper)
     return float(lib.oracle_grad_norm(_ptr(f), _ptr(i), arrs[0].size, ptrs))
+
+
+def nonfinite_count(hyper: Hyper, grads) -> int:
+    """Elements whose reduced gradient (rank-order fp32 sum x 1/N) is inf or NaN."""
+    lib = _load()
+    f, i = hyper.pack()
+    arrs, ptrs = _grad_ptrs(grads, hyper)
+    return int(lib.oracle_nonfinite_count(_ptr(f), _ptr(i), arrs[0].size, ptrs))
 
 
 def clip_coef(norm: float, max_norm: float) -> float:

@@ -404,6 +404,21 @@ double oracle_grad_norm(const float* hyper_f, const int32_t* hyper_i, int64_t n,
 
 float oracle_clip_coef(double norm, float max_norm) { return clip_coefficient(norm, max_norm); }
 
+// How many flat elements j in [0, n) have a reduced gradient (the rank-order
+// fp32 sum times 1/N, before any clipping) that is not finite: a replica
+// holds an inf or a NaN there, or the fp32 sum of the replicas overflows.
+// This is what the overflow check at the start of DeepSpeed's ZeRO step
+// looks for (source guide §4.3: step() checks for overflow, then clips).
+int64_t oracle_nonfinite_count(const float* hyper_f, const int32_t* hyper_i, int64_t n, const void* const* grads) {
+  const Hyper h = hyper_from(hyper_f, hyper_i);
+  const StepScalars s = step_scalars(h, 1);
+  int64_t count = 0;
+  for (int64_t j = 0; j < n; ++j) {
+    if (!std::isfinite(reduce_element(h, s, grads, j))) ++count;
+  }
+  return count;
+}
+
 // The fp32 scalars of step t (exposed for pinning):
 // out = {1-beta1, 1-beta2, bc1, bc2, decay, 1/N}.
 void oracle_step_scalars(const float* hyper_f, const int32_t* hyper_i, int64_t t, float* out) {
