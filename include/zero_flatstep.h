@@ -235,13 +235,43 @@ zero_status zero_step(zero_ctx* ctx, void* stream);
 zero_status zero_clip_workspace_bytes(const zero_ctx* ctx, int64_t* bytes);
 
 /*
+ * zero_count_nonfinite — overflow count of the step.  DeepSpeed's ZeRO step
+ * checks the gradients for overflow before it clips and updates (source guide
+ * §4.3); here the fused step counts, at no extra memory traffic, the elements
+ * whose reduced gradient g = (sum of the N replicas, rank order, fp32) / N is
+ * inf or NaN — a non-finite replica gradient or an fp32 overflow of the sum —
+ * and adds that number to *counter.  Every later zero_step (and
+ * zero_offload_step) of this context counts, clipped or not; the step is
+ * taken all the same (the non-finite values propagate as IEEE arithmetic
+ * makes them), so a caller that wants to skip such steps clips first and
+ * reads zero_grad_norm, or restores a checkpoint when the count moves.
+ *  counter  caller-owned device uint64_t, 8-byte aligned, on the context's
+ *           device; the library adds to it and never clears it (the caller
+ *           zeroes it, e.g. with cudaMemsetAsync, for a fresh count) and it
+ *           must stay allocated while counting is on.  NULL stops counting.
+ * Errors: ZERO_EINVAL (misaligned, host or other-device counter).
+ */
+zero_status zero_count_nonfinite(zero_ctx* ctx, uint64_t* counter);
+
+/*
+ * zero_read_nonfinite — waits for `stream` and copies the counter given to
+ * zero_count_nonfinite into *count.  ZERO_ESTATE when no counter is set;
+ * ZERO_ECUDA if the copy fails.
+ */
+zero_status zero_read_nonfinite(zero_ctx* ctx, uint64_t* count, void* stream);
+
+/*
  * zero_clip_grad_norm — global-norm gradient clipping, the ClipGradNorm
  * transform Femtotron dev logs #4/#5 apply to the fp32 gradient before AdamW
  * (the source guide's --clip-grad 1.0 / gradient_clipping 1.0).  On `stream`
  * it computes the L2 norm of the reduced gradient g = (sum of the N
  * registered replicas) / N over every element of every unit, and the
  * coefficient c = min(1, max_norm / (norm + 1e-6)) rounded to fp32; the next
- * zero_step multiplies every reduced gradient by c before Adam.  The squared
+ * zero_step multiplies every reduced gradient by c before Adam.  Non-finite
+ * gradients follow IEEE arithmetic and torch's clip_grad_norm_: an inf makes
+ * the norm inf and c = 0 (the inf element becomes inf * 0 = NaN, every other
+ * gradient 0); a NaN makes the norm NaN and c = NaN (every gradient NaN).  A
+ * caller that skips such steps reads zero_grad_norm before zero_step.  The squared
  * norm is summed over fixed chunks of 16,384 elements of each unit (pads
  * included, they add zero) in a fixed order, so the result is reproducible
  * and identical for every stage and for padded or unpadded layouts.

@@ -260,10 +260,12 @@ def _same_norm(a, b):
 @pytest.mark.parametrize("gd,keep", [("bf16", False), ("bf16", True), ("fp32", False)])
 def test_non_finite_gradients(gd, keep):
     # step 1: an inf gradient (norm inf: every gradient scaled by 0, inf * 0 = NaN);
-    # step 2: a NaN in an element-wise tail (norm NaN: coefficient 1);
-    # step 3: the largest finite values in both replicas at one position, whose
+    # step 2: the largest finite values in both replicas at one position, whose
     #         fp32 sum overflows (the reduced gradient is inf);
-    # step 4: finite again.  Norms and every state element follow the oracle.
+    # step 3: finite again;
+    # step 4: a NaN in an element-wise tail (norm NaN: coefficient NaN, every
+    #         gradient NaN, every state element NaN).
+    # Norms and every state element follow the oracle.
     pl = si.from_units([3000, 77, 5001])
     pb = make_problem(pl, 2, 2, grad_dtype=gd, steps=4, seed=90, max_norm=0.5)
     lay = pb.lay
@@ -273,12 +275,13 @@ def test_non_finite_gradients(gd, keep):
     else:
         inf, nan, top = np.float32(np.inf), np.float32(np.nan), np.float32(3.0e38)
     pb.grads[0][0][1234] = inf
-    pb.grads[1][1][tail] = nan
-    pb.grads[2][0][4321] = top
-    pb.grads[2][1][4321] = top
+    pb.grads[1][0][4321] = top
+    pb.grads[1][1][4321] = top
+    pb.grads[3][1][tail] = nan
     ref_states, ref_norms, gpu_norms = {}, [], []
     oracle_run(pb, every_step=lambda t, s: ref_states.__setitem__(t, s), norms=ref_norms)
-    assert ref_norms[0] == np.inf and np.isnan(ref_norms[1]) and ref_norms[2] == np.inf and np.isfinite(ref_norms[3])
+    assert ref_norms[0] == np.inf and ref_norms[1] == np.inf and np.isfinite(ref_norms[2]) and np.isnan(ref_norms[3])
+    assert np.isnan(ref_states[4][0]).all() and not np.isnan(ref_states[3][0][:100]).any()
 
     def check(t, fs):
         compare_state(fs, ref_states[t], f"non-finite step {t}")

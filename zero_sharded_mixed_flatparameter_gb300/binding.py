@@ -31,7 +31,7 @@ EXPORTED = (
     "zero_import_state", "zero_clip_workspace_bytes_ex", "zero_clip_grad_norm_ex", "zero_kernel_timeouts",
     "zero_make_master_offload", "zero_offload_workspace_bytes", "zero_offload_step", "zero_cpu_adam",
     "zero_debug_inject", "zero_debug_check_failures", "zero_capturable_workspace_bytes", "zero_enable_capturable",
-    "zero_disable_capturable",
+    "zero_disable_capturable", "zero_count_nonfinite", "zero_read_nonfinite",
 )
 ZERO_CLIP_KEEP_REDUCED = 1
 ZERO_INJECT_MISSING_COPY = 1
@@ -99,6 +99,8 @@ def load(path: str = LIB_PATH):
             "zero_clip_workspace_bytes_ex": [vp, i32, P(i64)],
             "zero_clip_grad_norm_ex": [vp, f32, i32, vp, i64, vp],
             "zero_kernel_timeouts": [vp, P(ctypes.c_uint32)],
+            "zero_count_nonfinite": [vp, vp],
+            "zero_read_nonfinite": [vp, P(ctypes.c_uint64), vp],
             "zero_make_master_offload": [P(zero_config), vp, vp, i32, vp, P(zero_buffers), vp, P(vp)],
             "zero_offload_workspace_bytes": [vp, i64, P(i64), P(i64)],
             "zero_offload_step": [vp, i64, vp, i64, vp, i64, i32, vp, vp],
@@ -276,6 +278,16 @@ def zero_import_state(ctx: int, master_in: int, exp_avg_in: int, exp_avg_sq_in: 
                       stream: int = 0) -> None:
     _check(load().zero_import_state(ctx, master_in or None, exp_avg_in or None, exp_avg_sq_in or None, t,
                                     stream or None), ctx)
+
+
+def zero_count_nonfinite(ctx: int, counter: int) -> None:
+    _check(load().zero_count_nonfinite(ctx, counter or None), ctx)
+
+
+def zero_read_nonfinite(ctx: int, stream: int = 0) -> int:
+    n = ctypes.c_uint64()
+    _check(load().zero_read_nonfinite(ctx, ctypes.byref(n), stream or None), ctx)
+    return n.value
 
 
 def zero_kernel_timeouts(ctx: int | None = None) -> int:

@@ -45,7 +45,8 @@ struct NormArgs {
 // Norm pass: one CTA per chunk; writes one partial per chunk.
 cudaError_t launch_grad_sq(const NormArgs& a, long long chunks, cudaStream_t stream);
 // Sums n partials in a fixed order and writes the norm and the clip
-// coefficient min(1, max_norm / (norm + 1e-6)) into the workspace header.
+// coefficient min(1, max_norm / (norm + 1e-6)) into the workspace header (NaN
+// when the norm is NaN).
 cudaError_t launch_clip_finalize(void* workspace, long long n_partials, float max_norm, cudaStream_t stream);
 
 // make_master pieces.
@@ -82,6 +83,7 @@ struct ReduceSeg {
 };
 
 struct ReduceArgs {
+  unsigned long long* nonfinite;  // caller's overflow counter, or nullptr
   float* out;
   long long out_len;  // elements of out (debug bounds checks)
   const float* clip;  // device clip coefficient, or nullptr

@@ -230,7 +230,8 @@ __global__ void __launch_bounds__(kFinalizeThreads) clip_finalize_kernel(char* w
     const double norm = __dsqrt_rn(sum_sq);
     const double coef = __ddiv_rn(static_cast<double>(max_norm), __dadd_rn(norm, 1e-6));
     *reinterpret_cast<double*>(ws) = norm;
-    *reinterpret_cast<float*>(ws + 8) = coef < 1.0 ? __double2float_rn(coef) : 1.0f;
+    // the cap at 1 keeps a NaN: a NaN norm makes every clipped gradient NaN
+    *reinterpret_cast<float*>(ws + 8) = isnan(coef) ? __int_as_float(0x7fc00000) : (coef < 1.0 ? __double2float_rn(coef) : 1.0f);
   }
 }
 
@@ -443,6 +444,7 @@ __global__ void __launch_bounds__(kStepThreads) reduce_out_kernel(const __grid_c
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const float clip = a.clip ? *a.clip : 1.0f;
+  unsigned nf = 0;  // non-finite reduced gradients seen by this thread
   int s = 0;
   for (long long q = tid; q < a.total_groups; q += stride) {
     while (s + 1 < a.nseg && q >= a.seg[s + 1].group_start) ++s;
@@ -469,15 +471,21 @@ __global__ void __launch_bounds__(kStepThreads) reduce_out_kernel(const __grid_c
 #pragma unroll
         for (int e = 0; e < kVec; ++e) acc[e] = r == 0 ? x[e] : __fadd_rn(acc[e], x[e]);
       }
+      if (a.nonfinite) nf += count_nonfinite<kVec>(acc);
 #pragma unroll
       for (int e = 0; e < kVec; ++e) acc[e] = __fmul_rn(__fmul_rn(acc[e], a.inv_n), clip);
       st_stream_f4(out, make_float4(acc[0], acc[1], acc[2], acc[3]));
       st_stream_f4(out + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
     } else {
       const long long end = k + kVec < sg.len ? k + kVec : sg.len;
-      for (long long e = k; e < end; ++e) out[e - k] = __fmul_rn(__fmul_rn(reduce_one(a, sg, e), a.inv_n), clip);
+      for (long long e = k; e < end; ++e) {
+        const float r = reduce_one(a, sg, e);
+        if (a.nonfinite) nf += count_nonfinite<1>(&r);
+        out[e - k] = __fmul_rn(__fmul_rn(r, a.inv_n), clip);
+      }
     }
   }
+  flush_nonfinite(a.nonfinite, nf);
 }
 
 }  // namespace

@@ -44,6 +44,26 @@ __device__ __forceinline__ float4 ld_stream_f4(const float* p) { return __ldcs(r
 __device__ __forceinline__ void st_stream_f4(float* p, float4 x) { __stcs(reinterpret_cast<float4*>(p), x); }
 __device__ __forceinline__ void st_stream(void* p, uint4 x) { __stcs(reinterpret_cast<uint4*>(p), x); }
 
+// How many of kN reduced gradients are inf or NaN (the step's overflow
+// count).  One comparison per value; the count itself only where some value
+// is not finite.
+template <int kN>
+__device__ __forceinline__ unsigned count_nonfinite(const float* g) {
+  bool any = false;
+#pragma unroll
+  for (int e = 0; e < kN; ++e) any |= !(fabsf(g[e]) <= 0x1.fffffep127f);
+  if (!any) return 0u;
+  unsigned c = 0;
+#pragma unroll
+  for (int e = 0; e < kN; ++e) c += !(fabsf(g[e]) <= 0x1.fffffep127f) ? 1u : 0u;
+  return c;
+}
+
+// Adds a thread's overflow count to the caller's counter (none when zero).
+__device__ __forceinline__ void flush_nonfinite(unsigned long long* counter, unsigned count) {
+  if (count != 0u && counter != nullptr) atomicAdd(counter, static_cast<unsigned long long>(count));
+}
+
 // First index >= 0 congruent to (tid - start) modulo stride: walking a
 // segment from there in steps of `stride` makes the launch's grid-stride
 // loop run over all segments as one concatenated index space.

@@ -61,6 +61,8 @@ struct StepArgs {
   const long long* dev_t;
   const float* dev_bias;
   long long dev_steps;
+  unsigned long long* nonfinite;  // caller's counter of non-finite reduced
+                                  // gradients, or nullptr (not counted)
   int inject_missing_copy; // test hook: the tile-staged kernel announces the
                            // launch's first tile but issues none of its copies
   Seg seg[kMaxSegs];

@@ -76,6 +76,9 @@ struct zero_ctx {
   bool offload = false;
   zfs_host::Pool* pool = nullptr;
 
+  // Caller's device counter of non-finite reduced gradients (zero_count_nonfinite), or nullptr.
+  unsigned long long* nonfinite = nullptr;
+
   // Test hook armed by zero_debug_inject for the next step's first launch.
   int32_t inject = 0;
 
@@ -326,6 +329,7 @@ zero_status launch_batches(zero_ctx* ctx, const std::vector<PlannedSeg>& segs, b
     a.v = ctx->bufs.exp_avg_sq;
     a.p16 = static_cast<uint16_t*>(ctx->bufs.param16);
     a.clip = ctx->clip_ws ? reinterpret_cast<const float*>(ctx->clip_ws + 8) : nullptr;
+    a.nonfinite = ctx->nonfinite;
     fill_scalars(ctx, t, &a);
     a.total_padded = ctx->padded_total;
     a.dev_t = ctx->cap_t;
@@ -704,6 +708,7 @@ zero_status zero_step(zero_ctx* ctx, void* stream) {
       a.v = ctx->bufs.exp_avg_sq;
       a.p16 = static_cast<uint16_t*>(ctx->bufs.param16);
       a.clip = reinterpret_cast<const float*>(ctx->clip_ws + 8);
+      a.nonfinite = ctx->nonfinite;
       fill_scalars(ctx, t, &a);
       a.total_padded = ctx->padded_total - (ctx->inject == ZERO_INJECT_SHORT_BOUNDS ? zfs::kVec : 0);
       a.dev_t = ctx->cap_t;
@@ -806,6 +811,7 @@ cudaError_t enqueue_chunk_reduce(const zero_ctx* ctx, const std::vector<PlannedS
   a.out = out;
   a.out_len = c1 - c0;
   a.clip = clip;
+  a.nonfinite = ctx->nonfinite;
   a.inv_n = 1.0f / static_cast<float>(N);
   a.n_ranks = N;
   a.grad_fp32 = ctx->cfg.grad_dtype == ZERO_GRAD_FP32 ? 1 : 0;
@@ -1260,6 +1266,31 @@ zero_status zero_debug_inject(zero_ctx* ctx, int32_t what) {
   if (what != 0 && what != ZERO_INJECT_MISSING_COPY && what != ZERO_INJECT_SHORT_BOUNDS)
     return fail(ctx, ZERO_EINVAL, "unknown injection %d", what);
   ctx->inject = what;
+  return ZERO_OK;
+}
+
+zero_status zero_count_nonfinite(zero_ctx* ctx, uint64_t* counter) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  if (counter) {
+    if (!aligned(counter, 8)) return fail(ctx, ZERO_EINVAL, "counter is not 8-byte aligned");
+    int pdev = -1;
+    if (!is_device_pointer(counter, &pdev)) return fail(ctx, ZERO_EINVAL, "counter is not CUDA device memory");
+    if (ctx->device >= 0 && pdev != ctx->device)
+      return fail(ctx, ZERO_EINVAL, "counter is on device %d, the context's buffers on %d", pdev, ctx->device);
+  }
+  ctx->nonfinite = reinterpret_cast<unsigned long long*>(counter);
+  return ZERO_OK;
+}
+
+zero_status zero_read_nonfinite(zero_ctx* ctx, uint64_t* count, void* stream) {
+  if (!ctx || !count) return fail(ctx, ZERO_EINVAL, "NULL argument");
+  if (!ctx->nonfinite) return fail(ctx, ZERO_ESTATE, "no counter: call zero_count_nonfinite first");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ctx->nonfinite, sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(ctx, "reading the non-finite counter", e);
+  *count = v;
   return ZERO_OK;
 }
 

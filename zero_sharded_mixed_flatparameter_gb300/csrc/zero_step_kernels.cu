@@ -71,10 +71,12 @@ __device__ __forceinline__ float reduce_scalar(const StepArgs& a, const Seg& s, 
 }
 
 __device__ __forceinline__ void step_scalar_element(const StepArgs& a, const Seg& s, long long k, float clip,
-                                                    float bc1, float bc2) {
+                                                    float bc1, float bc2, unsigned& nf) {
   const long long j = s.base + k;
   if (!ZFS_CHECK(k >= 0 && k < s.len && j < a.total_padded)) return;
-  const float g = __fmul_rn(reduce_scalar(a, s, k), clip);
+  const float r = reduce_scalar(a, s, k);
+  if (a.nonfinite) nf += count_nonfinite<1>(&r);
+  const float g = __fmul_rn(r, clip);
   float w = a.master[j], m = a.m[j], v = a.v[j];
   adam(a, bc1, bc2, g, w, m, v);
   a.master[j] = w;
@@ -88,7 +90,7 @@ __device__ __forceinline__ void step_scalar_element(const StepArgs& a, const Seg
 // ---------------------------------------------------------------------------
 template <int N, bool kFp32>
 __device__ __forceinline__ void step_vec8(const StepArgs& a, const Seg& s, long long vi, float clip, float bc1,
-                                          float bc2) {
+                                          float bc2, unsigned& nf) {
   const long long j = s.base + vi * kVec;
   if (!ZFS_CHECK(vi >= 0 && (vi + 1) * kVec <= s.len && j + kVec <= a.total_padded)) return;
   float g[kVec];
@@ -125,6 +127,7 @@ __device__ __forceinline__ void step_vec8(const StepArgs& a, const Seg& s, long 
       g[6] = __fadd_rn(g[6], raw[r][1].z); g[7] = __fadd_rn(g[7], raw[r][1].w);
     }
   }
+  if (a.nonfinite) nf += count_nonfinite<kVec>(g);  // the sum is non-finite exactly when g / N is
   const float4 w0 = ld_stream_f4(a.master + j), w1 = ld_stream_f4(a.master + j + 4);
   const float4 m0 = ld_stream_f4(a.m + j), m1 = ld_stream_f4(a.m + j + 4);
   const float4 v0 = ld_stream_f4(a.v + j), v1 = ld_stream_f4(a.v + j + 4);
@@ -158,11 +161,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
   if (!step_bias<kDevBias>(a, &bc1, &bc2)) return;
   // Clip coefficient of the global norm (x 1 is exact when not clipping).
   const float clip = a.clip ? *a.clip : 1.0f;
+  unsigned nf = 0;  // non-finite reduced gradients seen by this thread
   for (int s = 0; s < a.nseg; ++s) {
     const Seg& seg = a.seg[s];
     const long long nvec = seg.len / kVec;
     for (long long vi = first_index(tid, seg.vec_start, stride); vi < nvec; vi += stride) {
-      step_vec8<N, kFp32>(a, seg, vi, clip, bc1, bc2);
+      step_vec8<N, kFp32>(a, seg, vi, clip, bc1, bc2, nf);
     }
   }
   // Ragged ends (fewer than 8 elements per segment), element by element.
@@ -171,9 +175,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
     const long long done = (seg.len / kVec) * kVec;
     const long long k = done + tid - static_cast<long long>(s) * kVec;
     if (tid >= static_cast<long long>(s) * kVec && k < seg.len && k < done + kVec) {
-      step_scalar_element(a, seg, k, clip, bc1, bc2);
+      step_scalar_element(a, seg, k, clip, bc1, bc2, nf);
     }
   }
+  flush_nonfinite(a.nonfinite, nf);
 }
 
 // ---------------------------------------------------------------------------
@@ -321,6 +326,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
     }
   }
   long long gave_up_at = -1;  // the tile whose wait ran out, if any
+  unsigned nf = 0;            // non-finite reduced gradients seen by this thread
   for (long long k = 0;; ++k) {
     const long long id = blockIdx.x + k * gridDim.x;
     if (id >= n_tiles) break;
@@ -389,6 +395,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
       const long long next = id + static_cast<long long>(kTmaStages) * gridDim.x;
       if (next < n_tiles) issue(next, stage);
     }
+    if (a.nonfinite) nf += count_nonfinite<kVec>(g);
 #pragma unroll
     for (int e = 0; e < kVec; ++e) adam(a, bc1, bc2, __fmul_rn(__fmul_rn(g[e], a.inv_n), clip), w[e], m[e], v[e]);
     int si;
@@ -439,6 +446,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
       while (!mbar_try_wait(&bars[s], parity) && global_ns() - t0 < kTmaDrainNs) {
       }
     }
+    flush_nonfinite(a.nonfinite, nf);
     return;
   }
   // The part of each segment after its last full tile (fewer than kTmaTile
@@ -448,9 +456,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
   for (int s = 0; s < a.nseg; ++s) {
     const Seg& sg = a.seg[s];
     for (long long k = (sg.len / kTmaTile) * kTmaTile + tid; k < sg.len; k += stride) {
-      step_scalar_element(a, sg, k, clip, bc1, bc2);
+      step_scalar_element(a, sg, k, clip, bc1, bc2, nf);
     }
   }
+  flush_nonfinite(a.nonfinite, nf);
 }
 
 // ---------------------------------------------------------------------------
@@ -536,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_tma4_kernel(const __grid_con
     }
   }
   long long gave_up_at = -1;
+  unsigned nf = 0;  // non-finite reduced gradients seen by this thread
   const int t4 = threadIdx.x * 4;
   for (long long k = 0;; ++k) {
     const long long id = blockIdx.x + k * gridDim.x;
@@ -580,6 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_tma4_kernel(const __grid_con
       if (next < n_tiles) issue(next, stage);
     }
     float w[4] = {w4.x, w4.y, w4.z, w4.w}, m[4] = {m4.x, m4.y, m4.z, m4.w}, v[4] = {v4.x, v4.y, v4.z, v4.w};
+    if (a.nonfinite) nf += count_nonfinite<4>(gg);
 #pragma unroll
     for (int e = 0; e < 4; ++e) adam(a, bc1, bc2, __fmul_rn(__fmul_rn(gg[e], a.inv_n), clip), w[e], m[e], v[e]);
     int si;
@@ -606,6 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_tma4_kernel(const __grid_con
       while (!mbar_try_wait(&bars[s], parity) && global_ns() - t0 < kTmaDrainNs) {
       }
     }
+    flush_nonfinite(a.nonfinite, nf);
     return;
   }
   // The part of each segment after its last full tile, element by element.
@@ -614,9 +626,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_tma4_kernel(const __grid_con
   for (int s = 0; s < a.nseg; ++s) {
     const Seg& sg = a.seg[s];
     for (long long k = (sg.len / T) * T + tid; k < sg.len; k += stride) {
-      step_scalar_element(a, sg, k, clip, bc1, bc2);
+      step_scalar_element(a, sg, k, clip, bc1, bc2, nf);
     }
   }
+  flush_nonfinite(a.nonfinite, nf);
 }
 
 // ---------------------------------------------------------------------------
@@ -685,7 +698,7 @@ __device__ __forceinline__ uint4 shfl_down_u4(const uint4& w) {
 // lane its neighbour's first word.
 template <int N, bool kFp32>
 __device__ __forceinline__ void shifted_vec8(const StepArgs& a, const Seg& s, int si, long long vi, bool active,
-                                             bool own_next, float clip, float bc1, float bc2) {
+                                             bool own_next, float clip, float bc1, float bc2, unsigned& nf) {
   const long long j = s.base + vi * kVec;
   const bool ok = active && ZFS_CHECK(vi >= 0 && (vi + 1) * kVec <= s.len && j >= 0 && j + kVec <= a.total_padded);
   constexpr int kWords = kFp32 ? 2 : 1;  // 16-byte words per replica and vector
@@ -728,6 +741,7 @@ __device__ __forceinline__ void shifted_vec8(const StepArgs& a, const Seg& s, in
     }
   }
   if (!ok) return;
+  if (a.nonfinite) nf += count_nonfinite<kVec>(g);
   float wv[kVec] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
   float mv[kVec] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
   float vv[kVec] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -749,10 +763,12 @@ __device__ __forceinline__ void shifted_vec8(const StepArgs& a, const Seg& s, in
 
 // One head or tail element k of the body (k < 0: the head) of segment si.
 __device__ __forceinline__ void shifted_element(const StepArgs& a, const Seg& s, int si, long long k, float clip,
-                                                float bc1, float bc2) {
+                                                float bc1, float bc2, unsigned& nf) {
   const long long j = s.base + k;
   if (!ZFS_CHECK(k >= -static_cast<long long>(a.head[si]) && k < s.len && j >= 0 && j < a.total_padded)) return;
-  const float g = __fmul_rn(reduce_scalar(a, s, k), clip);
+  const float r = reduce_scalar(a, s, k);
+  if (a.nonfinite) nf += count_nonfinite<1>(&r);
+  const float g = __fmul_rn(r, clip);
   float w = a.master[j], m = a.m[j], v = a.v[j];
   adam(a, bc1, bc2, g, w, m, v);
   a.master[j] = w;
@@ -769,6 +785,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_shift_kernel(const __gri
   float bc1, bc2;
   if (!step_bias<kDevBias>(a, &bc1, &bc2)) return;  // the same for every thread
   const float clip = a.clip ? *a.clip : 1.0f;
+  unsigned nf = 0;  // non-finite reduced gradients seen by this thread
   for (int si = 0; si < a.nseg; ++si) {
     const Seg& seg = a.seg[si];
     const long long nvec = seg.len / kVec;
@@ -779,7 +796,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_shift_kernel(const __gri
       const long long nb_vi = __shfl_down_sync(kFullWarp, vi, 1);
       const int nb_active = __shfl_down_sync(kFullWarp, active ? 1 : 0, 1);
       const bool own_next = !(lane < 31 && nb_active && nb_vi == vi + 1);
-      shifted_vec8<N, kFp32>(a, seg, si, vi, active, own_next, clip, bc1, bc2);
+      shifted_vec8<N, kFp32>(a, seg, si, vi, active, own_next, clip, bc1, bc2, nf);
     }
   }
   // Heads and ragged ends: 16 threads per segment, at most 7 + 7 elements.
@@ -789,8 +806,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_shift_kernel(const __gri
     if (q < 0 || q >= 2 * kVec) continue;
     const long long head = a.head[si];
     const long long k = q < head ? q - head : (seg.len / kVec) * kVec + (q - head);
-    if (q < head || (q - head < kVec && k < seg.len)) shifted_element(a, seg, si, k, clip, bc1, bc2);
+    if (q < head || (q - head < kVec && k < seg.len)) shifted_element(a, seg, si, k, clip, bc1, bc2, nf);
   }
+  flush_nonfinite(a.nonfinite, nf);
 }
 
 // Capturable steps: the device step count advances after the step's launches.

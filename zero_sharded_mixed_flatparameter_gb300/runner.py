@@ -233,6 +233,19 @@ class FlatStep:
         B.zero_disable_capturable(self.ctx, self.stream_handle(stream))
         self._cap_ws = None
 
+    def count_nonfinite(self, counter: Optional[torch.Tensor]) -> None:
+        """Every later step adds its number of non-finite reduced gradients to
+        `counter` (a one-element int64 device tensor, zeroed by the caller);
+        None stops counting."""
+        if counter is not None and (counter.dtype != torch.int64 or counter.device != self.device):
+            raise ValueError("the counter must be an int64 tensor on the context's device")
+        B.zero_count_nonfinite(self.ctx, counter.data_ptr() if counter is not None else 0)
+        self._nonfinite = counter
+
+    def kernel_timeouts(self) -> int:
+        """Bounded waits of the tile-staged step kernels that gave up (process-wide count)."""
+        return B.zero_kernel_timeouts(self.ctx)
+
     def step_count(self) -> int:
         return B.zero_step_count(self.ctx)
 
