@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(kStepThreads) reduce_out_kernel(const __grid_c
 #pragma unroll
         for (int e = 0; e < kVec; ++e) acc[e] = r == 0 ? x[e] : __fadd_rn(acc[e], x[e]);
       }
-      if (a.nonfinite) nf += count_nonfinite<kVec>(acc);
+      nf += tally_nonfinite<kVec>(acc);
 #pragma unroll
       for (int e = 0; e < kVec; ++e) acc[e] = __fmul_rn(__fmul_rn(acc[e], a.inv_n), clip);
       st_stream_f4(out, make_float4(acc[0], acc[1], acc[2], acc[3]));
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kStepThreads) reduce_out_kernel(const __grid_c
       const long long end = k + kVec < sg.len ? k + kVec : sg.len;
       for (long long e = k; e < end; ++e) {
         const float r = reduce_one(a, sg, e);
-        if (a.nonfinite) nf += count_nonfinite<1>(&r);
+        nf += tally_nonfinite<1>(&r);
         out[e - k] = __fmul_rn(__fmul_rn(r, a.inv_n), clip);
       }
     }

@@ -45,17 +45,14 @@ __device__ __forceinline__ void st_stream_f4(float* p, float4 x) { __stcs(reinte
 __device__ __forceinline__ void st_stream(void* p, uint4 x) { __stcs(reinterpret_cast<uint4*>(p), x); }
 
 // How many of kN reduced gradients are inf or NaN (the step's overflow
-// count).  One comparison per value; the count itself only where some value
-// is not finite.
+// count): one comparison and one add per value, no branch, so that the
+// kernels' loads are not held behind it; the sum reaches the caller's counter
+// only when counting is on (flush_nonfinite).
 template <int kN>
-__device__ __forceinline__ unsigned count_nonfinite(const float* g) {
-  bool any = false;
-#pragma unroll
-  for (int e = 0; e < kN; ++e) any |= !(fabsf(g[e]) <= 0x1.fffffep127f);
-  if (!any) return 0u;
+__device__ __forceinline__ unsigned tally_nonfinite(const float* g) {
   unsigned c = 0;
 #pragma unroll
-  for (int e = 0; e < kN; ++e) c += !(fabsf(g[e]) <= 0x1.fffffep127f) ? 1u : 0u;
+  for (int e = 0; e < kN; ++e) c += (fabsf(g[e]) <= 0x1.fffffep127f) ? 0u : 1u;
   return c;
 }
 

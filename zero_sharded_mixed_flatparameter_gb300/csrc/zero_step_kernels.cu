@@ -75,7 +75,7 @@ __device__ __forceinline__ void step_scalar_element(const StepArgs& a, const Seg
   const long long j = s.base + k;
   if (!ZFS_CHECK(k >= 0 && k < s.len && j < a.total_padded)) return;
   const float r = reduce_scalar(a, s, k);
-  if (a.nonfinite) nf += count_nonfinite<1>(&r);
+  nf += tally_nonfinite<1>(&r);
   const float g = __fmul_rn(r, clip);
   float w = a.master[j], m = a.m[j], v = a.v[j];
   adam(a, bc1, bc2, g, w, m, v);
@@ -127,13 +127,13 @@ __device__ __forceinline__ void step_vec8(const StepArgs& a, const Seg& s, long 
       g[6] = __fadd_rn(g[6], raw[r][1].z); g[7] = __fadd_rn(g[7], raw[r][1].w);
     }
   }
-  if (a.nonfinite) nf += count_nonfinite<kVec>(g);  // the sum is non-finite exactly when g / N is
   const float4 w0 = ld_stream_f4(a.master + j), w1 = ld_stream_f4(a.master + j + 4);
   const float4 m0 = ld_stream_f4(a.m + j), m1 = ld_stream_f4(a.m + j + 4);
   const float4 v0 = ld_stream_f4(a.v + j), v1 = ld_stream_f4(a.v + j + 4);
   float w[kVec] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
   float m[kVec] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
   float v[kVec] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  nf += tally_nonfinite<kVec>(g);  // the sum is non-finite exactly when g / N is
 #pragma unroll
   for (int e = 0; e < kVec; ++e) adam(a, bc1, bc2, __fmul_rn(__fmul_rn(g[e], a.inv_n), clip), w[e], m[e], v[e]);
   st_stream_f4(a.master + j, make_float4(w[0], w[1], w[2], w[3]));
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_tma_kernel(const __grid_
       const long long next = id + static_cast<long long>(kTmaStages) * gridDim.x;
       if (next < n_tiles) issue(next, stage);
     }
-    if (a.nonfinite) nf += count_nonfinite<kVec>(g);
+    nf += tally_nonfinite<kVec>(g);
 #pragma unroll
     for (int e = 0; e < kVec; ++e) adam(a, bc1, bc2, __fmul_rn(__fmul_rn(g[e], a.inv_n), clip), w[e], m[e], v[e]);
     int si;
@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_tma4_kernel(const __grid_con
       if (next < n_tiles) issue(next, stage);
     }
     float w[4] = {w4.x, w4.y, w4.z, w4.w}, m[4] = {m4.x, m4.y, m4.z, m4.w}, v[4] = {v4.x, v4.y, v4.z, v4.w};
-    if (a.nonfinite) nf += count_nonfinite<4>(gg);
+    nf += tally_nonfinite<4>(gg);
 #pragma unroll
     for (int e = 0; e < 4; ++e) adam(a, bc1, bc2, __fmul_rn(__fmul_rn(gg[e], a.inv_n), clip), w[e], m[e], v[e]);
     int si;
@@ -741,7 +741,7 @@ __device__ __forceinline__ void shifted_vec8(const StepArgs& a, const Seg& s, in
     }
   }
   if (!ok) return;
-  if (a.nonfinite) nf += count_nonfinite<kVec>(g);
+  nf += tally_nonfinite<kVec>(g);
   float wv[kVec] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
   float mv[kVec] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
   float vv[kVec] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -767,7 +767,7 @@ __device__ __forceinline__ void shifted_element(const StepArgs& a, const Seg& s,
   const long long j = s.base + k;
   if (!ZFS_CHECK(k >= -static_cast<long long>(a.head[si]) && k < s.len && j >= 0 && j < a.total_padded)) return;
   const float r = reduce_scalar(a, s, k);
-  if (a.nonfinite) nf += count_nonfinite<1>(&r);
+  nf += tally_nonfinite<1>(&r);
   const float g = __fmul_rn(r, clip);
   float w = a.master[j], m = a.m[j], v = a.v[j];
   adam(a, bc1, bc2, g, w, m, v);
