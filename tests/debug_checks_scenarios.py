@@ -47,6 +47,7 @@ def main():
     scenario("tile-staged N = 2 bf16 (4 elements per thread)", make_problem(big, 2, 3, steps=1, seed=219),
              mode="separate")
     scenario("tile-staged N = 4 bf16 (512-thread CTAs)", make_problem(big, 4, 2, steps=1, seed=220), mode="all")
+    scenario("pipelined tile-staged N = 10 bf16", make_problem(big, 10, 3, steps=1, seed=224), mode="separate")
     scenario("clipped N = 8", make_problem(odd, 8, 2, steps=2, seed=214, max_norm=0.05))
     scenario("clipped, reduced gradient kept", make_problem(odd, 8, 1, steps=2, seed=215, max_norm=0.05),
              clip_keep=True)

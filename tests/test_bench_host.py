@@ -11,14 +11,16 @@ import bench
 
 
 @pytest.mark.parametrize("n,gd,keep,elems,want", [
-    (8, "bf16", False, 73_417_728, "step_vec_kernel"),        # the default workload
+    (8, "bf16", False, 73_417_728, "step_pipe_kernel"),       # the Llama-1024 workload
     (8, "bf16", False, 2 ** 23 - 1, "step_vec_kernel"),
     (1, "bf16", False, 2 ** 23, "step_tma4_kernel"),
     (2, "bf16", False, 10 ** 9, "step_tma4_kernel"),
     (4, "bf16", False, 10 ** 9, "step_tma4_kernel"),
     (5, "bf16", False, 10 ** 9, "step_vec_kernel"),
-    (10, "bf16", False, 10 ** 9, "step_vec_kernel"),
-    (11, "bf16", False, 10 ** 9, "step_tma_kernel"),
+    (7, "bf16", False, 10 ** 9, "step_vec_kernel"),
+    (10, "bf16", False, 10 ** 9, "step_pipe_kernel"),
+    (12, "bf16", False, 10 ** 9, "step_pipe_kernel"),
+    (13, "bf16", False, 10 ** 9, "step_tma_kernel"),
     (16, "bf16", False, 10 ** 9, "step_tma_kernel"),
     (16, "bf16", False, 10 ** 6, "step_vec_kernel"),          # small launches stay register-staged
     (2, "fp32", False, 2_030_174_208, "step_vec_kernel"),     # the stage-buffer workload

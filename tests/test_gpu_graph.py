@@ -31,6 +31,8 @@ def _refs(pb):
     ("toy MLP ZeRO-3", si.toy_mlp(), 4, 3, "bf16", 0.0, False),
     ("odd units, clipped, kept gradient", si.from_units([1552, 7, 9312, 33]), 3, 2, "bf16", 0.05, True),
     ("tile-staged N = 16", si.from_units([4_200_005, 2_000_000, 2_300_003]), 16, 2, "bf16", 0.0, False),
+    ("pipelined staged N = 10, clipped", si.from_units([4_200_005, 2_000_000, 2_300_003]), 10, 3, "bf16", 0.5,
+     False),
     ("fp32 N = 9 staged, clipped", si.from_units([4_200_005, 4_300_003]), 9, 1, "fp32", 0.5, False),
     ("fp32 N = 12 staged, 1,024-element tiles", si.from_units([4_200_005, 4_300_003]), 12, 2, "fp32", 0.0, False),
     ("bf16 N = 2 staged, 4 elements per thread, clipped", si.from_units([4_200_005, 4_300_003]), 2, 3, "bf16", 0.5,

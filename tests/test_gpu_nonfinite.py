@@ -92,7 +92,7 @@ def test_shifted_kernel_heads_and_tails():
                                                              base[3] + 32, base[4] + t])
 
 
-@pytest.mark.parametrize("n,gd", [(2, "bf16"), (16, "bf16"), (8, "fp32"), (12, "fp32")])
+@pytest.mark.parametrize("n,gd", [(2, "bf16"), (10, "bf16"), (16, "bf16"), (8, "fp32"), (12, "fp32")])
 def test_tile_staged_kernels(n, gd):
     # launches of at least 2^23 elements take the tile-staged kernels;
     # the count only (the state of these kernels is checked elsewhere)

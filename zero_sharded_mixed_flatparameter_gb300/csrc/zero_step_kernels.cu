@@ -811,6 +811,203 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_shift_kernel(const __gri
   flush_nonfinite(a.nonfinite, nf);
 }
 
+// ---------------------------------------------------------------------------
+// Tile-staged kernel without a CTA barrier in its loop (bf16 N = 8..12).
+//
+// step_tma4_kernel synchronises the whole CTA twice per tile: a give-up
+// decision after the wait, and a barrier after every thread has read the
+// stage so that thread 0 may refill it.  Here every stage also has an
+// "empty" mbarrier on which each warp arrives once it has read its part of
+// the stage; thread 0 refills the stage consumed in the previous iteration
+// after waiting (bounded) on that barrier, so no warp waits for the others
+// and the next tiles stay in flight while the slowest warp finishes.
+// Give-up decisions are warp-uniform (a warp meets __syncwarp below); a CTA
+// whose producer or consumers give up counts one timeout, thread 0 waits
+// (bounded) for every copy it issued, and the CTA leaves with the rest of its
+// tiles not updated, as in the other staged kernels.  Tile geometry, the test
+// hook, the index checks and the per-element arithmetic are
+// step_tma4_kernel's, so results are bit-identical.
+//
+// Measured on GB300 over 100 M bf16 elements (step GB/s against the kernel
+// each N took before): N = 8 6872 / 6781-6802 (register-staged; 6834-6844 /
+// 6785-6803 over the 73.4 M-param Llama-1024 layout), N = 9 6966 / 6748-6759,
+// N = 10 7025-7038 / 6753-6764, N = 11 7119-7121 / 6778-6787 (2,048-element
+// staged kernel), N = 12 7173 / 6914-6915.  512 threads with three stages of
+// 2,048-element tiles; 256-thread CTAs (two per SM, four stages), 384 threads
+// with four stages, 768 or 1,024 threads with two stages and 512 threads
+// with two stages measured 1-20 % slower at N = 8..10; at N <= 7, N >= 13
+// (two stages fit) and for fp32 gradients this kernel was slower than the
+// kernels those take.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+template <int N, bool kFp32, int kThreads, int kStages, bool kDevBias>
+__global__ void __launch_bounds__(kThreads, 1) step_pipe_kernel(const __grid_constant__ StepArgs a) {
+  float bc1, bc2;
+  if (!step_bias<kDevBias>(a, &bc1, &bc2)) return;
+  using L = Tma4Tile<N, kFp32, kThreads, kStages>;
+  constexpr int S = kStages;
+  constexpr long long T = L::kElems;
+  constexpr int kWarps = kThreads / 32;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t full[S];
+  __shared__ __align__(8) uint64_t empty[S];
+  __shared__ int cta_gave_up;  // some warp of the CTA gave up (counted once, below)
+  long long n_tiles = 0;
+  for (int s = 0; s < a.nseg; ++s) n_tiles += a.seg[s].len / T;
+  const float clip = a.clip ? *a.clip : 1.0f;
+  if (threadIdx.x == 0) {
+    cta_gave_up = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  auto issue = [&](long long id, int stage) {  // thread 0 only
+    int si;
+    long long ti;
+    locate_tile4<T>(a, id, &si, &ti);
+    const Seg& sg = a.seg[si];
+    unsigned char* st = smem + static_cast<size_t>(stage) * L::kStageBytes;
+    const long long e0 = ti * T;
+    if (!ZFS_CHECK(ti >= 0 && e0 + T <= sg.len && sg.base + e0 + T <= a.total_padded)) {
+      mbar_arrive1(&full[stage]);
+      return;
+    }
+    mbar_expect_tx(&full[stage], L::kStageBytes);
+    if (a.inject_missing_copy && id == 0) return;
+    for (int r = 0; r < N; ++r)
+      bulk_load(st + r * L::kGradBytes, static_cast<const unsigned char*>(sg.g[r]) + e0 * (kFp32 ? 4 : 2),
+                L::kGradBytes, &full[stage]);
+    const long long j0 = sg.base + e0;
+    unsigned char* st_state = st + N * L::kGradBytes;
+    bulk_load(st_state, a.master + j0, L::kStateBytes, &full[stage]);
+    bulk_load(st_state + L::kStateBytes, a.m + j0, L::kStateBytes, &full[stage]);
+    bulk_load(st_state + 2 * L::kStateBytes, a.v + j0, L::kStateBytes, &full[stage]);
+  };
+  long long issued = 0;  // tiles issued by thread 0 (k-indices 0 .. issued-1)
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      const long long id = blockIdx.x + static_cast<long long>(i) * gridDim.x;
+      if (id < n_tiles) {
+        issue(id, i);
+        issued = i + 1;
+      }
+    }
+  }
+  bool gave_up = false;
+  unsigned nf = 0;
+  const int t4 = threadIdx.x * 4;
+  const int lane = threadIdx.x & 31;
+  long long k = 0;
+  for (;; ++k) {
+    const long long id = blockIdx.x + k * gridDim.x;
+    if (id >= n_tiles) break;
+    const int stage = static_cast<int>(k % S);
+    const uint32_t parity = static_cast<uint32_t>((k / S) & 1);
+    const bool got = mbar_try_wait(&full[stage], parity) || wait_tile(&full[stage], parity);
+    if (!__all_sync(0xffffffffu, got)) {  // the warp gives up together (it meets __syncwarp below)
+      gave_up = true;
+      if (lane == 0) cta_gave_up = 1;
+      break;
+    }
+    const unsigned char* st = smem + static_cast<size_t>(stage) * L::kStageBytes;
+    float gg[4];
+    if constexpr (kFp32) {
+      const float4 x0 = *reinterpret_cast<const float4*>(st + t4 * 4);
+      gg[0] = x0.x; gg[1] = x0.y; gg[2] = x0.z; gg[3] = x0.w;
+#pragma unroll
+      for (int r = 1; r < N; ++r) {
+        const float4 x = *reinterpret_cast<const float4*>(st + r * L::kGradBytes + t4 * 4);
+        gg[0] = __fadd_rn(gg[0], x.x); gg[1] = __fadd_rn(gg[1], x.y);
+        gg[2] = __fadd_rn(gg[2], x.z); gg[3] = __fadd_rn(gg[3], x.w);
+      }
+    } else {
+      const uint2 x0 = *reinterpret_cast<const uint2*>(st + t4 * 2);
+      gg[0] = bf16_lo(x0.x); gg[1] = bf16_hi(x0.x); gg[2] = bf16_lo(x0.y); gg[3] = bf16_hi(x0.y);
+#pragma unroll
+      for (int r = 1; r < N; ++r) {
+        const uint2 x = *reinterpret_cast<const uint2*>(st + r * L::kGradBytes + t4 * 2);
+        gg[0] = __fadd_rn(gg[0], bf16_lo(x.x)); gg[1] = __fadd_rn(gg[1], bf16_hi(x.x));
+        gg[2] = __fadd_rn(gg[2], bf16_lo(x.y)); gg[3] = __fadd_rn(gg[3], bf16_hi(x.y));
+      }
+    }
+    const unsigned char* st_state = st + N * L::kGradBytes;
+    const float4 w4 = *reinterpret_cast<const float4*>(st_state + t4 * 4);
+    const float4 m4 = *reinterpret_cast<const float4*>(st_state + L::kStateBytes + t4 * 4);
+    const float4 v4 = *reinterpret_cast<const float4*>(st_state + 2 * L::kStateBytes + t4 * 4);
+    __syncwarp();
+    if (lane == 0) mbar_arrive1(&empty[stage]);  // this warp has read the stage
+    // Thread 0 refills the stage consumed in the previous iteration.
+    if (threadIdx.x == 0 && k >= 1) {
+      const long long kp = k - 1;
+      const long long nid = blockIdx.x + (kp + S) * gridDim.x;
+      if (nid < n_tiles) {
+        const int ps = static_cast<int>(kp % S);
+        const uint32_t pp = static_cast<uint32_t>((kp / S) & 1);
+        if (!mbar_try_wait(&empty[ps], pp) && !wait_tile(&empty[ps], pp)) {
+          gave_up = true;
+        } else {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          issue(nid, ps);
+          issued = kp + S + 1;
+        }
+      }
+    }
+    if (threadIdx.x < 32) gave_up = __shfl_sync(0xffffffffu, gave_up, 0);  // warp 0 leaves together
+    if (threadIdx.x == 0 && gave_up) cta_gave_up = 1;
+    float w[4] = {w4.x, w4.y, w4.z, w4.w}, m[4] = {m4.x, m4.y, m4.z, m4.w}, v[4] = {v4.x, v4.y, v4.z, v4.w};
+    nf += tally_nonfinite<4>(gg);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) adam(a, bc1, bc2, __fmul_rn(__fmul_rn(gg[e], a.inv_n), clip), w[e], m[e], v[e]);
+    int si;
+    long long ti;
+    locate_tile4<T>(a, id, &si, &ti);
+    if (ZFS_CHECK((ti + 1) * T <= a.seg[si].len && a.seg[si].base + (ti + 1) * T <= a.total_padded)) {
+      const long long j = a.seg[si].base + ti * T + t4;
+      st_stream_f4(a.master + j, make_float4(w[0], w[1], w[2], w[3]));
+      st_stream_f4(a.m + j, make_float4(m[0], m[1], m[2], m[3]));
+      st_stream_f4(a.v + j, make_float4(v[0], v[1], v[2], v[3]));
+      uint2 out;
+      out.x = pack_bf16x2(w[0], w[1]);
+      out.y = pack_bf16x2(w[2], w[3]);
+      __stcs(reinterpret_cast<uint2*>(a.p16 + j), out);
+    }
+    if (gave_up) break;  // thread 0 could not refill: warp 0 leaves after this tile
+  }
+  // Every thread gets here once (every wait above is bounded): whether any
+  // warp gave up is then known to all.
+  __syncthreads();
+  if (cta_gave_up) {
+    if (threadIdx.x == 0) {
+      atomicAdd(&g_step_timeouts, 1u);
+      // every tile issued and not consumed by thread 0: wait (bounded) for its copies
+      for (long long j = k; j < issued; ++j) {
+        const int s = static_cast<int>(j % S);
+        const uint32_t parity = static_cast<uint32_t>((j / S) & 1);
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(&full[s], parity) && global_ns() - t0 < kTmaDrainNs) {
+        }
+      }
+    }
+    flush_nonfinite(a.nonfinite, nf);
+    return;
+  }
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (int s = 0; s < a.nseg; ++s) {
+    const Seg& sg = a.seg[s];
+    for (long long kk = (sg.len / T) * T + tid; kk < sg.len; kk += stride) {
+      step_scalar_element(a, sg, kk, clip, bc1, bc2, nf);
+    }
+  }
+  flush_nonfinite(a.nonfinite, nf);
+}
+
 // Capturable steps: the device step count advances after the step's launches.
 __global__ void count_step_kernel(long long* t) { *t += 1; }
 
@@ -949,6 +1146,21 @@ cudaError_t launch_tma(const StepArgs& a, cudaStream_t stream) {
 }
 
 template <int N, bool kFp32, int kThreads, int kStages, int kCtasPerSm, bool kDevBias>
+cudaError_t launch_pipe(const StepArgs& a, cudaStream_t stream) {
+  constexpr uint32_t kSmem = Tma4Tile<N, kFp32, kThreads, kStages>::kSmemBytes;
+  static_assert(kSmem + 128 <= 227 * 1024, "staged tiles must fit one CTA's shared memory (227 KB)");
+  auto kernel = step_pipe_kernel<N, kFp32, kThreads, kStages, kDevBias>;
+  const int dev = current_device();
+  const cudaError_t e = ensure_smem(dev, reinterpret_cast<const void*>(kernel), kSmem);
+  if (e != cudaSuccess) return e;
+  int per_sm = static_cast<int>(kMaxSmemPerSm / (kSmem + kSmemReservedPerCta));
+  if (per_sm < 1) per_sm = 1;
+  if (per_sm > kCtasPerSm) per_sm = kCtasPerSm;
+  kernel<<<static_cast<unsigned>(cached_sms(dev) * per_sm), kThreads, kSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int N, bool kFp32, int kThreads, int kStages, int kCtasPerSm, bool kDevBias>
 cudaError_t launch_tma4(const StepArgs& a, cudaStream_t stream) {
   constexpr uint32_t kSmem = Tma4Tile<N, kFp32, kThreads, kStages>::kSmemBytes;
   static_assert(kSmem + 128 <= 227 * 1024, "staged tiles must fit one CTA's shared memory (227 KB)");
@@ -994,8 +1206,9 @@ cudaError_t launch_tma4_bf16(const StepArgs& a, cudaStream_t stream) {
 }
 
 // A staged kernel where one measured faster than the register-staged kernel
-// (launches of at least kTmaMinElems elements): bf16 N = 1..4 and N >= 11,
-// fp32 N >= 7.  Other rank counts return with *launched = false.
+// (launches of at least kTmaMinElems elements): bf16 N = 1..4 (4-element
+// staged), N = 8..12 (barrier-free pipelined), N >= 13 (2,048-element
+// staged); fp32 N >= 7.  Other rank counts return with *launched = false.
 template <bool kDevBias>
 cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launched) {
   *launched = true;
@@ -1005,8 +1218,11 @@ cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launche
       case 2: return launch_tma4_bf16<2, kDevBias>(a, stream);
       case 3: return launch_tma4_bf16<3, kDevBias>(a, stream);
       case 4: return launch_tma4_bf16<4, kDevBias>(a, stream);
-      case 11: return launch_tma<11, false, kDevBias>(a, stream);
-      case 12: return launch_tma<12, false, kDevBias>(a, stream);
+      case 8: return launch_pipe<8, false, 512, 3, 1, kDevBias>(a, stream);
+      case 9: return launch_pipe<9, false, 512, 3, 1, kDevBias>(a, stream);
+      case 10: return launch_pipe<10, false, 512, 3, 1, kDevBias>(a, stream);
+      case 11: return launch_pipe<11, false, 512, 3, 1, kDevBias>(a, stream);
+      case 12: return launch_pipe<12, false, 512, 3, 1, kDevBias>(a, stream);
       case 13: return launch_tma<13, false, kDevBias>(a, stream);
       case 14: return launch_tma<14, false, kDevBias>(a, stream);
       case 15: return launch_tma<15, false, kDevBias>(a, stream);
