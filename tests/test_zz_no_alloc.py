@@ -9,6 +9,10 @@ agree within the clip tests' 1e-12 and the states within the parity
 tolerances (they are expected to be bit-identical).  This file is collected
 last so that a failure here comes after every other test has run."""
 
+import os
+import subprocess
+import sys
+
 import pytest
 import torch
 
@@ -64,3 +68,17 @@ def test_static_scratch_rejects_layouts_beyond_its_size():
         assert "static scratch" in B.zero_last_error(ctx)
     finally:
         B.zero_destroy(ctx)
+
+
+def test_static_scratch_in_every_cuda_context():
+    # The scratch array has one copy per CUDA context; a caller running in a
+    # second context of the GPU (or in one created after another was
+    # destroyed) must get its own context's copy, never an address from
+    # another context.  Run in a subprocess without torch, every buffer made
+    # with the driver API in the context that uses it (the scenario also
+    # steps a tile-staged kernel in each context).
+    here = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, os.path.join(here, "no_alloc_contexts_scenario.py")], capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
+    assert r.stdout.strip().splitlines()[-1] == "all contexts ok"

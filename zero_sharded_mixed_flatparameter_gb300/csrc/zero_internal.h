@@ -85,6 +85,13 @@ cudaError_t launch_step_shift(const StepArgs& a, cudaStream_t stream);
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
 
+// The unique id of the calling thread's current CUDA context, which the
+// driver never reuses within a process; false when no context is current or
+// the driver cannot say.  State that belongs to a context rather than to a
+// device (a kernel's raised shared-memory limit, the address of a __device__
+// object) is cached under it.
+bool current_context_id(unsigned long long* id);
+
 // Bounded waits of the tile-staged step kernel that gave up on the current
 // device since the library was loaded (0xFFFFFFFF if it cannot be read).
 unsigned int step_timeouts();

@@ -24,7 +24,6 @@
 // and not once per device ordinal: a non-primary context, or the primary
 // context created again after cudaDeviceReset, gets its own lookup.
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -40,40 +39,6 @@ namespace {
 constexpr long long kStaticClipBytes = 1LL << 20;
 
 static __device__ __align__(256) unsigned char g_clip_scratch[kStaticClipBytes];
-
-// Driver calls reached through the runtime's entry-point query, so that the
-// library needs no link-time dependency on the driver library.
-using CtxGetCurrentFn = CUresult (*)(CUcontext*);
-using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
-
-std::once_flag g_driver_once;
-CtxGetCurrentFn g_ctx_get_current = nullptr;
-CtxGetIdFn g_ctx_get_id = nullptr;
-
-void load_driver_calls() {
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-      q == cudaDriverEntryPointSuccess && fn) {
-    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
-  }
-  fn = nullptr;
-  q = cudaDriverEntryPointSymbolNotFound;
-  if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-      q == cudaDriverEntryPointSuccess && fn) {
-    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(fn);
-  }
-}
-
-// The unique id of the calling thread's current context; false when no
-// context is current or the driver cannot say.
-bool current_context_id(unsigned long long* id) {
-  std::call_once(g_driver_once, load_driver_calls);
-  if (!g_ctx_get_current || !g_ctx_get_id) return false;
-  CUcontext ctx = nullptr;
-  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
-  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
-}
 
 // Addresses of the array in the contexts seen so far (a small ring: an
 // evicted context is simply looked up again).
@@ -107,7 +72,7 @@ extern "C" zero_status zero_clip_grad_norm_static(zero_ctx* ctx, float max_norm,
   }
   void* scratch = nullptr;
   unsigned long long ctx_id = 0;
-  bool have_id = current_context_id(&ctx_id);
+  bool have_id = zfs::current_context_id(&ctx_id);
   std::lock_guard<std::mutex> lock(g_mutex);
   if (have_id) {
     for (const CachedAddress& c : g_cache) {
@@ -137,7 +102,7 @@ extern "C" zero_status zero_clip_grad_norm_static(zero_ctx* ctx, float max_norm,
           ctx, ZERO_ECUDA, "the static clip scratch is not device memory of the current device"));
     }
     scratch = address;
-    if (!have_id) have_id = current_context_id(&ctx_id);  // the lookup may have made the context current
+    if (!have_id) have_id = zfs::current_context_id(&ctx_id);  // the lookup may have made the context current
     if (have_id) {
       g_cache[g_cache_next] = CachedAddress{ctx_id, address};
       g_cache_next = (g_cache_next + 1) % kCachedContexts;

@@ -29,6 +29,7 @@
 #include <string>
 #include <vector>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "zero_flatstep.h"
@@ -398,6 +399,44 @@ int64_t padded_as_stage(const zero_ctx* ctx, int32_t i, int32_t stage) {
 }
 
 }  // namespace
+
+namespace zfs {
+namespace {
+
+// Driver calls reached through the runtime's entry-point query, so that the
+// library needs no link-time dependency on the driver library.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+std::once_flag g_driver_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+void load_driver_calls() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess && fn) {
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+  }
+  fn = nullptr;
+  q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess && fn) {
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(fn);
+  }
+}
+
+}  // namespace
+
+bool current_context_id(unsigned long long* id) {
+  std::call_once(g_driver_once, load_driver_calls);
+  if (!g_ctx_get_current || !g_ctx_get_id) return false;
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+}  // namespace zfs
 
 int zfs_report_error(zero_ctx* ctx, int status, const char* message) {
   return fail(ctx, static_cast<zero_status>(status), "%s", message);

@@ -1048,9 +1048,12 @@ struct DeviceInfo {
   // [device-side bias][fp32 gradients][N]
   int vec_blocks_per_sm[2][2][kMaxRanks + 1] = {};
   int shift_blocks_per_sm[2][2][kMaxRanks + 1] = {};
-  // Staged kernels whose dynamic shared memory limit is raised on the device.
-  const void* smem_set[kMaxSmemKernels] = {};
-  int n_smem_set = 0;
+  // Staged kernels whose dynamic shared memory limit is raised, and in which
+  // CUDA context (a function attribute belongs to a context): a ring, an
+  // evicted entry is simply set again.
+  const void* smem_fn[kMaxSmemKernels] = {};
+  unsigned long long smem_ctx[kMaxSmemKernels] = {};
+  int smem_next = 0;
 };
 
 // Shared memory of one SM usable by CTAs, and what each CTA reserves.
@@ -1060,19 +1063,29 @@ constexpr long long kSmemReservedPerCta = 1024;
 std::mutex g_info_mutex;
 DeviceInfo g_info[kMaxDevices];
 
-// Raises `fn`'s dynamic shared memory limit to `bytes` once per device.  The
-// record lives in this file's tables (internal linkage), not in statics of
-// the launch templates: those would be one object process-wide, shared with
-// any other copy of the library loaded alongside, which then would skip the
-// call for its own kernels.
+// Raises `fn`'s dynamic shared memory limit to `bytes` once per CUDA context
+// (the attribute belongs to the context: a second context on the same GPU
+// needs its own call).  Without a context id the call is made every time.
+// The record lives in this file's tables (internal linkage), not in statics
+// of the launch templates: those would be one object process-wide, shared
+// with any other copy of the library loaded alongside, which then would skip
+// the call for its own kernels.
 cudaError_t ensure_smem(int dev, const void* fn, uint32_t bytes) {
+  unsigned long long cid = 0;
+  const bool have_id = current_context_id(&cid);
   std::lock_guard<std::mutex> lock(g_info_mutex);
   DeviceInfo& d = g_info[dev];
-  for (int i = 0; i < d.n_smem_set; ++i)
-    if (d.smem_set[i] == fn) return cudaSuccess;
+  if (have_id) {
+    for (int i = 0; i < kMaxSmemKernels; ++i)
+      if (d.smem_fn[i] == fn && d.smem_ctx[i] == cid) return cudaSuccess;
+  }
   const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
-  if (d.n_smem_set < kMaxSmemKernels) d.smem_set[d.n_smem_set++] = fn;
+  if (have_id) {
+    d.smem_fn[d.smem_next] = fn;
+    d.smem_ctx[d.smem_next] = cid;
+    d.smem_next = (d.smem_next + 1) % kMaxSmemKernels;
+  }
   return cudaSuccess;
 }
 
