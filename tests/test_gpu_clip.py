@@ -341,3 +341,45 @@ def test_norm_with_tiny_and_normal_elements_mixed(gd):
     for stage in (2, 3):
         assert out[stage][0] == out[0][0]
         assert np.array_equal(out[stage][1].view(np.uint32), out[0][1].view(np.uint32))
+
+
+@pytest.mark.parametrize("n,gd", [(1, "bf16"), (3, "bf16"), (6, "bf16"), (8, "bf16"), (16, "bf16"), (2, "fp32"),
+                                  (5, "fp32"), (9, "fp32")])
+def test_norm_of_unaligned_gradients(n, gd):
+    # Every unit's gradients placed 0..7 (bf16) or 0..3 (fp32) elements past a
+    # 16-byte boundary, differently per replica: the norm pass reads whole
+    # groups through shifted aligned words.  The norm must equal the one from
+    # 16-byte-aligned buffers bit for bit (same order) and the oracle's to
+    # 1e-12; the clipped state follows the oracle bit for bit.  Units span
+    # several chunks, a ragged last chunk and one shorter than a group.
+    from test_gpu_shifted import _register_offsets
+    pl = si.from_units([16384 * 3 + 77, 1552, 5, 40_003])
+    pb = make_problem(pl, n, 2, grad_dtype=gd, steps=2, seed=700 + n, max_norm=0.05)
+    k = 8 if gd == "bf16" else 4
+    offsets = [[(3 * r + u + 1) % k for u in range(k)] for r in range(n)]
+    ref_states, ref_norms = {}, []
+    oracle_run(pb, every_step=lambda t, s: ref_states.__setitem__(t, s), norms=ref_norms)
+    norms = {}
+    for mode in ("aligned", "shifted"):
+        fs = gpu_flatstep(pb)
+        try:
+            got = []
+            for t in (1, 2):
+                keep = []
+                flats = upload_grads(pb, t)
+                if mode == "aligned":
+                    register(fs, pb, flats, "separate", keep)
+                else:
+                    _register_offsets(fs, flats, offsets, keep)
+                fs.clip_grad_norm(pb.max_norm)
+                got.append(fs.grad_norm())
+                fs.step()
+                fs.post_step()
+                torch.cuda.synchronize()
+                compare_state(fs, ref_states[t], f"{mode} step {t}")
+            norms[mode] = got
+        finally:
+            fs.close()
+    assert norms["shifted"] == norms["aligned"]
+    for a, b in zip(norms["shifted"], ref_norms):
+        assert abs(a - b) <= 1e-12 * b, (a, b)

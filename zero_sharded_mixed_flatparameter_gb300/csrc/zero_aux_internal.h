@@ -28,6 +28,9 @@ struct NormSeg {
   long long chunk_start;  // first chunk's index within this launch
   long long out_start;    // first chunk's index in the workspace partials
   int vec_ok;             // 16-byte aligned gradients: vector loads allowed
+  // Otherwise replica r's gradient starts shift[r] elements past a 16-byte
+  // boundary: vector loads of aligned words, shifted into place.
+  unsigned char shift[kMaxRanks];
   float* keep;            // where to store this unit's reduced gradient, or nullptr
   int keep_vec;           // keep is 16-byte aligned: vector stores allowed
   const void* g[kMaxRanks];
@@ -42,8 +45,10 @@ struct NormArgs {
   NormSeg seg[kMaxSegs];
 };
 
-// Norm pass: one CTA per chunk; writes one partial per chunk.
-cudaError_t launch_grad_sq(const NormArgs& a, long long chunks, cudaStream_t stream);
+// Norm pass: one CTA per chunk; writes one partial per chunk.  `shifted`:
+// every segment of the launch has vec_ok == 0 (unaligned gradients; the
+// instances with shifted loads); otherwise every segment has vec_ok == 1.
+cudaError_t launch_grad_sq(const NormArgs& a, long long chunks, bool shifted, cudaStream_t stream);
 // Sums n partials in a fixed order and writes the norm and the clip
 // coefficient min(1, max_norm / (norm + 1e-6)) into the workspace header (NaN
 // when the norm is NaN).

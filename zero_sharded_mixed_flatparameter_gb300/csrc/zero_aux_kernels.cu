@@ -109,6 +109,76 @@ __device__ __forceinline__ void reduced8(const NormArgs& a, const NormSeg& s, lo
   for (int e = 0; e < kVec; ++e) g[e] = __fmul_rn(g[e], a.inv_n);
 }
 
+// reduced8 for a unit whose gradients are not 16-byte aligned: replica r
+// starts s.shift[r] elements past a boundary.  Lane L holds group grp and
+// lane L + 1 group grp + 1 (consecutive groups of the chunk), so each lane
+// loads the aligned word holding its group's first element and takes the
+// next word from its neighbour by warp shuffle; lane 31 (and a lane whose
+// neighbour has no full group) loads that word itself, issued with the
+// others.  Called by every lane of the warp; `full`: this lane's group is a
+// whole group of the unit.  Same values, same rank order as reduced8.
+template <int N, bool kFp32>
+__device__ __forceinline__ void shifted_reduced8(const NormArgs& a, const NormSeg& s, long long e0, bool full,
+                                                 float* g) {
+  const int lane = threadIdx.x & 31;
+  const bool nb_full = __shfl_down_sync(0xffffffffu, full ? 1 : 0, 1) != 0;
+  const bool own_next = full && (lane == 31 || !nb_full);
+  constexpr int W = kFp32 ? 2 : 1;  // 16-byte words of one group and replica
+  uint4 w[N][W + 1];
+#pragma unroll
+  for (int r = 0; r < N; ++r) {
+    const int phi = s.shift[r];
+    const uint4* words = reinterpret_cast<const uint4*>(static_cast<const char*>(s.g[r]) - phi * (kFp32 ? 4 : 2)) +
+                         (e0 / kVec) * W;
+#pragma unroll
+    for (int q = 0; q < W; ++q) w[r][q] = full ? ld_stream(words + q) : make_uint4(0u, 0u, 0u, 0u);
+    w[r][W] = (own_next && phi != 0) ? ld_stream(words + W) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int r = 0; r < N; ++r) {
+    const int phi = s.shift[r];  // uniform over the launch
+    if (phi != 0) {
+      const uint4 nb = make_uint4(__shfl_down_sync(0xffffffffu, w[r][0].x, 1), __shfl_down_sync(0xffffffffu, w[r][0].y, 1),
+                                  __shfl_down_sync(0xffffffffu, w[r][0].z, 1), __shfl_down_sync(0xffffffffu, w[r][0].w, 1));
+      if (!own_next) w[r][W] = nb;
+    }
+    float x[kVec];
+    if constexpr (!kFp32) {
+      const uint32_t u[8] = {w[r][0].x, w[r][0].y, w[r][0].z, w[r][0].w, w[r][1].x, w[r][1].y, w[r][1].z, w[r][1].w};
+      const int k = phi >> 1;
+      uint32_t t[6], v[5];
+#pragma unroll
+      for (int i = 0; i < 6; ++i) t[i] = (k & 2) ? u[i + 2] : u[i];
+#pragma unroll
+      for (int i = 0; i < 5; ++i) v[i] = (k & 1) ? t[i + 1] : t[i];
+      const uint32_t sh = static_cast<uint32_t>(phi & 1) * 16;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t y = __funnelshift_r(v[i], v[i + 1], sh);
+        x[2 * i] = bf16_lo(y);
+        x[2 * i + 1] = bf16_hi(y);
+      }
+    } else {
+      const uint32_t u[12] = {w[r][0].x, w[r][0].y, w[r][0].z, w[r][0].w, w[r][1].x, w[r][1].y,
+                              w[r][1].z, w[r][1].w, w[r][2].x, w[r][2].y, w[r][2].z, w[r][2].w};
+      uint32_t t[9];
+#pragma unroll
+      for (int i = 0; i < 9; ++i) t[i] = (phi & 2) ? u[i + 2] : u[i];
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) x[i] = __uint_as_float((phi & 1) ? t[i + 1] : t[i]);
+    }
+    if (r == 0) {
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) g[e] = x[e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) g[e] = __fadd_rn(g[e], x[e]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) g[e] = __fmul_rn(g[e], a.inv_n);
+}
+
 // Same reduction as the step (rank order, then x 1/N) for one element of any alignment.
 __device__ __forceinline__ float reduced1(const NormArgs& a, const NormSeg& s, long long k) {
   float acc;
@@ -171,8 +241,12 @@ __device__ __noinline__ double exact_thread_sum(const NormArgs& a, const NormSeg
   return w;
 }
 
-template <int N, bool kFp32>
-__global__ void __launch_bounds__(kStepThreads, NormShape<N, kFp32>::kMinBlocks)
+// kShifted instances take the launches of units whose gradients are not
+// 16-byte aligned (whole groups through shifted aligned words, one group at a
+// time, every register they need); the others take aligned units, so their
+// code and register budget are those of the aligned path alone.
+template <int N, bool kFp32, bool kShifted>
+__global__ void __launch_bounds__(kStepThreads, kShifted ? 1 : NormShape<N, kFp32>::kMinBlocks)
     grad_sq_kernel(const __grid_constant__ NormArgs a) {
   constexpr bool kPairs = NormShape<N, kFp32>::kPairs;
   __shared__ double smem[kStepThreads / 32];
@@ -187,6 +261,26 @@ __global__ void __launch_bounds__(kStepThreads, NormShape<N, kFp32>::kMinBlocks)
   const long long len = ZFS_CHECK(k >= 0 && k < s.n_chunks && c1 <= s.len) ? c1 - c0 : 0;
   SqAcc acc;
   long long grp = threadIdx.x;
+  if constexpr (kShifted) {
+    // Unaligned gradients: whole groups through shifted aligned words, in the
+    // same order.  The loop runs while any lane of the warp has a whole group
+    // (the shuffles need every lane); a lane advances only past whole groups,
+    // so it leaves at its first group that is not whole, which the loop below
+    // takes element by element.  Whole groups are a prefix of the lanes in
+    // every iteration, so two neighbouring lanes that both hold one hold
+    // consecutive groups.
+    for (;;) {
+      const bool full = grp * kVec + kVec <= len;
+      if (!__any_sync(0xffffffffu, full)) break;
+      float g[kVec];
+      shifted_reduced8<N, kFp32>(a, s, c0 + grp * kVec, full, g);
+      if (full) {
+        if (s.keep) keep8(s, c0 + grp * kVec, g);
+        acc.add8(g);
+        grp += kStepThreads;
+      }
+    }
+  }
   for (; kPairs && s.vec_ok && (grp + kStepThreads) * kVec + kVec <= len; grp += 2 * kStepThreads) {
     float g0[kVec], g1[kVec];
     reduced8<N, kFp32>(a, s, c0 + grp * kVec, g0);
@@ -509,32 +603,33 @@ cudaError_t launch_reduce_out(const ReduceArgs& a, cudaStream_t stream) {
 
 using NormKernel = void (*)(NormArgs);
 
-template <bool kFp32>
+template <bool kFp32, bool kShifted>
 NormKernel norm_kernel_for(int n) {
   switch (n) {
-    case 1: return grad_sq_kernel<1, kFp32>;
-    case 2: return grad_sq_kernel<2, kFp32>;
-    case 3: return grad_sq_kernel<3, kFp32>;
-    case 4: return grad_sq_kernel<4, kFp32>;
-    case 5: return grad_sq_kernel<5, kFp32>;
-    case 6: return grad_sq_kernel<6, kFp32>;
-    case 7: return grad_sq_kernel<7, kFp32>;
-    case 8: return grad_sq_kernel<8, kFp32>;
-    case 9: return grad_sq_kernel<9, kFp32>;
-    case 10: return grad_sq_kernel<10, kFp32>;
-    case 11: return grad_sq_kernel<11, kFp32>;
-    case 12: return grad_sq_kernel<12, kFp32>;
-    case 13: return grad_sq_kernel<13, kFp32>;
-    case 14: return grad_sq_kernel<14, kFp32>;
-    case 15: return grad_sq_kernel<15, kFp32>;
-    case 16: return grad_sq_kernel<16, kFp32>;
+    case 1: return grad_sq_kernel<1, kFp32, kShifted>;
+    case 2: return grad_sq_kernel<2, kFp32, kShifted>;
+    case 3: return grad_sq_kernel<3, kFp32, kShifted>;
+    case 4: return grad_sq_kernel<4, kFp32, kShifted>;
+    case 5: return grad_sq_kernel<5, kFp32, kShifted>;
+    case 6: return grad_sq_kernel<6, kFp32, kShifted>;
+    case 7: return grad_sq_kernel<7, kFp32, kShifted>;
+    case 8: return grad_sq_kernel<8, kFp32, kShifted>;
+    case 9: return grad_sq_kernel<9, kFp32, kShifted>;
+    case 10: return grad_sq_kernel<10, kFp32, kShifted>;
+    case 11: return grad_sq_kernel<11, kFp32, kShifted>;
+    case 12: return grad_sq_kernel<12, kFp32, kShifted>;
+    case 13: return grad_sq_kernel<13, kFp32, kShifted>;
+    case 14: return grad_sq_kernel<14, kFp32, kShifted>;
+    case 15: return grad_sq_kernel<15, kFp32, kShifted>;
+    case 16: return grad_sq_kernel<16, kFp32, kShifted>;
     default: return nullptr;
   }
 }
 
-cudaError_t launch_grad_sq(const NormArgs& a, long long chunks, cudaStream_t stream) {
+cudaError_t launch_grad_sq(const NormArgs& a, long long chunks, bool shifted, cudaStream_t stream) {
   if (chunks <= 0) return cudaSuccess;
-  NormKernel k = a.grad_fp32 ? norm_kernel_for<true>(a.n_ranks) : norm_kernel_for<false>(a.n_ranks);
+  NormKernel k = shifted ? (a.grad_fp32 ? norm_kernel_for<true, true>(a.n_ranks) : norm_kernel_for<false, true>(a.n_ranks))
+                         : (a.grad_fp32 ? norm_kernel_for<true, false>(a.n_ranks) : norm_kernel_for<false, false>(a.n_ranks));
   if (!k) return cudaErrorInvalidValue;
   k<<<static_cast<unsigned>(chunks), kStepThreads, 0, stream>>>(a);
   return cudaGetLastError();

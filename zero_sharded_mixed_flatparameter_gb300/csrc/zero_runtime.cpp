@@ -1087,40 +1087,54 @@ zero_status zero_clip_grad_norm_ex(zero_ctx* ctx, float max_norm, int32_t flags,
   const int N = ctx->cfg.n_ranks;
   int32_t launches = 0;
   int64_t out = 0;
-  int32_t i = 0;
-  while (i < ctx->n_units) {
-    zfs::NormArgs a;
-    std::memset(&a, 0, sizeof a);
-    a.n_ranks = N;
-    a.grad_fp32 = ctx->cfg.grad_dtype == ZERO_GRAD_FP32 ? 1 : 0;
-    a.inv_n = 1.0f / static_cast<float>(N);
-    a.partials = partials;
-    long long chunks = 0;
-    int n = 0;
-    for (; i < ctx->n_units && n < zfs::kMaxSegs; ++i) {
-      const int64_t c = unit_chunks(ctx, i);
-      if (c == 0) continue;
-      zfs::NormSeg& g = a.seg[n++];
-      g.len = ctx->unit_padded[i];
-      g.n_chunks = c;
-      g.chunk_start = chunks;
-      g.out_start = out;
-      g.vec_ok = 1;
-      g.keep = keep ? keep_base + ctx->unit_base[i] : nullptr;
-      g.keep_vec = keep && aligned(g.keep, 16) ? 1 : 0;
-      for (int r = 0; r < N; ++r) {
-        g.g[r] = ctx->grads[static_cast<size_t>(i) * zfs::kMaxRanks + r];
-        if (!aligned(g.g[r], 16)) g.vec_ok = 0;
-      }
-      chunks += c;
-      out += c;
+  // Units with 16-byte-aligned gradients and units without go to separate
+  // launches (the instances with shifted loads take the latter); partials
+  // keep their unit-order places whatever launch writes them.
+  zfs::NormArgs batch[2];
+  long long batch_chunks[2] = {0, 0};
+  for (int b = 0; b < 2; ++b) {
+    std::memset(&batch[b], 0, sizeof batch[b]);
+    batch[b].n_ranks = N;
+    batch[b].grad_fp32 = ctx->cfg.grad_dtype == ZERO_GRAD_FP32 ? 1 : 0;
+    batch[b].inv_n = 1.0f / static_cast<float>(N);
+    batch[b].partials = partials;
+  }
+  auto flush = [&](int b) -> cudaError_t {
+    if (batch[b].nseg == 0) return cudaSuccess;
+    const cudaError_t e = zfs::launch_grad_sq(batch[b], batch_chunks[b], b == 1, s);
+    if (e == cudaSuccess) ++launches;
+    batch[b].nseg = 0;
+    batch_chunks[b] = 0;
+    return e;
+  };
+  for (int32_t i = 0; i < ctx->n_units; ++i) {
+    const int64_t c = unit_chunks(ctx, i);
+    if (c == 0) continue;
+    zfs::NormSeg g{};
+    g.len = ctx->unit_padded[i];
+    g.n_chunks = c;
+    g.out_start = out;
+    g.vec_ok = 1;
+    g.keep = keep ? keep_base + ctx->unit_base[i] : nullptr;
+    g.keep_vec = keep && aligned(g.keep, 16) ? 1 : 0;
+    for (int r = 0; r < N; ++r) {
+      g.g[r] = ctx->grads[static_cast<size_t>(i) * zfs::kMaxRanks + r];
+      if (!aligned(g.g[r], 16)) g.vec_ok = 0;
+      g.shift[r] = static_cast<unsigned char>((reinterpret_cast<uintptr_t>(g.g[r]) % 16) / grad_bytes(ctx->cfg));
     }
-    a.nseg = n;
-    if (chunks > 0) {
-      const cudaError_t e = zfs::launch_grad_sq(a, chunks, s);
+    const int b = g.vec_ok ? 0 : 1;
+    if (batch[b].nseg == zfs::kMaxSegs) {
+      const cudaError_t e = flush(b);
       if (e != cudaSuccess) return fail_cuda(ctx, "norm kernel launch", e);
-      ++launches;
     }
+    g.chunk_start = batch_chunks[b];
+    batch[b].seg[batch[b].nseg++] = g;
+    batch_chunks[b] += c;
+    out += c;
+  }
+  for (int b = 0; b < 2; ++b) {
+    const cudaError_t e = flush(b);
+    if (e != cudaSuccess) return fail_cuda(ctx, "norm kernel launch", e);
   }
   const cudaError_t e = zfs::launch_clip_finalize(ws, out, max_norm, s);
   if (e != cudaSuccess) return fail_cuda(ctx, "clip finalize launch", e);
