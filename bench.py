@@ -102,7 +102,7 @@ def step_kernel_name(n: int, grad_dtype: str, clip_keep: bool, elems: int) -> st
     """The step kernel the library launches for an aligned segment (base a
     multiple of 8, gradients 16-byte aligned; the others take the
     shifted-gradient kernel, see Workbench.kernel_name): over >= 2^23
-    elements the barrier-free pipelined staged one for N = 8..12 bf16, the
+    elements the barrier-free pipelined staged one for N = 7..12 bf16, the
     tile-staged one with 2,048-element tiles for N >= 13 bf16 or
     N = 8, 9 fp32 replicas and the one with 4 elements per thread for N = 7
     or N >= 10 fp32 or N = 1..4 bf16 replicas; the register-staged one
@@ -114,7 +114,7 @@ def step_kernel_name(n: int, grad_dtype: str, clip_keep: bool, elems: int) -> st
     if grad_dtype == "bf16":
         if n <= 4:
             return "step_tma4_kernel"
-        if 8 <= n <= 12:
+        if 7 <= n <= 12:
             return "step_pipe_kernel"
         return "step_tma_kernel" if n >= 13 else "step_vec_kernel"
     if n >= 10 or n == 7:

@@ -17,7 +17,8 @@ import bench
     (2, "bf16", False, 10 ** 9, "step_tma4_kernel"),
     (4, "bf16", False, 10 ** 9, "step_tma4_kernel"),
     (5, "bf16", False, 10 ** 9, "step_vec_kernel"),
-    (7, "bf16", False, 10 ** 9, "step_vec_kernel"),
+    (6, "bf16", False, 10 ** 9, "step_vec_kernel"),
+    (7, "bf16", False, 10 ** 9, "step_pipe_kernel"),
     (10, "bf16", False, 10 ** 9, "step_pipe_kernel"),
     (12, "bf16", False, 10 ** 9, "step_pipe_kernel"),
     (13, "bf16", False, 10 ** 9, "step_tma_kernel"),

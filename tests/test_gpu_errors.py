@@ -127,7 +127,7 @@ def test_stage3_gather_argument_checks():
 
 @pytest.mark.parametrize("n,gd,tile,ctas_per_sm,threads", [(16, "bf16", 2048, 1, 256), (12, "fp32", 1024, 1, 256),
                                                             (2, "bf16", 1024, 2, 256), (4, "bf16", 2048, 1, 512),
-                                                            (10, "bf16", 2048, 1, 512)])
+                                                            (10, "bf16", 2048, 1, 512), (8, "bf16", 2048, 1, 512)])
 def test_staged_wait_runs_out_and_the_device_stays_usable(n, gd, tile, ctas_per_sm, threads):
     # The tile-staged step kernel bounds every wait for its bulk copies.  The
     # test hook announces the launch's first tile to its mbarrier without

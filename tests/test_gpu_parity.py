@@ -150,13 +150,14 @@ def test_set_lr_between_steps():
     fs.close()
 
 
-@pytest.mark.parametrize("n,gd", [(n, "bf16") for n in (1, 2, 3, 4, 5, 7, 8, 10, 12, 13, 16)]
+@pytest.mark.parametrize("n,gd", [(n, "bf16") for n in (1, 2, 3, 4, 5, 6, 7, 8, 10, 12, 13, 16)]
                          + [(n, "fp32") for n in (6, 7, 8, 9, 10, 11, 12, 16)])
 def test_tile_staged_kernel(n, gd):
-    # Over >= 2^23 elements per launch, N = 1..4 and N >= 8 bf16 and N >= 7
+    # Over >= 2^23 elements per launch, N = 1..4 and N >= 7 bf16 and N >= 7
     # fp32 replicas take a tile-staged (bulk copy) kernel: 2,048-element
     # tiles for bf16 N >= 13 and fp32 N = 8, 9; the barrier-free pipelined
-    # kernel (2,048-element tiles, three stages) for bf16 N = 8..12; 4
+    # kernel (2,048-element tiles, four stages at N = 7, 8, three from 9) for
+    # bf16 N = 7..12; 4
     # elements per thread (1,024- or 2,048-element tiles) for bf16 N = 1..4
     # and fp32 N = 7 and N >= 10.  The neighbours of the rank thresholds take
     # the register-staged one.  8.7 M elements in several segments, each with

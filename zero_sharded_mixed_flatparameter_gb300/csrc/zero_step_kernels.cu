@@ -829,15 +829,17 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_shift_kernel(const __gri
 // step_tma4_kernel's, so results are bit-identical.
 //
 // Measured on GB300 over 100 M bf16 elements (step GB/s against the kernel
-// each N took before): N = 8 6872 / 6781-6802 (register-staged; 6834-6844 /
-// 6785-6803 over the 73.4 M-param Llama-1024 layout), N = 9 6966 / 6748-6759,
-// N = 10 7025-7038 / 6753-6764, N = 11 7119-7121 / 6778-6787 (2,048-element
-// staged kernel), N = 12 7173 / 6914-6915.  512 threads with three stages of
-// 2,048-element tiles; 256-thread CTAs (two per SM, four stages), 384 threads
-// with four stages, 768 or 1,024 threads with two stages and 512 threads
-// with two stages measured 1-20 % slower at N = 8..10; at N <= 7, N >= 13
-// (two stages fit) and for fp32 gradients this kernel was slower than the
-// kernels those take.
+// each N took before): 512 threads with four stages of 2,048-element tiles at
+// N = 7 6902-6903 / 6771-6814 (register-staged) and N = 8 7003-7012 /
+// 6827-6830 (7001-7012 against 6826-6827 in another run; three stages
+// 6872; the 73.4 M-param Llama-1024 layout 6972 / 6798-6799), three stages
+// (four do not fit) at N = 9 6966 / 6748-6759, N = 10 7025-7038 / 6753-6764,
+// N = 11 7119-7121 / 6778-6787 (2,048-element staged kernel), N = 12 7173 /
+// 6914-6915.  256-thread CTAs (two per SM, four stages), 384 threads with
+// four stages, 768 or 1,024 threads with two stages and 512 threads with two
+// stages measured 1-20 % slower at N = 8..10; at N <= 6 (four or five stages
+// as well), N >= 13 (two stages fit) and for fp32 gradients this kernel was
+// slower than the kernels those take.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -1220,7 +1222,8 @@ cudaError_t launch_tma4_bf16(const StepArgs& a, cudaStream_t stream) {
 
 // A staged kernel where one measured faster than the register-staged kernel
 // (launches of at least kTmaMinElems elements): bf16 N = 1..4 (4-element
-// staged), N = 8..12 (barrier-free pipelined), N >= 13 (2,048-element
+// staged), N = 7..12 (barrier-free pipelined: four stages of 2,048-element
+// tiles at N = 7, 8, where they fit, three from N = 9), N >= 13 (2,048-element
 // staged); fp32 N >= 7.  Other rank counts return with *launched = false.
 template <bool kDevBias>
 cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launched) {
@@ -1231,7 +1234,8 @@ cudaError_t try_launch_tma(const StepArgs& a, cudaStream_t stream, bool* launche
       case 2: return launch_tma4_bf16<2, kDevBias>(a, stream);
       case 3: return launch_tma4_bf16<3, kDevBias>(a, stream);
       case 4: return launch_tma4_bf16<4, kDevBias>(a, stream);
-      case 8: return launch_pipe<8, false, 512, 3, 1, kDevBias>(a, stream);
+      case 7: return launch_pipe<7, false, 512, 4, 1, kDevBias>(a, stream);
+      case 8: return launch_pipe<8, false, 512, 4, 1, kDevBias>(a, stream);
       case 9: return launch_pipe<9, false, 512, 3, 1, kDevBias>(a, stream);
       case 10: return launch_pipe<10, false, 512, 3, 1, kDevBias>(a, stream);
       case 11: return launch_pipe<11, false, 512, 3, 1, kDevBias>(a, stream);
