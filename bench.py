@@ -588,9 +588,33 @@ def also_block(name: str, device, rank: int, args, peak: float) -> dict:
                              "gather_ms_median": statistics.median(r["gather_ms"]), "gather_bytes": 4 * wb.padded,
                              "gather_gbs": 4 * wb.padded / (g / 1e3) / 1e9,
                              "gather_frac": 4 * wb.padded / (g / 1e3) / 1e9 / peak}
+            out["gather_prefetch"] = prefetch_leg(wb, steps, peak)
         return out
     finally:
         wb.close()
+
+
+def prefetch_leg(wb: Workbench, steps: int, peak: float) -> dict:
+    """The same ZeRO-3 gathers issued as one zero_gather_units call for every
+    unit (the prefetch form: one kernel per 32 units instead of one per unit),
+    timed alone after the steps: 3 untimed calls, then ``steps`` calls, each
+    bracketed by CUDA events on the launching stream."""
+    import torch
+    fs, s = wb.fs, wb.stream
+    for _ in range(3):
+        fs.gather_units(0, wb.gather_bufs, stream=s)
+    ev = _pairs(steps)
+    torch.cuda.synchronize(wb.device)
+    for k in range(steps):
+        ev[k][0].record(s)
+        fs.gather_units(0, wb.gather_bufs, stream=s)
+        ev[k][1].record(s)
+    torch.cuda.synchronize(wb.device)
+    ms = _ms(ev)
+    g = statistics.mean(ms)
+    return {"units": len(wb.gather_bufs), "launches_per_call": fs.last_launches(), "calls": steps,
+            "gather_ms_mean": g, "gather_ms_median": statistics.median(ms), "gather_bytes": 4 * wb.padded,
+            "gather_gbs": 4 * wb.padded / (g / 1e3) / 1e9, "gather_frac": 4 * wb.padded / (g / 1e3) / 1e9 / peak}
 
 
 def e2e_leg(wb: Workbench, steps: int, warm: int, world: int) -> dict:

@@ -357,6 +357,25 @@ zero_status zero_grad_norm(zero_ctx* ctx, double* norm, void* stream);
 zero_status zero_gather_weights(zero_ctx* ctx, int32_t unit, void* unit_buf, void* stream);
 
 /*
+ * zero_gather_units — zero_gather_weights for `count` consecutive units
+ * first_unit .. first_unit + count - 1 at once: unit first_unit + k into
+ * unit_bufs[k] (a host array of `count` device pointers, each padded_i bf16
+ * elements, 2-byte aligned; NULL allowed only for empty units).  The
+ * ZeRO-3 prefetch of the source guide's DeepSpeed section (the parameter
+ * coordinator gathers the next modules' parameters ahead of use, several
+ * parameters coalesced into one collective) and Megatron's bucket-by-bucket
+ * parameter all-gather: the copies are those of zero_gather_weights, issued
+ * as one kernel per 32 units instead of one per unit.  The buffers must not
+ * overlap one another or the parameter storage.  count == 0 and stages 0-2:
+ * ZERO_OK without device work (unit_bufs may be NULL).
+ * Errors: ZERO_EINVAL (count < 0, units out of range, null unit_bufs, null
+ * or misaligned buffer of a non-empty unit at stage 3); ZERO_ESTATE (no
+ * buffers bound); ZERO_ECUDA.
+ */
+zero_status zero_gather_units(zero_ctx* ctx, int32_t first_unit, int32_t count, void* const* unit_bufs,
+                              void* stream);
+
+/*
  * zero_post_step — the protocol's post_step: forget the registered gradients
  * (and the pending clip coefficient) so the next step needs fresh ones.
  * ZERO_ESTATE unless a step was taken since the last post_step.  No device
@@ -559,7 +578,7 @@ zero_status zero_debug_check_failures(uint32_t* count);
 zero_status zero_step_count(const zero_ctx* ctx, int64_t* t);
 
 /*
- * Number of kernels the last zero_step / zero_gather_weights call on this
+ * Number of kernels the last zero_step / zero_gather_weights / zero_gather_units call on this
  * context enqueued (0 when it had nothing to do).  Host bookkeeping only.
  */
 zero_status zero_last_launches(const zero_ctx* ctx, int32_t* launches);

@@ -96,6 +96,9 @@ def test_state_machine_and_no_side_effects():
         # gather on a non-stage-3 context is a no-op that accepts NULL
         fs.gather_weights(0, None)
         assert _status(lambda: fs.gather_weights(7, None)) == B.ZERO_EINVAL
+        fs.gather_units(0, [None] * fs.n_units)
+        assert fs.last_launches() == 0
+        assert _status(lambda: fs.gather_units(1, [None] * fs.n_units)) == B.ZERO_EINVAL
     finally:
         fs.close()
 
@@ -121,6 +124,19 @@ def test_stage3_gather_argument_checks():
         fs.gather_weights(-1, full)
         torch.cuda.synchronize()
         assert torch.equal(full.view(torch.int16), fs.param16.view(torch.int16))
+        # several units at once: range, NULL and alignment checks
+        nu = fs.n_units
+        assert _status(lambda: B.zero_gather_units(fs.ctx, 0, [0] * nu, 0)) == B.ZERO_EINVAL
+        assert _status(lambda: B.zero_gather_units(fs.ctx, -1, [buf.data_ptr()], 0)) == B.ZERO_EINVAL
+        assert _status(lambda: B.zero_gather_units(fs.ctx, nu, [buf.data_ptr()], 0)) == B.ZERO_EINVAL
+        assert _status(lambda: B.zero_gather_units(fs.ctx, 0, [buf.data_ptr()] * (nu + 1), 0)) == B.ZERO_EINVAL
+        assert _status(lambda: B.zero_gather_units(fs.ctx, 0, [buf.data_ptr() + 1], 0)) == B.ZERO_EINVAL
+        assert B.load().zero_gather_units(fs.ctx, 0, 1, None, None) == B.ZERO_EINVAL  # NULL array
+        assert B.load().zero_gather_units(fs.ctx, 0, -1, None, None) == B.ZERO_EINVAL  # negative count
+        B.zero_gather_units(fs.ctx, nu, [], 0)  # an empty range at the end
+        assert fs.last_launches() == 0
+        with pytest.raises(ValueError, match="padded"):
+            fs.gather_units(0, [buf[2:]])
     finally:
         fs.close()
 

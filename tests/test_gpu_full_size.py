@@ -106,6 +106,15 @@ def run_full(pl, n, stage, grad_dtype, steps, seed, grad_std, outlier_fraction=0
                     torch.cuda.synchronize()
                     assert torch.equal(unit_buf.view(torch.int16), fs.param16[b:b + p].view(torch.int16))
                     del unit_buf
+                if t == steps:  # every unit in one call (the prefetch form)
+                    bufs = [torch.empty(int(p), dtype=torch.bfloat16, device="cuda") for p in lay.unit_padded]
+                    fs.gather_units(0, bufs)
+                    assert fs.last_launches() == 1
+                    torch.cuda.synchronize()
+                    for i, buf in enumerate(bufs):
+                        b, p = int(lay.unit_base[i]), int(lay.unit_padded[i])
+                        assert torch.equal(buf.view(torch.int16), fs.param16[b:b + p].view(torch.int16)), i
+                    del bufs
             fs.post_step()
             torch.cuda.synchronize()
             del grads

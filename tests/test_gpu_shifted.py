@@ -175,6 +175,15 @@ def test_llama_2048_units_one_buffer_per_unit(n):
                    to_np(fs.param16[a:a + W]))
             for name, g, w in zip(("master", "m", "v", "param16"), got, win[a]):
                 assert_bit_exact(g, w, f"N={n} window@{a} {name}")
+        # the ZeRO-3 gathers of these unaligned units: one launch for all ten
+        bufs = [torch.empty(int(fs.layout(i)[1]), dtype=torch.bfloat16, device="cuda") for i in range(fs.n_units)]
+        fs.gather_units(0, bufs)
+        assert fs.last_launches() == 1
+        torch.cuda.synchronize()
+        for i, buf in enumerate(bufs):
+            numel, padded, shard, base = fs.layout(i)
+            assert torch.equal(buf.view(torch.int16), fs.param16[base:base + padded].view(torch.int16)), i
+        del bufs
     finally:
         fs.close()
         torch.cuda.empty_cache()

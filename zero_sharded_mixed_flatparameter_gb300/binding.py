@@ -31,7 +31,7 @@ EXPORTED = (
     "zero_import_state", "zero_clip_workspace_bytes_ex", "zero_clip_grad_norm_ex", "zero_kernel_timeouts",
     "zero_make_master_offload", "zero_offload_workspace_bytes", "zero_offload_step", "zero_cpu_adam",
     "zero_debug_inject", "zero_debug_check_failures", "zero_capturable_workspace_bytes", "zero_enable_capturable",
-    "zero_disable_capturable", "zero_count_nonfinite", "zero_read_nonfinite",
+    "zero_disable_capturable", "zero_count_nonfinite", "zero_read_nonfinite", "zero_gather_units",
 )
 ZERO_CLIP_KEEP_REDUCED = 1
 ZERO_INJECT_MISSING_COPY = 1
@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH):
             "zero_reduce_grads": [vp, i32, vp, vp],
             "zero_step": [vp, vp],
             "zero_gather_weights": [vp, i32, vp, vp],
+            "zero_gather_units": [vp, i32, i32, P(vp), vp],
             "zero_post_step": [vp, vp],
             "zero_step_count": [vp, P(i64)],
             "zero_last_launches": [vp, P(i32)],
@@ -260,6 +261,13 @@ def zero_step(ctx: int, stream: int = 0) -> None:
 
 def zero_gather_weights(ctx: int, unit: int, unit_buf: int, stream: int = 0) -> None:
     _check(load().zero_gather_weights(ctx, unit, unit_buf or None, stream or None), ctx)
+
+
+def zero_gather_units(ctx: int, first_unit: int, unit_bufs, stream: int = 0) -> None:
+    """Units first_unit .. first_unit + len(unit_bufs) - 1 into the device
+    addresses unit_bufs (0 for an empty unit)."""
+    arr = (ctypes.c_void_p * max(len(unit_bufs), 1))(*[b or None for b in unit_bufs])
+    _check(load().zero_gather_units(ctx, first_unit, len(unit_bufs), arr, stream or None), ctx)
 
 
 def zero_post_step(ctx: int, stream: int = 0) -> None:

@@ -108,4 +108,25 @@ unsigned int aux_debug_failures();
 // ZeRO-3 unit gather: copy n bf16 elements; *launches counts the kernels enqueued.
 cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaStream_t stream, int* launches);
 
+// Several unit gathers in as few launches as the batch limits allow.
+constexpr int kMaxGatherUnits = 32;
+constexpr long long kMaxGatherCtas = 0x7fffffffLL;  // grid.x limit
+struct GatherUnit {
+  const uint16_t* src;
+  uint16_t* dst;
+  long long n;        // elements
+  long long nvec;     // 16-byte destination vectors (after the head when shifted)
+  long long threads;  // threads the unit's CTAs cover
+  int shifted;        // 0: aligned vector copy; 1: head + shifted vectors + tail
+  int head;           // shifted: elements before the destination is aligned
+  int phi;            // shifted: source offset from a 16-byte boundary there, in elements
+};
+struct GatherBatch {
+  int count;
+  long long cta_begin[kMaxGatherUnits + 1];
+  GatherUnit unit[kMaxGatherUnits];
+};
+cudaError_t launch_gather_units(const uint16_t* const* src, uint16_t* const* dst, const long long* n, int count,
+                                cudaStream_t stream, int* launches);
+
 }  // namespace zfs

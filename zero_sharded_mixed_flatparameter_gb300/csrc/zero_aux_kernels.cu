@@ -463,8 +463,8 @@ __global__ void copy_f32_kernel(const float* __restrict__ src, float* __restrict
 // stride loop) with plain loads and stores: measured as the fastest of the
 // copy variants tried — on 800 MB 6566 GB/s against 6353-6404 for a
 // persistent 8-CTA-per-SM grid with streaming hints (cudaMemcpyAsync: 6621).
-__global__ void gather_vec_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n16) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+__device__ __forceinline__ void gather_vec_body(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n16,
+                                                long long i) {
   if (i < n16) dst[i] = src[i];
 }
 
@@ -477,9 +477,9 @@ __global__ void gather_vec_kernel(const uint4* __restrict__ src, uint4* __restri
 // with the next word — which the neighbouring lane loaded as its own (warp
 // shuffle), or, for lane 31 and the last vector, this lane loads itself.
 // The threads after the last vector copy the head and the ragged tail.
-__global__ void gather_shift_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, long long n,
-                                    int head, int phi, long long nvec) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+// Every lane of a warp must call this with the same unit (the shuffle).
+__device__ __forceinline__ void gather_shift_body(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                                  long long n, int head, int phi, long long nvec, long long i) {
   const int lane = threadIdx.x & 31;
   const bool active = i < nvec;
   const uint4* words = reinterpret_cast<const uint4*>(src + head - phi);  // 16-byte aligned
@@ -489,7 +489,7 @@ __global__ void gather_shift_kernel(const uint16_t* __restrict__ src, uint16_t* 
     w0 = words[i];
     if (own_next && phi != 0) w1 = words[i + 1];
   }
-  if (phi != 0) {  // uniform over the launch; every lane takes part in the shuffle
+  if (phi != 0) {  // uniform over the unit; every lane takes part in the shuffle
     const uint4 nb = make_uint4(__shfl_down_sync(0xffffffffu, w0.x, 1), __shfl_down_sync(0xffffffffu, w0.y, 1),
                                 __shfl_down_sync(0xffffffffu, w0.z, 1), __shfl_down_sync(0xffffffffu, w0.w, 1));
     if (!own_next) w1 = nb;
@@ -514,6 +514,37 @@ __global__ void gather_shift_kernel(const uint16_t* __restrict__ src, uint16_t* 
   if (q >= 0 && q < 16) {
     const long long k = q < head ? q : head + 8 * nvec + (q - head);
     if ((q < head || q - head < 8) && k < n) dst[k] = src[k];
+  }
+}
+
+__global__ void gather_vec_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n16) {
+  gather_vec_body(src, dst, n16, static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
+}
+
+__global__ void gather_shift_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, long long n,
+                                    int head, int phi, long long nvec) {
+  gather_shift_body(src, dst, n, head, phi, nvec, static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
+}
+
+// Several units in one launch (a prefetch of the next units, the way ZeRO-3
+// implementations gather more than one module's parameters ahead of use):
+// unit u owns CTAs [cta_begin[u], cta_begin[u+1]), so every CTA — and every
+// warp's shuffle — stays within one unit; aligned units take the vector body,
+// the others the shifted one.  One launch instead of one per unit spares the
+// ramp and drain between consecutive copies.
+__global__ void __launch_bounds__(kStepThreads) gather_units_kernel(const __grid_constant__ GatherBatch b) {
+  const long long blk = blockIdx.x;
+  int lo = 0, hi = b.count - 1;  // the last unit with cta_begin <= blk
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (b.cta_begin[mid] <= blk) lo = mid; else hi = mid - 1;
+  }
+  const GatherUnit& g = b.unit[lo];
+  const long long i = (blk - b.cta_begin[lo]) * blockDim.x + threadIdx.x;
+  if (g.shifted) {
+    gather_shift_body(g.src, g.dst, g.n, g.head, g.phi, g.nvec, i);
+  } else {
+    gather_vec_body(reinterpret_cast<const uint4*>(g.src), reinterpret_cast<uint4*>(g.dst), g.nvec, i);
   }
 }
 
@@ -683,28 +714,77 @@ cudaError_t launch_copy_f32(const float* src, float* dst, long long n, cudaStrea
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaStream_t stream, int* launches) {
-  if (n <= 0) return cudaSuccess;
+namespace {
+
+// How one unit is copied: the vector body when source and destination are
+// 16-byte aligned and the unit is whole vectors, else the shifted body.
+GatherUnit plan_gather(const uint16_t* src, uint16_t* dst, long long n) {
+  GatherUnit g{};
+  g.src = src;
+  g.dst = dst;
+  g.n = n;
   const bool aligned = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (reinterpret_cast<uintptr_t>(dst) % 16 == 0);
   if (aligned && n % 8 == 0) {
-    // one thread per vector: under 2^31 blocks for any unit a device can hold
-    const long long n16 = n / 8;
-    const long long grid = (n16 + kStepThreads - 1) / kStepThreads;
-    gather_vec_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(
-        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), n16);
+    g.nvec = n / 8;
+    g.threads = g.nvec;
   } else {
     // the destination aligned after `head` elements; the source's offset
     // from a 16-byte boundary there, in elements
-    const long long head = std::min<long long>(n, (8 - static_cast<long long>(reinterpret_cast<uintptr_t>(dst) / 2 % 8)) % 8);
-    const int phi = static_cast<int>(reinterpret_cast<uintptr_t>(src + head) / 2 % 8);
-    const long long nvec = (n - head) / 8;
-    const long long grid = (nvec + 2 * kVec + kStepThreads - 1) / kStepThreads;
-    gather_shift_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(src, dst, n, static_cast<int>(head),
-                                                                                   phi, nvec);
+    const long long head =
+        std::min<long long>(n, (8 - static_cast<long long>(reinterpret_cast<uintptr_t>(dst) / 2 % 8)) % 8);
+    g.shifted = 1;
+    g.head = static_cast<int>(head);
+    g.phi = static_cast<int>(reinterpret_cast<uintptr_t>(src + head) / 2 % 8);
+    g.nvec = (n - head) / 8;
+    g.threads = g.nvec + 2 * kVec;  // the head and tail threads after the vectors
+  }
+  return g;
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaStream_t stream, int* launches) {
+  if (n <= 0) return cudaSuccess;
+  const GatherUnit g = plan_gather(src, dst, n);
+  // one thread per vector: under 2^31 blocks for any unit a device can hold
+  const long long grid = (g.threads + kStepThreads - 1) / kStepThreads;
+  if (!g.shifted) {
+    gather_vec_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(
+        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), g.nvec);
+  } else {
+    gather_shift_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(src, dst, n, g.head, g.phi,
+                                                                                   g.nvec);
   }
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ++*launches;
   return e;
+}
+
+cudaError_t launch_gather_units(const uint16_t* const* src, uint16_t* const* dst, const long long* n, int count,
+                                cudaStream_t stream, int* launches) {
+  GatherBatch b{};
+  auto flush = [&]() -> cudaError_t {
+    if (b.count == 0) return cudaSuccess;
+    const long long grid = b.cta_begin[b.count];
+    gather_units_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(b);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) ++*launches;
+    b = GatherBatch{};
+    return e;
+  };
+  for (int k = 0; k < count; ++k) {
+    if (n[k] <= 0) continue;
+    const GatherUnit g = plan_gather(src[k], dst[k], n[k]);
+    const long long ctas = (g.threads + kStepThreads - 1) / kStepThreads;
+    if (b.count == kMaxGatherUnits || b.cta_begin[b.count] + ctas > kMaxGatherCtas) {
+      const cudaError_t e = flush();
+      if (e != cudaSuccess) return e;
+    }
+    b.unit[b.count] = g;
+    b.cta_begin[b.count + 1] = b.cta_begin[b.count] + ctas;
+    ++b.count;
+  }
+  return flush();
 }
 
 }  // namespace zfs

@@ -1185,6 +1185,40 @@ zero_status zero_gather_weights(zero_ctx* ctx, int32_t unit, void* unit_buf, voi
   return ZERO_OK;
 }
 
+zero_status zero_gather_units(zero_ctx* ctx, int32_t first_unit, int32_t count, void* const* unit_bufs,
+                              void* stream) {
+  if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");
+  zero_status st = require_bound(ctx);
+  if (st != ZERO_OK) return st;
+  if (count < 0) return fail(ctx, ZERO_EINVAL, "count %d is negative", count);
+  if (first_unit < 0 || first_unit > ctx->n_units || count > ctx->n_units - first_unit) {
+    return fail(ctx, ZERO_EINVAL, "units [%d, %d + %d) out of range (%d units)", first_unit, first_unit, count,
+                ctx->n_units);
+  }
+  ctx->last_launches = 0;
+  if (ctx->cfg.stage != 3 || count == 0) return ZERO_OK;  // stages 0-2: the step wrote every full copy
+  if (!unit_bufs) return fail(ctx, ZERO_EINVAL, "unit_bufs is NULL");
+  std::vector<const uint16_t*> src;
+  std::vector<uint16_t*> dst;
+  std::vector<long long> len;
+  for (int32_t k = 0; k < count; ++k) {
+    const int32_t u = first_unit + k;
+    if (ctx->unit_padded[u] == 0) continue;
+    void* buf = unit_bufs[k];
+    if (!buf) return fail(ctx, ZERO_EINVAL, "unit_bufs[%d] (unit %d) is NULL", k, u);
+    if (!aligned(buf, 2)) return fail(ctx, ZERO_EINVAL, "unit_bufs[%d] (unit %d) is not 2-byte aligned", k, u);
+    src.push_back(static_cast<const uint16_t*>(ctx->bufs.param16) + ctx->unit_base[u]);
+    dst.push_back(static_cast<uint16_t*>(buf));
+    len.push_back(ctx->unit_padded[u]);
+  }
+  int32_t launches = 0;
+  const cudaError_t e = zfs::launch_gather_units(src.data(), dst.data(), len.data(), static_cast<int>(src.size()),
+                                                 static_cast<cudaStream_t>(stream), &launches);
+  if (e != cudaSuccess) return fail_cuda(ctx, "gather kernel launch", e);
+  ctx->last_launches = launches;
+  return ZERO_OK;
+}
+
 zero_status zero_post_step(zero_ctx* ctx, void* stream) {
   (void)stream;
   if (!ctx) return fail(nullptr, ZERO_EINVAL, "ctx is NULL");

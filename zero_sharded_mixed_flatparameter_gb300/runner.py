@@ -202,6 +202,23 @@ class FlatStep:
                 raise ValueError(f"the gather buffer must hold the padded {need} elements, got {out.numel()}")
         B.zero_gather_weights(self.ctx, unit, out.data_ptr() if out is not None else 0, self.stream_handle(stream))
 
+    def gather_units(self, first_unit: int, outs: Sequence[Optional[torch.Tensor]], stream=None) -> None:
+        """ZeRO-3 prefetch: units first_unit .. first_unit + len(outs) - 1
+        into `outs` (one bf16 device tensor per unit, None for an empty unit)
+        with one kernel per 32 units; a no-op for stages 0-2."""
+        if self.stage == 3:
+            for k, out in enumerate(outs):
+                need = self._need(first_unit + k) if 0 <= first_unit + k < self.n_units else 0
+                if out is None:
+                    continue
+                if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.device != self.device:
+                    raise ValueError("a gather buffer must be a contiguous bf16 device tensor")
+                if out.numel() < need:
+                    raise ValueError(f"the gather buffer of unit {first_unit + k} must hold the padded {need} "
+                                     f"elements, got {out.numel()}")
+        B.zero_gather_units(self.ctx, first_unit, [o.data_ptr() if o is not None else 0 for o in outs],
+                            self.stream_handle(stream))
+
     def post_step(self, stream=None) -> None:
         B.zero_post_step(self.ctx, self.stream_handle(stream))
         self._registered.clear()
