@@ -232,6 +232,16 @@ def run_gpu(pb: Problem, mode: str = "units", every_step=None, guard: int = 64,
                     fs.gather_weights(i, buf)
                     torch.cuda.synchronize()
                     assert torch.equal(buf[:padded].view(torch.int16), fs.param16[base:base + padded].view(torch.int16))
+                # the same units in one call (the prefetch form), each buffer
+                # one element past a 16-byte boundary on odd steps
+                o = t % 2
+                bufs = [torch.empty(int(fs.layout(i)[1]) + o, dtype=torch.bfloat16, device="cuda")[o:]
+                        for i in range(fs.n_units)]
+                fs.gather_units(0, bufs)
+                torch.cuda.synchronize()
+                for i, buf in enumerate(bufs):
+                    numel, padded, shard, base = fs.layout(i)
+                    assert torch.equal(buf.view(torch.int16), fs.param16[base:base + padded].view(torch.int16)), i
             fs.post_step()
             torch.cuda.synchronize()
             if every_step:
