@@ -109,20 +109,16 @@ __device__ __forceinline__ void reduced8(const NormArgs& a, const NormSeg& s, lo
   for (int e = 0; e < kVec; ++e) g[e] = __fmul_rn(g[e], a.inv_n);
 }
 
-// reduced8 for a unit whose gradients are not 16-byte aligned: replica r
-// starts s.shift[r] elements past a boundary.  Lane L holds group grp and
-// lane L + 1 group grp + 1 (consecutive groups of the chunk), so each lane
-// loads the aligned word holding its group's first element and takes the
-// next word from its neighbour by warp shuffle; lane 31 (and a lane whose
-// neighbour has no full group) loads that word itself, issued with the
-// others.  Called by every lane of the warp; `full`: this lane's group is a
-// whole group of the unit.  Same values, same rank order as reduced8.
+// reduced8 for a whole group of a unit whose gradients are not 16-byte
+// aligned: replica r starts s.shift[r] elements past a boundary, so the
+// group's elements lie in W + 1 aligned 16-byte words (W for phi == 0), all
+// loaded before any is used; the word past the group starts inside it.  The
+// last word is also the next thread's first: the duplicate request is served
+// on chip (against taking it from the neighbouring lane by warp shuffle:
+// N = 3 bf16 +11 %, elsewhere within 1 %).  Same values, same rank order as
+// reduced8.
 template <int N, bool kFp32>
-__device__ __forceinline__ void shifted_reduced8(const NormArgs& a, const NormSeg& s, long long e0, bool full,
-                                                 float* g) {
-  const int lane = threadIdx.x & 31;
-  const bool nb_full = __shfl_down_sync(0xffffffffu, full ? 1 : 0, 1) != 0;
-  const bool own_next = full && (lane == 31 || !nb_full);
+__device__ __forceinline__ void shifted_reduced8(const NormArgs& a, const NormSeg& s, long long e0, float* g) {
   constexpr int W = kFp32 ? 2 : 1;  // 16-byte words of one group and replica
   uint4 w[N][W + 1];
 #pragma unroll
@@ -131,17 +127,12 @@ __device__ __forceinline__ void shifted_reduced8(const NormArgs& a, const NormSe
     const uint4* words = reinterpret_cast<const uint4*>(static_cast<const char*>(s.g[r]) - phi * (kFp32 ? 4 : 2)) +
                          (e0 / kVec) * W;
 #pragma unroll
-    for (int q = 0; q < W; ++q) w[r][q] = full ? ld_stream(words + q) : make_uint4(0u, 0u, 0u, 0u);
-    w[r][W] = (own_next && phi != 0) ? ld_stream(words + W) : make_uint4(0u, 0u, 0u, 0u);
+    for (int q = 0; q < W; ++q) w[r][q] = ld_stream(words + q);
+    w[r][W] = phi != 0 ? ld_stream(words + W) : make_uint4(0u, 0u, 0u, 0u);
   }
 #pragma unroll
   for (int r = 0; r < N; ++r) {
     const int phi = s.shift[r];  // uniform over the launch
-    if (phi != 0) {
-      const uint4 nb = make_uint4(__shfl_down_sync(0xffffffffu, w[r][0].x, 1), __shfl_down_sync(0xffffffffu, w[r][0].y, 1),
-                                  __shfl_down_sync(0xffffffffu, w[r][0].z, 1), __shfl_down_sync(0xffffffffu, w[r][0].w, 1));
-      if (!own_next) w[r][W] = nb;
-    }
     float x[kVec];
     if constexpr (!kFp32) {
       const uint32_t u[8] = {w[r][0].x, w[r][0].y, w[r][0].z, w[r][0].w, w[r][1].x, w[r][1].y, w[r][1].z, w[r][1].w};
@@ -263,22 +254,13 @@ __global__ void __launch_bounds__(kStepThreads, kShifted ? 1 : NormShape<N, kFp3
   long long grp = threadIdx.x;
   if constexpr (kShifted) {
     // Unaligned gradients: whole groups through shifted aligned words, in the
-    // same order.  The loop runs while any lane of the warp has a whole group
-    // (the shuffles need every lane); a lane advances only past whole groups,
-    // so it leaves at its first group that is not whole, which the loop below
-    // takes element by element.  Whole groups are a prefix of the lanes in
-    // every iteration, so two neighbouring lanes that both hold one hold
-    // consecutive groups.
-    for (;;) {
-      const bool full = grp * kVec + kVec <= len;
-      if (!__any_sync(0xffffffffu, full)) break;
+    // same order; a thread leaves at its first group that is not whole, which
+    // the loop below takes element by element.
+    for (; grp * kVec + kVec <= len; grp += kStepThreads) {
       float g[kVec];
-      shifted_reduced8<N, kFp32>(a, s, c0 + grp * kVec, full, g);
-      if (full) {
-        if (s.keep) keep8(s, c0 + grp * kVec, g);
-        acc.add8(g);
-        grp += kStepThreads;
-      }
+      shifted_reduced8<N, kFp32>(a, s, c0 + grp * kVec, g);
+      if (s.keep) keep8(s, c0 + grp * kVec, g);
+      acc.add8(g);
     }
   }
   for (; kPairs && s.vec_ok && (grp + kStepThreads) * kVec + kVec <= len; grp += 2 * kStepThreads) {
@@ -473,26 +455,20 @@ __device__ __forceinline__ void gather_vec_body(const uint4* __restrict__ src, u
 // multiple of N moved it, CMU 15-779 Lecture 13 notes §3.6): the first
 // `head` elements are copied one by one so that the destination is aligned
 // from there on; thread i then writes destination vector i, built from the
-// aligned source word that holds its first element, shifted by phi elements
-// with the next word — which the neighbouring lane loaded as its own (warp
-// shuffle), or, for lane 31 and the last vector, this lane loads itself.
-// The threads after the last vector copy the head and the ragged tail.
-// Every lane of a warp must call this with the same unit (the shuffle).
+// two aligned source words that hold its elements, shifted by phi elements
+// (the second word starts inside the unit: its first phi elements are the
+// vector's last).  The second word is also the next thread's first: the
+// duplicate request is served on chip (measured 3-4 % faster than passing
+// it between lanes by warp shuffle).  The threads after the last vector
+// copy the head and the ragged tail.
 __device__ __forceinline__ void gather_shift_body(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
                                                   long long n, int head, int phi, long long nvec, long long i) {
-  const int lane = threadIdx.x & 31;
   const bool active = i < nvec;
   const uint4* words = reinterpret_cast<const uint4*>(src + head - phi);  // 16-byte aligned
-  const bool own_next = active && (lane == 31 || i + 1 >= nvec);
   uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = make_uint4(0u, 0u, 0u, 0u);
   if (active && ZFS_CHECK(head + 8 * i + 8 <= n)) {
     w0 = words[i];
-    if (own_next && phi != 0) w1 = words[i + 1];
-  }
-  if (phi != 0) {  // uniform over the unit; every lane takes part in the shuffle
-    const uint4 nb = make_uint4(__shfl_down_sync(0xffffffffu, w0.x, 1), __shfl_down_sync(0xffffffffu, w0.y, 1),
-                                __shfl_down_sync(0xffffffffu, w0.z, 1), __shfl_down_sync(0xffffffffu, w0.w, 1));
-    if (!own_next) w1 = nb;
+    if (phi != 0) w1 = words[i + 1];
   }
   if (active && ZFS_CHECK(head + 8 * i + 8 <= n)) {
     uint4 out = w0;
@@ -528,9 +504,9 @@ __global__ void gather_shift_kernel(const uint16_t* __restrict__ src, uint16_t* 
 
 // Several units in one launch (a prefetch of the next units, the way ZeRO-3
 // implementations gather more than one module's parameters ahead of use):
-// unit u owns CTAs [cta_begin[u], cta_begin[u+1]), so every CTA — and every
-// warp's shuffle — stays within one unit; aligned units take the vector body,
-// the others the shifted one.  One launch instead of one per unit spares the
+// unit u owns CTAs [cta_begin[u], cta_begin[u+1]), so every CTA stays within
+// one unit (its branch between the bodies is uniform); aligned units take
+// the vector body, the others the shifted one.  One launch instead of one per unit spares the
 // ramp and drain between consecutive copies.
 __global__ void __launch_bounds__(kStepThreads) gather_units_kernel(const __grid_constant__ GatherBatch b) {
   const long long blk = blockIdx.x;

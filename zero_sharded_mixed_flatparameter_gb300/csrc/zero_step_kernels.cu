@@ -644,16 +644,17 @@ __global__ void __launch_bounds__(kThreads, 1) step_tma4_kernel(const __grid_con
 // so that the body's master, m, v and bf16 parameters are 16-byte aligned,
 // and records per replica how many elements (phi) its gradient sits past a
 // 16-byte boundary at the body's start.  A thread takes 8 body elements per
-// iteration as step_vec8 does; for a replica with phi != 0 it loads the
-// aligned 16-byte word that holds the vector's first elements, takes the
-// next word from the neighbouring lane by warp shuffle (that lane loaded it
-// as its own first word), loads it itself only where the neighbour holds
-// another vector, and funnel-shifts the 32 bytes into place.  DRAM traffic is
-// that of the aligned kernel; the arithmetic and its order are step_vec8's,
-// so the results are bit-identical.  Heads and ragged ends (at most 7
-// elements each per segment) go element by element.
+// iteration as step_vec8 does; for a replica with phi != 0 it loads the two
+// aligned 16-byte words that hold the vector's elements and funnel-shifts
+// them into place.  The second word is also the next lane's first: the
+// duplicate request is served on chip, so DRAM traffic is that of the
+// aligned kernel (measured against taking the word from the neighbouring
+// lane by warp shuffle: level for bf16, +6 % for fp32 gradients at N = 3 —
+// the shuffles and the bookkeeping of which lane loads cost more issue slots
+// than the extra on-chip request).  The arithmetic and its order are
+// step_vec8's, so the results are bit-identical.  Heads and ragged ends (at
+// most 7 elements each per segment) go element by element.
 // ---------------------------------------------------------------------------
-constexpr unsigned kFullWarp = 0xffffffffu;
 
 // Elements phi .. phi + 7 of the 16 bf16 in (lo, hi), 0 <= phi < 8.
 __device__ __forceinline__ uint4 shift_bf16x8(const uint4& lo, const uint4& hi, int phi) {
@@ -683,24 +684,17 @@ __device__ __forceinline__ float4 u4_as_f4(const uint4& w) {
   return make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w));
 }
 
-__device__ __forceinline__ uint4 shfl_down_u4(const uint4& w) {
-  return make_uint4(__shfl_down_sync(kFullWarp, w.x, 1), __shfl_down_sync(kFullWarp, w.y, 1),
-                    __shfl_down_sync(kFullWarp, w.z, 1), __shfl_down_sync(kFullWarp, w.w, 1));
-}
-
-// One iteration of the shifted-gradient kernel: vector vi of segment si.
-// Called by every lane of the warp (the shuffles need all 32).  `active`: vi
-// is a vector of the segment; `own_next`: the next lane does not hold vector
-// vi + 1 (it is lane 31's successor, or inactive, or at the stride's wrap),
-// so this lane loads the word past its vector itself.  Every load of the
-// iteration — gradient words, that extra word, master, m, v — is issued
-// before any of them is used, as in step_vec8; the shuffles then pass each
-// lane its neighbour's first word.
+// One iteration of the shifted-gradient kernel: vector vi of segment si (a
+// whole vector of the body).  Every load of the iteration — the gradient
+// words, master, m, v — is issued before any of them is used, as in
+// step_vec8.  The word past the vector is loaded only for phi != 0: its
+// first phi elements are the vector's last ones, so it starts inside the
+// segment.
 template <int N, bool kFp32>
-__device__ __forceinline__ void shifted_vec8(const StepArgs& a, const Seg& s, int si, long long vi, bool active,
-                                             bool own_next, float clip, float bc1, float bc2, unsigned& nf) {
+__device__ __forceinline__ void shifted_vec8(const StepArgs& a, const Seg& s, int si, long long vi, float clip,
+                                             float bc1, float bc2, unsigned& nf) {
   const long long j = s.base + vi * kVec;
-  const bool ok = active && ZFS_CHECK(vi >= 0 && (vi + 1) * kVec <= s.len && j >= 0 && j + kVec <= a.total_padded);
+  const bool ok = ZFS_CHECK(vi >= 0 && (vi + 1) * kVec <= s.len && j >= 0 && j + kVec <= a.total_padded);
   constexpr int kWords = kFp32 ? 2 : 1;  // 16-byte words per replica and vector
   uint4 w[N][kWords + 1];
 #pragma unroll
@@ -710,7 +704,7 @@ __device__ __forceinline__ void shifted_vec8(const StepArgs& a, const Seg& s, in
                         vi * kWords;
 #pragma unroll
     for (int q = 0; q < kWords; ++q) w[r][q] = ok ? ld_stream(base + q) : make_uint4(0u, 0u, 0u, 0u);
-    w[r][kWords] = (ok && own_next && phi != 0) ? ld_stream(base + kWords) : make_uint4(0u, 0u, 0u, 0u);
+    w[r][kWords] = (ok && phi != 0) ? ld_stream(base + kWords) : make_uint4(0u, 0u, 0u, 0u);
   }
   const float4 zero = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   const float4 w0 = ok ? ld_stream_f4(a.master + j) : zero, w1 = ok ? ld_stream_f4(a.master + j + 4) : zero;
@@ -721,10 +715,6 @@ __device__ __forceinline__ void shifted_vec8(const StepArgs& a, const Seg& s, in
   for (int r = 0; r < N; ++r) {
     const int phi = a.gshift[si][r];  // uniform over the launch
     float x[kVec];
-    if (phi != 0) {
-      const uint4 nb = shfl_down_u4(w[r][0]);
-      if (!own_next) w[r][kWords] = nb;
-    }
     if constexpr (!kFp32) {
       const uint4 y = phi != 0 ? shift_bf16x8(w[r][0], w[r][1], phi) : w[r][0];
       x[0] = bf16_lo(y.x); x[1] = bf16_hi(y.x); x[2] = bf16_lo(y.y); x[3] = bf16_hi(y.y);
@@ -781,7 +771,6 @@ template <int N, bool kFp32, bool kDevBias>
 __global__ void __launch_bounds__(kStepThreads, 1) step_shift_kernel(const __grid_constant__ StepArgs a) {
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  const int lane = threadIdx.x & 31;
   float bc1, bc2;
   if (!step_bias<kDevBias>(a, &bc1, &bc2)) return;  // the same for every thread
   const float clip = a.clip ? *a.clip : 1.0f;
@@ -789,14 +778,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_shift_kernel(const __gri
   for (int si = 0; si < a.nseg; ++si) {
     const Seg& seg = a.seg[si];
     const long long nvec = seg.len / kVec;
-    // The loop runs while any lane of the warp has a vector: the shuffles
-    // need every lane.
-    for (long long vi = first_index(tid, seg.vec_start, stride); __any_sync(kFullWarp, vi < nvec); vi += stride) {
-      const bool active = vi < nvec;
-      const long long nb_vi = __shfl_down_sync(kFullWarp, vi, 1);
-      const int nb_active = __shfl_down_sync(kFullWarp, active ? 1 : 0, 1);
-      const bool own_next = !(lane < 31 && nb_active && nb_vi == vi + 1);
-      shifted_vec8<N, kFp32>(a, seg, si, vi, active, own_next, clip, bc1, bc2, nf);
+    for (long long vi = first_index(tid, seg.vec_start, stride); vi < nvec; vi += stride) {
+      shifted_vec8<N, kFp32>(a, seg, si, vi, clip, bc1, bc2, nf);
     }
   }
   // Heads and ragged ends: 16 threads per segment, at most 7 + 7 elements.
