@@ -15,7 +15,7 @@ constexpr int kVec = 8;           // elements per thread-iteration (16 B of bf16
 constexpr int kStepThreads = 256; // threads per CTA of the step kernels
 constexpr int kStepCtasPerSm = 2; // resident CTAs per SM of the vector step kernel
 // Tile-staged (TMA bulk copy) step kernels: used for launches of at least
-// kTmaMinElems elements with bf16 replicas N = 1..4 or N >= 11 and fp32
+// kTmaMinElems elements with bf16 replicas N = 1..4 or N >= 7 and fp32
 // replicas N >= 7 (the rank counts where they measured faster).
 constexpr long long kTmaMinElems = 1LL << 23;
 constexpr long long kTmaTile = 2048; // elements per tile (one 8-element vector per thread)

@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
 // ---------------------------------------------------------------------------
 // Staged kernel for many replicas: TMA (1-D bulk copy) of whole tiles.
 //
-// With N >= 11 bf16 replicas (N = 8 or 9 fp32) the step is
+// With N >= 13 bf16 replicas (N = 8 or 9 fp32) the step is
 // read-heavy and has 3 + N input streams.  Here one thread per CTA moves each
 // kTmaTile-element tile of every input stream into shared memory with one
 // cp.async.bulk per stream (4-8 KB contiguous requests), completing on an
@@ -194,7 +194,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_vec_kernel(const __grid_
 // N = 16 7200 / 6618; fp32 N = 8 7164 / 6651, N = 9 7190 / 6634.  At bf16
 // N <= 10 (N = 8: 6143 / 6806), fp32 N = 7 and fp32 N >= 10 the
 // register-staged kernel is as fast or faster than this kernel (fp32 N = 7,
-// N >= 10 and bf16 N = 1..4 have their own staged shapes, step_tma4_kernel);
+// N >= 10 and bf16 N = 1..4 have their own staged shapes, step_tma4_kernel,
+// and bf16 N = 7..12 the pipelined step_pipe_kernel, faster than this one
+// from N = 11 on as well);
 // so it does for launches of fewer than kTmaMinElems elements, where one CTA
 // per SM works through too few tiles to hide the latency of each (N = 16
 // bf16: 2363 / 3152 GB/s at 1 M elements, 5481 / 5479 at 6 M, 6179 / 5962
@@ -795,7 +797,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_shift_kernel(const __gri
 }
 
 // ---------------------------------------------------------------------------
-// Tile-staged kernel without a CTA barrier in its loop (bf16 N = 8..12).
+// Tile-staged kernel without a CTA barrier in its loop (bf16 N = 7..12).
 //
 // step_tma4_kernel synchronises the whole CTA twice per tile: a give-up
 // decision after the wait, and a barrier after every thread has read the
