@@ -3,6 +3,7 @@
 // make_master's fills and copies, checkpoint copies and the ZeRO-3 gather.
 
 #include <algorithm>
+#include <utility>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -493,12 +494,28 @@ __device__ __forceinline__ void gather_shift_body(const uint16_t* __restrict__ s
   }
 }
 
+// Gathers are launched with programmatic stream serialization: a gather's
+// CTAs may become resident while the kernel before it on the stream (the
+// step, or the previous unit's gather) is still finishing, and wait here —
+// griddepcontrol.wait returns once every prerequisite grid has completed and
+// its memory operations are visible — before their first load.  So a gather
+// reads only what an ordinary launch would; what it gains is that its CTAs
+// start the moment the previous kernel ends instead of being launched then
+// (ten per-unit gathers of the Llama-2048 units at N = 8: 6,285 -> 6,714
+// GB/s).  Each CTA then lets the next gather's CTAs be scheduled.
+__device__ __forceinline__ void gather_prologue() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __global__ void gather_vec_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n16) {
+  gather_prologue();
   gather_vec_body(src, dst, n16, static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
 }
 
 __global__ void gather_shift_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, long long n,
                                     int head, int phi, long long nvec) {
+  gather_prologue();
   gather_shift_body(src, dst, n, head, phi, nvec, static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
 }
 
@@ -509,6 +526,7 @@ __global__ void gather_shift_kernel(const uint16_t* __restrict__ src, uint16_t* 
 // the vector body, the others the shifted one.  One launch instead of one per unit spares the
 // ramp and drain between consecutive copies.
 __global__ void __launch_bounds__(kStepThreads) gather_units_kernel(const __grid_constant__ GatherBatch b) {
+  gather_prologue();
   const long long blk = blockIdx.x;
   int lo = 0, hi = b.count - 1;  // the last unit with cta_begin <= blk
   while (lo < hi) {
@@ -692,6 +710,24 @@ cudaError_t launch_copy_f32(const float* src, float* dst, long long n, cudaStrea
 
 namespace {
 
+// A gather launch with programmatic stream serialization (see
+// gather_prologue): kStepThreads-thread CTAs, no dynamic shared memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_gather_kernel(void (*kernel)(KArgs...), long long grid, cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kStepThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // How one unit is copied: the vector body when source and destination are
 // 16-byte aligned and the unit is whole vectors, else the shifted body.
 GatherUnit plan_gather(const uint16_t* src, uint16_t* dst, long long n) {
@@ -724,14 +760,10 @@ cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaS
   const GatherUnit g = plan_gather(src, dst, n);
   // one thread per vector: under 2^31 blocks for any unit a device can hold
   const long long grid = (g.threads + kStepThreads - 1) / kStepThreads;
-  if (!g.shifted) {
-    gather_vec_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(
-        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), g.nvec);
-  } else {
-    gather_shift_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(src, dst, n, g.head, g.phi,
-                                                                                   g.nvec);
-  }
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e =
+      !g.shifted ? launch_gather_kernel(gather_vec_kernel, grid, stream, reinterpret_cast<const uint4*>(src),
+                                        reinterpret_cast<uint4*>(dst), g.nvec)
+                 : launch_gather_kernel(gather_shift_kernel, grid, stream, src, dst, n, g.head, g.phi, g.nvec);
   if (e == cudaSuccess) ++*launches;
   return e;
 }
@@ -742,8 +774,7 @@ cudaError_t launch_gather_units(const uint16_t* const* src, uint16_t* const* dst
   auto flush = [&]() -> cudaError_t {
     if (b.count == 0) return cudaSuccess;
     const long long grid = b.cta_begin[b.count];
-    gather_units_kernel<<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(b);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_gather_kernel(gather_units_kernel, grid, stream, b);
     if (e == cudaSuccess) ++*launches;
     b = GatherBatch{};
     return e;
