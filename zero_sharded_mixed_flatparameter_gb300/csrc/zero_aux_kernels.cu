@@ -16,6 +16,42 @@ namespace zfs {
 namespace {
 
 // ---------------------------------------------------------------------------
+// Overlapped launches.  The norm pass, its finalize and the ZeRO-3 gathers
+// are launched with programmatic stream serialization: their CTAs may become
+// resident while the kernel before them on the stream is still finishing,
+// and wait in await_previous_grid() — griddepcontrol.wait returns once every
+// prerequisite grid has completed and its memory operations are visible —
+// before their first load.  So such a kernel reads only what an ordinary
+// launch would; what it gains is that its CTAs start the moment the previous
+// kernel ends instead of being launched then.  Each CTA then lets the next
+// kernel's CTAs be scheduled.  Measured on GB300: ten per-unit gathers of the
+// Llama-2048 units at N = 8 6,285 -> 6,714 GB/s; the clip call (norm pass +
+// finalize) over 73.4 M elements at N = 8 bf16 6,640 -> 6,721 GB/s of
+// gradient reads, 268 M at N = 2 fp32 7,075 -> 7,142.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void await_previous_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), long long grid, int threads, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Global gradient norm.
 // ---------------------------------------------------------------------------
 // Squares are accumulated per thread as an unevaluated fp32 pair (hi, lo):
@@ -240,6 +276,7 @@ __device__ __noinline__ double exact_thread_sum(const NormArgs& a, const NormSeg
 template <int N, bool kFp32, bool kShifted>
 __global__ void __launch_bounds__(kStepThreads, kShifted ? 1 : NormShape<N, kFp32>::kMinBlocks)
     grad_sq_kernel(const __grid_constant__ NormArgs a) {
+  await_previous_grid();
   constexpr bool kPairs = NormShape<N, kFp32>::kPairs;
   __shared__ double smem[kStepThreads / 32];
   const long long b = blockIdx.x;
@@ -298,6 +335,7 @@ __global__ void __launch_bounds__(kStepThreads, kShifted ? 1 : NormShape<N, kFp3
 }
 
 __global__ void __launch_bounds__(kFinalizeThreads) clip_finalize_kernel(char* ws, long long n, float max_norm) {
+  await_previous_grid();
   __shared__ double smem[kFinalizeThreads / 32];
   const double* partials = reinterpret_cast<const double*>(ws + kClipHeaderBytes);
   double d = 0.0;
@@ -494,28 +532,15 @@ __device__ __forceinline__ void gather_shift_body(const uint16_t* __restrict__ s
   }
 }
 
-// Gathers are launched with programmatic stream serialization: a gather's
-// CTAs may become resident while the kernel before it on the stream (the
-// step, or the previous unit's gather) is still finishing, and wait here —
-// griddepcontrol.wait returns once every prerequisite grid has completed and
-// its memory operations are visible — before their first load.  So a gather
-// reads only what an ordinary launch would; what it gains is that its CTAs
-// start the moment the previous kernel ends instead of being launched then
-// (ten per-unit gathers of the Llama-2048 units at N = 8: 6,285 -> 6,714
-// GB/s).  Each CTA then lets the next gather's CTAs be scheduled.
-__device__ __forceinline__ void gather_prologue() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
+// The gathers are overlapped launches (see await_previous_grid).
 __global__ void gather_vec_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n16) {
-  gather_prologue();
+  await_previous_grid();
   gather_vec_body(src, dst, n16, static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
 }
 
 __global__ void gather_shift_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, long long n,
                                     int head, int phi, long long nvec) {
-  gather_prologue();
+  await_previous_grid();
   gather_shift_body(src, dst, n, head, phi, nvec, static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
 }
 
@@ -526,7 +551,7 @@ __global__ void gather_shift_kernel(const uint16_t* __restrict__ src, uint16_t* 
 // the vector body, the others the shifted one.  One launch instead of one per unit spares the
 // ramp and drain between consecutive copies.
 __global__ void __launch_bounds__(kStepThreads) gather_units_kernel(const __grid_constant__ GatherBatch b) {
-  gather_prologue();
+  await_previous_grid();
   const long long blk = blockIdx.x;
   int lo = 0, hi = b.count - 1;  // the last unit with cta_begin <= blk
   while (lo < hi) {
@@ -656,13 +681,12 @@ cudaError_t launch_grad_sq(const NormArgs& a, long long chunks, bool shifted, cu
   NormKernel k = shifted ? (a.grad_fp32 ? norm_kernel_for<true, true>(a.n_ranks) : norm_kernel_for<false, true>(a.n_ranks))
                          : (a.grad_fp32 ? norm_kernel_for<true, false>(a.n_ranks) : norm_kernel_for<false, false>(a.n_ranks));
   if (!k) return cudaErrorInvalidValue;
-  k<<<static_cast<unsigned>(chunks), kStepThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_overlapped(k, chunks, kStepThreads, stream, a);
 }
 
 cudaError_t launch_clip_finalize(void* workspace, long long n_partials, float max_norm, cudaStream_t stream) {
-  clip_finalize_kernel<<<1, kFinalizeThreads, 0, stream>>>(static_cast<char*>(workspace), n_partials, max_norm);
-  return cudaGetLastError();
+  return launch_overlapped(clip_finalize_kernel, 1, kFinalizeThreads, stream, static_cast<char*>(workspace),
+                           n_partials, max_norm);
 }
 
 cudaError_t launch_accumulate(const AccumArgs& a, bool vec, cudaStream_t stream) {
@@ -710,24 +734,6 @@ cudaError_t launch_copy_f32(const float* src, float* dst, long long n, cudaStrea
 
 namespace {
 
-// A gather launch with programmatic stream serialization (see
-// gather_prologue): kStepThreads-thread CTAs, no dynamic shared memory.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_gather_kernel(void (*kernel)(KArgs...), long long grid, cudaStream_t stream, Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kStepThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-  return e != cudaSuccess ? e : cudaGetLastError();
-}
-
 // How one unit is copied: the vector body when source and destination are
 // 16-byte aligned and the unit is whole vectors, else the shifted body.
 GatherUnit plan_gather(const uint16_t* src, uint16_t* dst, long long n) {
@@ -761,9 +767,10 @@ cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, long long n, cudaS
   // one thread per vector: under 2^31 blocks for any unit a device can hold
   const long long grid = (g.threads + kStepThreads - 1) / kStepThreads;
   const cudaError_t e =
-      !g.shifted ? launch_gather_kernel(gather_vec_kernel, grid, stream, reinterpret_cast<const uint4*>(src),
-                                        reinterpret_cast<uint4*>(dst), g.nvec)
-                 : launch_gather_kernel(gather_shift_kernel, grid, stream, src, dst, n, g.head, g.phi, g.nvec);
+      !g.shifted ? launch_overlapped(gather_vec_kernel, grid, kStepThreads, stream, reinterpret_cast<const uint4*>(src),
+                                     reinterpret_cast<uint4*>(dst), g.nvec)
+                 : launch_overlapped(gather_shift_kernel, grid, kStepThreads, stream, src, dst, n, g.head, g.phi,
+                                     g.nvec);
   if (e == cudaSuccess) ++*launches;
   return e;
 }
@@ -774,7 +781,7 @@ cudaError_t launch_gather_units(const uint16_t* const* src, uint16_t* const* dst
   auto flush = [&]() -> cudaError_t {
     if (b.count == 0) return cudaSuccess;
     const long long grid = b.cta_begin[b.count];
-    const cudaError_t e = launch_gather_kernel(gather_units_kernel, grid, stream, b);
+    const cudaError_t e = launch_overlapped(gather_units_kernel, grid, kStepThreads, stream, b);
     if (e == cudaSuccess) ++*launches;
     b = GatherBatch{};
     return e;
