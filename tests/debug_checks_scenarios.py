@@ -48,6 +48,8 @@ def main():
              mode="separate")
     scenario("tile-staged N = 4 bf16 (512-thread CTAs)", make_problem(big, 4, 2, steps=1, seed=220), mode="all")
     scenario("pipelined tile-staged N = 10 bf16", make_problem(big, 10, 3, steps=1, seed=224), mode="separate")
+    scenario("shifted gradients over 2^23 elements, N = 3 bf16 (unaligned unit bases, one buffer per unit)",
+             make_problem(big, 3, 2, steps=2, seed=226), mode="separate")
     scenario("clipped N = 8", make_problem(odd, 8, 2, steps=2, seed=214, max_norm=0.05))
     scenario("clipped, reduced gradient kept", make_problem(odd, 8, 1, steps=2, seed=215, max_norm=0.05),
              clip_keep=True)

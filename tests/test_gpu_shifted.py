@@ -77,6 +77,40 @@ def test_every_head_and_offset(gd, n):
     _run(pb, offsets)
 
 
+# units summing to more than 2^23 elements (the size from which aligned
+# launches take the tile-staged kernels): every head and offset at a size
+# where many waves of the grid pass over each segment
+LARGE = [3_000_001, 5, 2_500_003, 4099, 3_100_007, 17]
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+def test_large_every_head_and_offset(n):
+    assert sum(LARGE) >= 1 << 23
+    pl = si.from_units(LARGE)
+    pb = make_problem(pl, n, 0 if n == 1 else 2, steps=2, seed=320 + n)
+    offsets = [[(r * 3 + u) % 8 for u in range(8)] for r in range(n)]
+    _run(pb, offsets)
+
+
+def test_large_clipped_adamw_capturable():
+    pl = si.from_units(LARGE)
+    pb = make_problem(pl, 3, 3, steps=3, seed=325, max_norm=0.05, adamw=True, weight_decay=0.1)
+    ref = oracle_run(pb)
+    fs = gpu_flatstep(pb)
+    try:
+        fs.enable_capturable(max_steps=8)
+        for t in range(1, 4):
+            keep = []
+            _register_offsets(fs, upload_grads(pb, t), [3, 0, 5], keep)
+            fs.clip_grad_norm(pb.max_norm)
+            fs.step()
+            fs.post_step()
+        torch.cuda.synchronize()
+        compare_state(fs, ref, "large shifted layout, clipped AdamW, capturable")
+    finally:
+        fs.close()
+
+
 @pytest.mark.parametrize("gd", ["bf16", "fp32"])
 def test_aligned_gradients_with_unaligned_bases(gd):
     # separate 16-byte-aligned buffers per unit while the unit bases are not
