@@ -1,5 +1,5 @@
-"""Host allocation failure inside the library (SURVEY-style injected host
-fault, no GPU): the library allocates no device memory, so the failure is
+"""Host allocation failure inside the library (an injected host fault, no
+GPU): the library allocates no device memory, so the failure is
 made on its host metadata — a child process limits its address space
 (RLIMIT_AS) just before zero_plan builds the tables of a 4 M-unit layout.
 The call must return ZERO_ENOMEM and no context, and the same call must
