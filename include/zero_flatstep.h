@@ -19,7 +19,12 @@
  *    threads (see the ZeRO-Offload calls).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Device work is enqueued on it asynchronously; the caller keeps
- *    every buffer alive until that work has completed on the stream.
+ *    every buffer alive until that work has completed on the stream.  The
+ *    ZeRO-3 gathers and the clip norm pass are launched with programmatic
+ *    stream serialization: their thread blocks may become resident while the
+ *    kernel before them on the stream finishes, but each waits for that
+ *    kernel to complete (and its writes to be visible) before it reads
+ *    anything, so the stream's ordering is the usual one.
  *  - Every call returns a zero_status; nothing crosses the ABI as an
  *    exception.  A call that fails leaves the context unchanged.  The text of
  *    the last error is available from zero_last_error().
