@@ -621,9 +621,12 @@ def e2e_leg(wb: Workbench, steps: int, warm: int, world: int) -> dict:
     """The same steps through the public API with HOST buffers: every step
     copies its N replica gradients from pinned host memory and reads the
     updated bf16 parameters back.  The host link (not HBM) bounds this, so the
-    copies are pipelined: step k+1's gradients travel on a copy stream into
-    the second of two device buffer sets while step k runs and its parameters
-    are read back on the compute stream."""
+    copies are pipelined on three streams: step k+1's gradients travel on a
+    copy stream into the second of two device buffer sets while step k runs
+    on the compute stream, which then copies the parameters into one of two
+    device staging buffers (a device-to-device copy) that a third stream
+    reads back to the host, so that a slow read-back holds up neither the
+    next step nor the next gradients."""
     import torch
     device, stream, padded = wb.device, wb.stream, wb.padded
     host_grads = []
@@ -633,12 +636,19 @@ def e2e_leg(wb: Workbench, steps: int, warm: int, world: int) -> dict:
         host_grads.append(h)
     host_out = torch.empty(padded, dtype=torch.bfloat16, pin_memory=True)
     bufs = [wb.grads, [torch.empty_like(g) for g in wb.grads]]
+    staging = [torch.empty_like(wb.fs.param16) for _ in range(2)]
     copy_stream = torch.cuda.Stream(device)
+    d2h_stream = torch.cuda.Stream(device)
     h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
     step_done = [torch.cuda.Event(), torch.cuda.Event()]
+    staged = [torch.cuda.Event(), torch.cuda.Event()]
+    d2h_done = [torch.cuda.Event(), torch.cuda.Event()]
 
     def run(k_steps):
+        start = torch.cuda.Event()
+        start.record(stream)
         with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(start)  # after everything before the run on the compute stream
             for hg, g in zip(host_grads, bufs[0]):
                 g.copy_(hg, non_blocking=True)
             h2d_done[0].record(copy_stream)
@@ -654,7 +664,16 @@ def e2e_leg(wb: Workbench, steps: int, warm: int, world: int) -> dict:
             stream.wait_event(h2d_done[cur])
             wb.one_step(grads=bufs[cur])
             step_done[cur].record(stream)
-            host_out.copy_(wb.fs.param16, non_blocking=True)
+            if k >= 2:
+                stream.wait_event(d2h_done[cur])  # staging[cur]'s previous read-back
+            with torch.cuda.stream(stream):
+                staging[cur].copy_(wb.fs.param16, non_blocking=True)
+            staged[cur].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(staged[cur])
+                host_out.copy_(staging[cur], non_blocking=True)
+                d2h_done[cur].record(d2h_stream)
+        stream.wait_event(d2h_done[(k_steps - 1) % 2])  # the last read-back ends the run
 
     run(warm)
     torch.cuda.synchronize(device)
@@ -672,7 +691,8 @@ def e2e_leg(wb: Workbench, steps: int, warm: int, world: int) -> dict:
     return {"value": params_all / (e2e_ms / 1e3), "unit": UNIT,
             "h2d_bytes_per_step": wb.wl["n"] * padded * esz, "d2h_bytes_per_step": padded * 2,
             "ms_per_step": e2e_ms / steps,
-            "pipelining": "double-buffered: step k+1's H2D overlaps step k and its D2H"}
+            "pipelining": "three streams: step k+1's H2D overlaps step k; each step's parameters are "
+                          "copied on the device into one of two staging buffers and read back from there"}
 
 
 def run_ours(args):
